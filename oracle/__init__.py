@@ -1,0 +1,42 @@
+"""CPU oracle for the wave-index hot path -- TEST INFRASTRUCTURE ONLY.
+
+A plain, slow, double-precision (numpy float64) statement of what the path
+computes, written from the RetroInfer summaries (wave index: tripartite
+attention approximation, accuracy-bounded estimation, segmented spherical
+k-means).  It exists to check the CUDA path; it is not part of the product.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import or call anything in this package.  It shares no code with the
+CUDA path (``clustered_sparse_kv_gb300``) and neither imports the other; the
+only common module is the seeded input generator ``kvsynth``.
+
+Parity status per function (what pins it is in ``tests/test_oracle_pins.py``):
+  bf16_round          pinned (torch's float32->bfloat16 cast; hand values)
+  assign / update     pinned (exhaustive argmax; planted clusters; objective)
+  build_unit_index    pinned (conservation invariants; singleton clusters)
+  decode_unit         pinned (all-clusters = textbook softmax attention;
+                              singleton clusters exact; Jensen bound; cosh
+                              closed form; explicit per-token loop)
+  lse_merge           pinned (associativity against the single sum)
+Approximation quality against full attention on synthetic data: parity
+unpinned (the summaries claim accuracy only on RULER / Needle-in-a-Haystack
+with trained models).
+"""
+from .bf16 import bf16_round, bf16_from_bits, bf16_to_bits, fp32_round  # noqa: F401
+from .wave_index import (  # noqa: F401
+    IndexParams,
+    steady_positions,
+    indexed_positions,
+    budget_k,
+    init_centroids,
+    assign,
+    update,
+    spherical_kmeans,
+    build_unit_index,
+    build_index,
+    select_topk,
+    zone_partial,
+    lse_merge,
+    decode_unit,
+    decode,
+)

@@ -1,0 +1,365 @@
+"""Pins of the CPU oracle to facts outside itself (CPU only).
+
+Each test ties an oracle function to mathematics or to an independent
+routine: textbook softmax attention, closed forms of the estimation zone,
+Jensen's inequality, exhaustive search on tiny inputs, torch's bf16 cast,
+conservation laws.  A plausible slip in the oracle (dropped n_j factor, wrong
+centroid in the estimate, off-by-one zone, reversed tie-break, transposed
+operand) fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import kvsynth
+import oracle
+from oracle import IndexParams
+
+D = 128
+LAM = 1.0 / math.sqrt(D)
+
+
+def textbook_attention(q, K, V):
+    """softmax(q K^T / sqrt(d)) V over all rows, written independently of the oracle."""
+    l = (K @ q) / math.sqrt(K.shape[1])
+    w = np.exp(l - l.max())
+    return (w @ V) / w.sum()
+
+
+def bf16_keys(rng, n, d=D, scale=1.0):
+    return oracle.bf16_round(scale * rng.standard_normal((n, d)))
+
+
+def tiny_workload(n, S, Cs, g=1, iters=4, n_sink=4, window=8, budget_k=2, topics=8, seed=5):
+    return kvsynth.get_workload("tiny-8k").with_(
+        n_ctx=n, seg_len=S, clusters_per_seg=Cs, iters=iters, n_sink=n_sink, local_window=window,
+        budget_k=budget_k, n_topics=topics, n_q_heads=g, n_kv_heads=1, seed=seed)
+
+
+def gen_unit(w, step=0):
+    k, v = kvsynth.kv_cache(w)
+    q = kvsynth.queries(w, step=step)
+    K = oracle.bf16_from_bits(k).reshape(w.units, w.n_ctx, D)
+    V = oracle.bf16_from_bits(v).reshape(w.units, w.n_ctx, D)
+    Q = oracle.bf16_from_bits(q).reshape(w.units, w.group, D)
+    return K, V, Q
+
+
+def params_of(w):
+    return IndexParams(seg_len=w.seg_len, clusters_per_seg=w.clusters_per_seg, iters=w.iters, n_sink=w.n_sink,
+                       local_window=w.local_window, budget_frac=w.budget_frac, budget_k=w.budget_k)
+
+
+# ------------------------------------------------------------------ bf16 ----
+
+def test_bf16_round_matches_torch_cast():
+    rng = np.random.default_rng(0)
+    x32 = (rng.standard_normal(200000) * np.exp(rng.uniform(-20, 20, 200000))).astype(np.float32)
+    ref = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle.bf16_round(x32.astype(np.float64)), ref)
+
+
+def test_bf16_round_hand_values():
+    # ulp of bf16 at 1.0 is 2**-7; halfway cases round to the even significand
+    assert oracle.bf16_round(1 + 2.0 ** -8) == 1.0
+    assert oracle.bf16_round(1 + 3 * 2.0 ** -8) == 1 + 2.0 ** -6
+    assert oracle.bf16_round(1 + 2.0 ** -8 + 2.0 ** -30) == 1 + 2.0 ** -7
+    assert oracle.bf16_round(-3.0) == -3.0
+    bits = oracle.bf16_to_bits(np.array([1.0, -2.0, 0.5]))
+    assert list(bits) == [0x3F80, 0xC000, 0x3F00]
+    np.testing.assert_array_equal(oracle.bf16_from_bits(bits), [1.0, -2.0, 0.5])
+
+
+def test_generator_rounding_agrees_with_oracle_rounding():
+    rng = np.random.default_rng(1)
+    xs = rng.standard_normal(2000) * 10
+    for x in xs:
+        assert oracle.bf16_from_bits(np.uint16(kvsynth.bf16_bits(x))) == oracle.bf16_round(x)
+
+
+def test_generator_splitmix_published_value():
+    # SplitMix64 seeded with 0: first output 0xE220A8397B1DCDAF (Steele et al. reference sequence)
+    assert kvsynth.draw(0, 0) == 0xE220A8397B1DCDAF
+
+
+# ---------------------------------------------------------- P1 all = full ----
+
+@pytest.mark.parametrize("g", [1, 4])
+def test_all_clusters_selected_is_full_attention(g):
+    w = tiny_workload(n=512, S=128, Cs=8, g=g, budget_k=10 ** 6)
+    K, V, Q = gen_unit(w)
+    p = params_of(w)
+    idx = oracle.build_index(K, V, p)
+    o = oracle.decode(Q, K, V, idx, p, g)
+    for h in range(g):
+        np.testing.assert_allclose(o[0, h], textbook_attention(Q[0, h], K[0], V[0]), rtol=0, atol=1e-12)
+
+
+def test_all_clusters_selected_with_appended_tokens():
+    w = tiny_workload(n=512, S=128, Cs=8, budget_k=10 ** 6)
+    K, V, Q = gen_unit(w)
+    ka, va = kvsynth.kv_cache(w, p0=512, p1=517)
+    KA = oracle.bf16_from_bits(ka).reshape(1, 5, D)
+    VA = oracle.bf16_from_bits(va).reshape(1, 5, D)
+    p = params_of(w)
+    idx = oracle.build_index(K, V, p)
+    o = oracle.decode(Q, K, V, idx, p, 1, k_app=KA, v_app=VA)
+    ref = textbook_attention(Q[0, 0], np.concatenate([K[0], KA[0]]), np.concatenate([V[0], VA[0]]))
+    np.testing.assert_allclose(o[0, 0], ref, rtol=0, atol=1e-12)
+
+
+# ----------------------------------------------------- P2 singletons exact ----
+
+@pytest.mark.parametrize("k", [1, 3, 7])
+def test_singleton_clusters_make_estimation_exact(k):
+    rng = np.random.default_rng(2)
+    n, S = 64, 32
+    K = bf16_keys(rng, n)[None]
+    V = bf16_keys(rng, n)[None]
+    q = bf16_keys(rng, 1, scale=0.5)
+    p = IndexParams(seg_len=S, clusters_per_seg=S, iters=3, n_sink=2, local_window=4, budget_k=k)
+    idx = oracle.build_index(K, V, p)
+    c = idx[0]["counts"]
+    # every clustered token sits alone; steady seeds leave their cluster empty
+    assert set(np.unique(c)) <= {0, 1}
+    assert c.sum() == n - 6
+    o = oracle.decode(q[None], K, V, idx, p, 1)
+    np.testing.assert_allclose(o[0, 0], textbook_attention(q[0], K[0], V[0]), rtol=0, atol=1e-12)
+
+
+# -------------------------------------------------------- P3 Jensen bound ----
+
+def test_estimate_is_jensen_lower_bound_per_cluster():
+    w = tiny_workload(n=1024, S=256, Cs=16, g=4, budget_k=3)
+    K, V, Q = gen_unit(w)
+    p = params_of(w)
+    idx = oracle.build_index(K, V, p)[0]
+    a = idx["assignment"]
+    d_est_total = d_exact_total = 0.0
+    for h in range(4):
+        q = Q[0, h]
+        for j in np.nonzero(idx["counts"] > 0)[0]:
+            members = K[0][a == j]
+            exact = np.exp(LAM * members @ q).sum()
+            est = idx["counts"][j] * np.exp(LAM * idx["mu"][j] @ q)
+            mean = members.mean(axis=0)
+            slack = math.exp(LAM * np.linalg.norm(q) * np.linalg.norm(idx["mu"][j] - mean))
+            assert est <= exact * slack * (1 + 1e-12)
+            # with the exact mean the inequality holds without slack
+            assert len(members) * np.exp(LAM * mean @ q) <= exact * (1 + 1e-12)
+            d_est_total += est / slack
+            d_exact_total += exact
+    assert d_est_total <= d_exact_total
+
+
+# ------------------------------------------------- P4 cosh closed form ----
+
+def test_two_token_cluster_estimate_closed_form():
+    """Cluster B = {mu + delta, mu - delta}, estimated: its exact share over its
+    estimated share is cosh(lam q.delta), and the output is the closed form."""
+    rng = np.random.default_rng(3)
+    d = 4
+    lam = 1 / math.sqrt(d)
+    # rows: 0 sink | 1, 2 cluster A (retrieved) | 3, 4 cluster B (estimated) | 5 window
+    muB = np.array([0.5, -0.25, 1.0, 0.75])
+    delta = np.array([0.25, 0.5, -0.125, 0.0])
+    K = np.stack([[1.0, 0, 0, 0], [2.0, 2.0, 2.0, 1.0], [2.0, 1.0, 2.0, 2.0], muB + delta, muB - delta,
+                  [0, 1.0, 0, 0]])
+    V = rng.standard_normal((6, d))
+    q = np.array([0.5, 1.0, 0.25, -0.5])
+    idx = {"assignment": np.array([-1, 0, 0, 1, 1, -1]), "counts": np.array([2, 2]),
+           "mu": np.array([(K[1] + K[2]) / 2, muB]), "valsum": np.array([V[1] + V[2], V[3] + V[4]])}
+    assert idx["mu"][0] @ q > muB @ q
+    p = IndexParams(seg_len=6, clusters_per_seg=2, n_sink=1, local_window=1, budget_k=1)
+    o = oracle.decode_unit(q[None], K, V, idx, p)[0]
+    exact_rows = [0, 1, 2, 5]
+    l = lam * K[exact_rows] @ q
+    eB = lam * muB @ q
+    N = np.exp(l) @ V[exact_rows] + math.exp(eB) * (V[3] + V[4])
+    Dn = np.exp(l).sum() + 2 * math.exp(eB)
+    np.testing.assert_allclose(o, N / Dn, rtol=1e-13, atol=0)
+    exact_B = math.exp(lam * K[3] @ q) + math.exp(lam * K[4] @ q)
+    np.testing.assert_allclose(exact_B / (2 * math.exp(eB)), math.cosh(lam * q @ delta), rtol=1e-14)
+
+
+# ----------------------------------------------------- P5 brute force ----
+
+def brute_assign(k_idx, c):
+    out = []
+    for i in range(k_idx.shape[0]):
+        best, bj = -math.inf, -1
+        for j in range(c.shape[0]):
+            s = sum(float(k_idx[i, e]) * float(c[j, e]) for e in range(k_idx.shape[1]))
+            if s > best:          # strict: the first (lowest) j keeps a tie
+                best, bj = s, j
+        out.append(bj)
+    return np.array(out)
+
+
+def brute_decode(q, K, V, idx, n_sink, window, k):
+    n, d = K.shape
+    lam = 1 / math.sqrt(d)
+    counts, mu, vs, a = idx["counts"], idx["mu"], idx["valsum"], idx["assignment"]
+    ids = [j for j in range(len(counts)) if counts[j] > 0]
+    scored = sorted(ids, key=lambda j: (-float(mu[j] @ q), j))
+    R = set(scored[:min(k, len(ids))])
+    num = np.zeros(d)
+    den = 0.0
+    for i in range(n):
+        if i < n_sink or i >= n - window or a[i] in R:
+            wgt = math.exp(lam * sum(q[e] * K[i, e] for e in range(d)))
+            den += wgt
+            num += wgt * V[i]
+    for j in ids:
+        if j not in R:
+            wgt = math.exp(lam * float(mu[j] @ q))
+            den += counts[j] * wgt
+            num += wgt * vs[j]
+    return num / den, sorted(R)
+
+
+def test_brute_force_tiny():
+    rng = np.random.default_rng(4)
+    n, S, Cs, d = 96, 32, 4, 16
+    K = oracle.bf16_round(rng.standard_normal((n, d)) + np.repeat(rng.standard_normal((12, d)) * 2, 8, axis=0))
+    V = oracle.bf16_round(rng.standard_normal((n, d)))
+    q = oracle.bf16_round(rng.standard_normal(d))
+    p = IndexParams(seg_len=S, clusters_per_seg=Cs, iters=3, n_sink=4, local_window=8, budget_k=3)
+    idx = oracle.build_unit_index(K, V, p)
+    # assignment of each segment's last iteration against exhaustive search
+    steady = np.zeros(n, bool)
+    steady[oracle.steady_positions(n, p)] = True
+    for s in range(n // S):
+        seg = np.arange(s * S, (s + 1) * S)
+        loc = np.nonzero(~steady[seg])[0]
+        c_last = idx["histories"][s][-1]
+        np.testing.assert_array_equal(idx["assignment"][seg[loc]] - s * Cs, brute_assign(K[seg[loc]], c_last))
+    o, info = oracle.decode_unit(q[None], K, V, idx, p, details=True)
+    ob, Rb = brute_decode(q, K, V, idx, 4, 8, 3)
+    np.testing.assert_array_equal(info[0]["selected"], Rb)
+    np.testing.assert_allclose(o[0], ob, rtol=1e-12, atol=1e-14)
+
+
+# ----------------------------------------------------- P6 k-means sanity ----
+
+def test_planted_clusters_recovered():
+    rng = np.random.default_rng(6)
+    S, Cs, d = 256, 16, D
+    dirs = rng.standard_normal((Cs, d))
+    dirs /= np.linalg.norm(dirs, axis=1, keepdims=True)
+    label = np.arange(S) // (S // Cs)          # seed 16*j lands in planted cluster j
+    K = oracle.bf16_round(10 * dirs[label] + 0.05 * rng.standard_normal((S, d)))
+    p = IndexParams(seg_len=S, clusters_per_seg=Cs, iters=5, n_sink=0, local_window=0)
+    a, _ = oracle.spherical_kmeans(K, np.arange(S), p)
+    np.testing.assert_array_equal(a, label)
+
+
+def test_kmeans_objective_non_decreasing():
+    w = tiny_workload(n=2048, S=2048, Cs=64, iters=8)
+    K, V, _ = gen_unit(w)
+    p = params_of(w)
+    steady = oracle.steady_positions(w.n_ctx, p)
+    loc = np.setdiff1d(np.arange(w.n_ctx), steady)
+    khat = K[0][loc] / np.linalg.norm(K[0][loc], axis=1, keepdims=True)
+    _, hist = oracle.spherical_kmeans(K[0], loc, p)
+    objs = []
+    for c in hist:
+        a = oracle.assign(K[0][loc], c)
+        objs.append(float((khat * c[a]).sum()))
+    # exact arithmetic gives a non-decreasing objective; bf16 centroids add
+    # at most about 2**-8 relative per cluster
+    for t in range(1, len(objs)):
+        assert objs[t] >= objs[t - 1] - 4e-3 * abs(objs[t - 1]) / math.sqrt(len(loc))
+    assert objs[-1] > objs[0]
+
+
+def test_segments_are_clustered_independently():
+    w = tiny_workload(n=1024, S=512, Cs=16)
+    K, V, _ = gen_unit(w)
+    p = params_of(w)
+    a1 = oracle.build_unit_index(K[0], V[0], p)["assignment"]
+    K2 = K[0].copy()
+    K2[600:900] = oracle.bf16_round(K2[600:900] * -1.5)
+    a2 = oracle.build_unit_index(K2, V[0], p)["assignment"]
+    np.testing.assert_array_equal(a1[:512], a2[:512])
+
+
+# ----------------------------------------------------- P7 conservation ----
+
+def test_index_conservation():
+    w = tiny_workload(n=4096, S=1024, Cs=64, g=1)
+    K, V, _ = gen_unit(w)
+    p = params_of(w)
+    idx = oracle.build_unit_index(K[0], V[0], p)
+    n = w.n_ctx
+    I = oracle.indexed_positions(n, p)
+    c = idx["counts"]
+    assert c.sum() == I.size
+    np.testing.assert_array_equal(np.sort(idx["perm"]), I)            # bijection on I
+    np.testing.assert_array_equal(idx["offsets"], p.n_sink + np.concatenate([[0], np.cumsum(c)]))
+    np.testing.assert_allclose(idx["valsum"].sum(0), V[0][I].sum(0), rtol=0, atol=1e-4)
+    for j in np.nonzero(c)[0]:
+        rows = idx["perm"][idx["offsets"][j] - p.n_sink: idx["offsets"][j + 1] - p.n_sink]
+        seg = j // p.clusters_per_seg
+        assert np.all(rows // p.seg_len == seg)                        # cluster inside its segment
+        assert np.all(np.diff(rows) > 0)                                # position order inside a cluster
+        assert np.all(idx["assignment"][rows] == j)
+        np.testing.assert_array_equal(idx["mu"][j], oracle.bf16_round(K[0][rows].mean(0)))
+        np.testing.assert_array_equal(idx["valsum"][j], oracle.fp32_round(V[0][rows].sum(0)))
+    # cluster-contiguous slots: slot offsets of segment s start at the segment start
+    for s in range(1, n // p.seg_len):
+        assert idx["offsets"][s * p.clusters_per_seg] == s * p.seg_len
+
+
+# ------------------------------------------------------- P8 LSE merge ----
+
+def test_lse_merge_associative():
+    rng = np.random.default_rng(8)
+    n = 300
+    K = bf16_keys(rng, n, scale=2.0)
+    V = bf16_keys(rng, n)
+    q = bf16_keys(rng, 1)[0]
+    single = textbook_attention(q, K, V)
+    for trial in range(5):
+        cuts = np.sort(rng.choice(np.arange(1, n), size=trial + 1, replace=False))
+        parts = [oracle.zone_partial(q, K[a:b], V[a:b], LAM) for a, b in zip([0, *cuts], [*cuts, n])]
+        parts.append(oracle.zone_partial(q, K[:0], V[:0], LAM))        # an empty chunk
+        np.testing.assert_allclose(oracle.lse_merge(parts), single, rtol=0, atol=1e-13)
+
+
+# ------------------------------------------------------------- P9 ties ----
+
+def test_ties_go_to_lowest_id():
+    rng = np.random.default_rng(9)
+    c = oracle.bf16_round(rng.standard_normal((6, D)))
+    c[4] = c[1]                                    # duplicated centroid
+    k = np.stack([c[1] * 3, c[4] * 2, c[0]])
+    a = oracle.assign(k, c)
+    assert a[0] == 1 and a[1] == 1 and a[2] == 0
+    scores = np.array([1.0, 5.0, 5.0, 2.0, 5.0, 0.5])
+    ne = np.array([True, True, True, True, True, False])
+    np.testing.assert_array_equal(oracle.select_topk(scores, ne, 2), [1, 2])
+    np.testing.assert_array_equal(oracle.select_topk(scores, ne, 4), [1, 2, 3, 4])
+    # empty clusters are never selected, and k is capped at the non-empty count
+    np.testing.assert_array_equal(oracle.select_topk(scores, ne, 10), [0, 1, 2, 3, 4])
+
+
+def test_budget_matches_configured_counts():
+    p = IndexParams()
+    assert oracle.budget_k(512, p) == 10
+    assert oracle.budget_k(8192, p) == 148
+    assert oracle.budget_k(7680, p) == 139
+    assert oracle.budget_k(65536, p) == 1180
+    assert oracle.budget_k(16384, p) == 295
+
+
+def test_steady_zone_partition():
+    p = IndexParams(n_sink=4, local_window=64)
+    n = 8192
+    s = oracle.steady_positions(n, p)
+    i = oracle.indexed_positions(n, p)
+    assert s.size == 68 and i.size == n - 68
+    assert np.intersect1d(s, i).size == 0
+    np.testing.assert_array_equal(np.sort(np.concatenate([s, i])), np.arange(n))
