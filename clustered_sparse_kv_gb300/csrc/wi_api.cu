@@ -1,0 +1,587 @@
+// wi_api.cu -- the C ABI (include/wave_index.h): argument checks, ownership,
+// allocation and the order of the kernels of a build and of a decode step.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "wave_index.h"
+#include "wi_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+#define WI_CUDA(call)                                                                          \
+  do {                                                                                         \
+    cudaError_t e_ = (call);                                                                   \
+    if (e_ != cudaSuccess) return fail(WI_ECUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+int env_int(const char* name, int dflt) {
+  const char* s = getenv(name);
+  if (!s || !*s) return dflt;
+  return atoi(s);
+}
+
+}  // namespace
+
+struct wi_index {
+  wi_config cfg;
+  WiGeom g;
+  int device = 0;
+  void* K = nullptr;
+  void* V = nullptr;
+  // index
+  void* mu = nullptr;
+  float* valsum = nullptr;
+  int* cnt = nullptr;
+  int* off = nullptr;
+  int* perm = nullptr;
+  int* nonempty = nullptr;
+  void* appK = nullptr;
+  void* appV = nullptr;
+  int* app_count = nullptr;
+  int appended = 0;
+  // decode scratch
+  WiDecodeBufs b{};
+  int* err = nullptr;
+  // host-buffer variant staging
+  void* q_dev = nullptr;
+  void* kn_dev = nullptr;
+  void* vn_dev = nullptr;
+  float* out_dev = nullptr;
+  cudaStream_t last_stream = nullptr;
+  std::vector<void*> allocs;
+  // decode profiling
+  std::vector<cudaEvent_t> prof_ev;  // (WI_DECODE_KERNELS + 1) per slot
+  int prof_slots = 0;
+  long long prof_steps = 0;
+};
+
+int wi_geom_from_config(const wi_config* c, WiGeom* g, char* msg, size_t msglen) {
+#define BAD(...)                          \
+  do {                                    \
+    snprintf(msg, msglen, __VA_ARGS__);   \
+    return WI_EINVAL;                     \
+  } while (0)
+  if (!c) BAD("config is NULL");
+  if (c->batch < 1 || c->layers < 1 || c->n_q_heads < 1 || c->n_kv_heads < 1)
+    BAD("batch, layers, n_q_heads, n_kv_heads must be >= 1");
+  if (c->n_q_heads % c->n_kv_heads) BAD("n_q_heads (%d) is not a multiple of n_kv_heads (%d)", c->n_q_heads,
+                                        c->n_kv_heads);
+  if (c->head_dim != 128) BAD("head_dim must be 128 (got %d)", c->head_dim);
+  if (c->seg_len < 128 || c->seg_len % 128) BAD("seg_len must be a positive multiple of 128 (got %d)", c->seg_len);
+  if (c->n_ctx < c->seg_len || c->n_ctx % c->seg_len) BAD("n_ctx (%lld) must be a positive multiple of seg_len",
+                                                          c->n_ctx);
+  if (c->clusters_per_seg < 16 || c->clusters_per_seg > 512 || c->clusters_per_seg % 16 ||
+      c->seg_len % c->clusters_per_seg)
+    BAD("clusters_per_seg must be a multiple of 16 in [16, 512] dividing seg_len (got %d)", c->clusters_per_seg);
+  if (c->iters < 1) BAD("iters must be >= 1");
+  if (c->n_sink < 0 || c->local_window < 0 || c->n_sink + c->local_window < 1 ||
+      c->n_sink + c->local_window >= c->n_ctx)
+    BAD("need 1 <= n_sink + local_window < n_ctx");
+  if (c->max_append < 0) BAD("max_append must be >= 0");
+  if (c->n_ctx + c->max_append >= (1LL << 24)) BAD("n_ctx + max_append must be < 2^24");
+  for (int i = 0; i < 3; ++i)
+    if (c->reserved[i]) BAD("reserved fields must be zero");
+  g->U = c->batch * c->layers * c->n_kv_heads;
+  g->G = c->n_q_heads / c->n_kv_heads;
+  g->S = c->seg_len;
+  g->Cs = c->clusters_per_seg;
+  g->nseg = (int)(c->n_ctx / c->seg_len);
+  if ((long long)g->nseg * g->Cs >= (1LL << 30)) BAD("too many clusters per unit");
+  g->C = g->nseg * g->Cs;
+  g->n = c->n_ctx;
+  g->n_sink = c->n_sink;
+  g->W = c->local_window;
+  g->n_idx = (int)(c->n_ctx - c->n_sink - c->local_window);
+  g->iters = c->iters;
+  g->max_append = c->max_append;
+  long long k = c->budget_k > 0 ? c->budget_k : (long long)std::ceil(c->budget_frac * (double)g->C);
+  if (k < 1 || k > g->C) BAD("retrieval budget k = %lld must be in [1, C = %d]", k, g->C);
+  g->kmax = (int)k;
+  if (g->G > 8) {
+    snprintf(msg, msglen, "query heads per kv head must be <= 8 (got %d)", g->G);
+    return WI_EUNSUPPORTED;
+  }
+  if (g->S > 16384) {
+    snprintf(msg, msglen, "seg_len must be <= 16384 (got %d)", g->S);
+    return WI_EUNSUPPORTED;
+  }
+  return WI_OK;
+#undef BAD
+}
+
+namespace {
+
+int alloc(wi_index* ix, void** p, size_t bytes) {
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(WI_ENOMEM, "cudaMalloc(%zu bytes) failed: %s", bytes, cudaGetErrorString(e));
+  }
+  ix->allocs.push_back(*p);
+  return WI_OK;
+}
+
+void destroy(wi_index* ix) {
+  if (!ix) return;
+  for (cudaEvent_t e : ix->prof_ev) cudaEventDestroy(e);
+  for (void* p : ix->allocs) cudaFree(p);
+  delete ix;
+}
+
+// Index storage, decode scratch and staging.
+int alloc_index(wi_index* ix, cudaStream_t st) {
+  const WiGeom& g = ix->g;
+  const size_t U = g.U, C = g.C, G = g.G;
+  int rc;
+#define A(ptr, bytes)                                                              \
+  if ((rc = alloc(ix, reinterpret_cast<void**>(&(ptr)), (bytes))) != WI_OK) return rc
+  A(ix->mu, U * C * 128 * 2);
+  A(ix->valsum, U * C * 128 * 4);
+  A(ix->cnt, U * C * 4);
+  A(ix->off, U * (C + 1) * 4);
+  A(ix->perm, U * (size_t)g.n_idx * 4);
+  A(ix->nonempty, U * 4);
+  const size_t app = (size_t)(g.max_append > 0 ? g.max_append : 1);
+  A(ix->appK, U * app * 128 * 2);
+  A(ix->appV, U * app * 128 * 2);
+  A(ix->app_count, 4);
+  A(ix->err, 4);
+  WiDecodeBufs& b = ix->b;
+  b.chunk = env_int("WI_D1_CHUNK", 256);
+  if (b.chunk < 32) b.chunk = 32;
+  b.nchunk = (int)((C + b.chunk - 1) / b.chunk);
+  int ns = env_int("WI_D3_SPLITS", 0);
+  if (ns <= 0) {
+    ns = (int)((4 * 152 + U - 1) / U);
+    if (ns > 64) ns = 64;
+    if (ns < 1) ns = 1;
+  }
+  b.nsplit = ns;
+  b.rows_cap = g.n + app;
+  A(b.scores, U * G * C * 4);
+  A(b.part1, U * G * (size_t)b.nchunk * WI_PART * 4);
+  A(b.sel, U * G * (size_t)g.kmax * 4);
+  A(b.selcnt, U * G * 4);
+  A(b.rows, U * (size_t)b.rows_cap * 4);
+  A(b.rcount, U * 4);
+  A(b.rows_total, 8);
+  A(b.part3, U * G * (size_t)b.nsplit * WI_PART * 4);
+  A(ix->q_dev, U * G * 128 * 2);
+  A(ix->out_dev, U * G * 128 * 4);
+  A(ix->kn_dev, U * 128 * 2);
+  A(ix->vn_dev, U * 128 * 2);
+#undef A
+  b.mu = ix->mu;
+  b.valsum = ix->valsum;
+  b.cnt = ix->cnt;
+  b.off = ix->off;
+  b.nonempty = ix->nonempty;
+  b.K = ix->K;
+  b.V = ix->V;
+  b.appK = ix->appK;
+  b.appV = ix->appV;
+  b.app_count = ix->app_count;
+  b.err = ix->err;
+  WI_CUDA(cudaMemsetAsync(ix->app_count, 0, 4, st));
+  WI_CUDA(cudaMemsetAsync(ix->err, 0, 4, st));
+  WI_CUDA(cudaMemsetAsync(b.selcnt, 0, U * G * 4, st));
+  WI_CUDA(cudaMemsetAsync(b.rcount, 0, U * 4, st));
+  WI_CUDA(cudaMemsetAsync(b.rows_total, 0, 8, st));
+  return WI_OK;
+}
+
+int new_index(const wi_config* cfg, void* k, void* v, wi_index** out, wi_index** ixp) {
+  if (!out) return fail(WI_EINVAL, "out is NULL");
+  *out = nullptr;
+  WiGeom g;
+  int rc = wi_geom_from_config(cfg, &g, g_err, sizeof(g_err));
+  if (rc != WI_OK) return rc;
+  if (!k || !v) return fail(WI_EINVAL, "k and v must be non-NULL device pointers");
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
+    return fail(WI_EINVAL, "k and v must be 16-byte aligned");
+  wi_index* ix = new (std::nothrow) wi_index();
+  if (!ix) return fail(WI_ENOMEM, "host allocation failed");
+  ix->cfg = *cfg;
+  ix->g = g;
+  ix->K = k;
+  ix->V = v;
+  cudaGetDevice(&ix->device);
+  *ixp = ix;
+  return WI_OK;
+}
+
+// Permute the clustered rows of K, V by ix->perm, through bounded scratch.
+int permute_kv(wi_index* ix, cudaStream_t st) {
+  const WiGeom& g = ix->g;
+  if (g.n_idx == 0) return WI_OK;
+  const size_t per_unit = (size_t)g.n_idx * 128 * 2;
+  const size_t cap = (size_t)1 << 30;
+  int nb = (int)(cap / per_unit);
+  if (nb < 1) nb = 1;
+  if (nb > g.U) nb = g.U;
+  void *tK = nullptr, *tV = nullptr;
+  if (cudaMallocAsync(&tK, per_unit * nb, st) != cudaSuccess ||
+      cudaMallocAsync(&tV, per_unit * nb, st) != cudaSuccess) {
+    cudaGetLastError();
+    if (tK) cudaFreeAsync(tK, st);
+    return fail(WI_ENOMEM, "permutation scratch (%zu bytes) allocation failed", 2 * per_unit * nb);
+  }
+  cudaError_t e = cudaSuccess;
+  for (int u0 = 0; u0 < g.U && e == cudaSuccess; u0 += nb) {
+    const int nu = (g.U - u0) < nb ? (g.U - u0) : nb;
+    e = wi_launch_permute(g, ix->K, ix->V, ix->perm, tK, tV, u0, nu, st);
+  }
+  cudaFreeAsync(tK, st);
+  cudaFreeAsync(tV, st);
+  if (e != cudaSuccess) return fail(WI_ECUDA, "permutation: %s", cudaGetErrorString(e));
+  return WI_OK;
+}
+
+struct BuildScratch {
+  void* chat = nullptr;
+  int32_t* assign = nullptr;
+  float* invnorm = nullptr;
+  int* seg_counts = nullptr;
+  int* seg_offsets = nullptr;
+  int* slots = nullptr;
+};
+
+int scratch_alloc(const WiGeom& g, BuildScratch* s, cudaStream_t st) {
+  const size_t SU = (size_t)g.U * g.nseg;
+  const size_t rows = (size_t)g.U * g.n;
+  cudaError_t e = cudaSuccess;
+  e = cudaMallocAsync(&s->chat, SU * g.Cs * 128 * 2, st);
+  if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&s->assign), rows * 4, st);
+  if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&s->invnorm), rows * 4, st);
+  if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&s->seg_counts), SU * g.Cs * 4, st);
+  if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&s->seg_offsets), SU * (g.Cs + 1) * 4, st);
+  if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&s->slots), SU * g.S * 4, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(WI_ENOMEM, "build scratch allocation failed: %s", cudaGetErrorString(e));
+  }
+  return WI_OK;
+}
+
+void scratch_free(BuildScratch* s, cudaStream_t st) {
+  void* ps[] = {s->chat, s->assign, s->invnorm, s->seg_counts, s->seg_offsets, s->slots};
+  for (void* p : ps)
+    if (p) cudaFreeAsync(p, st);
+}
+
+#define WI_LAUNCH(call)                                                                             \
+  do {                                                                                              \
+    cudaError_t e_ = (call);                                                                        \
+    if (e_ != cudaSuccess) {                                                                        \
+      rc = fail(WI_ECUDA, "%s: %s", #call, cudaGetErrorString(e_));                                 \
+      goto done;                                                                                    \
+    }                                                                                               \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* wi_last_error(void) { return g_err; }
+
+int wi_build_index(const wi_config* cfg, void* k, void* v, const void* init_centroids, void* stream,
+                   wi_index** out) {
+  g_err[0] = 0;
+  wi_index* ix = nullptr;
+  int rc = new_index(cfg, k, v, out, &ix);
+  if (rc != WI_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ix->last_stream = st;
+  const WiGeom& g = ix->g;
+  BuildScratch s;
+  if ((rc = alloc_index(ix, st)) != WI_OK || (rc = scratch_alloc(g, &s, st)) != WI_OK) {
+    scratch_free(&s, st);
+    destroy(ix);
+    return rc;
+  }
+  WI_LAUNCH(wi_launch_invnorm(k, s.invnorm, (long long)g.U * g.n, st));
+  if (init_centroids)
+    WI_LAUNCH(cudaMemcpyAsync(s.chat, init_centroids, (size_t)g.U * g.nseg * g.Cs * 128 * 2, cudaMemcpyDefault, st));
+  else
+    WI_LAUNCH(wi_launch_init_centroids(g, k, s.chat, st));
+  for (int t = 0; t < g.iters; ++t) {
+    WI_LAUNCH(wi_launch_assign(g, k, s.chat, s.assign, ix->err, st));
+    WI_LAUNCH(wi_launch_segment_sort(g, s.assign, s.seg_counts, s.seg_offsets, s.slots, ix->err, st));
+    if (t + 1 < g.iters)
+      WI_LAUNCH(wi_launch_centroid_update(g, k, s.invnorm, s.seg_counts, s.seg_offsets, s.slots, s.chat, st));
+  }
+  WI_LAUNCH(wi_launch_final_reduce(g, k, v, s.seg_counts, s.seg_offsets, s.slots, ix->mu, ix->valsum, ix->cnt,
+                                   ix->off, ix->perm, ix->nonempty, st));
+  scratch_free(&s, st);
+  s = BuildScratch();
+  if ((rc = permute_kv(ix, st)) != WI_OK) goto done;
+  *out = ix;
+  return WI_OK;
+done:
+  scratch_free(&s, st);
+  cudaStreamSynchronize(st);
+  destroy(ix);
+  return rc;
+}
+
+int wi_index_import(const wi_config* cfg, void* k, void* v, const int32_t* counts, const int32_t* perm,
+                    const uint16_t* mu, const float* valsum, void* stream, wi_index** out) {
+  g_err[0] = 0;
+  wi_index* ix = nullptr;
+  int rc = new_index(cfg, k, v, out, &ix);
+  if (rc != WI_OK) return rc;
+  if (!counts || !perm || !mu || !valsum) {
+    destroy(ix);
+    return fail(WI_EINVAL, "counts, perm, mu and valsum must be non-NULL");
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ix->last_stream = st;
+  const WiGeom& g = ix->g;
+  const size_t U = g.U, C = g.C;
+  std::vector<int32_t> hc(U * C), hp(U * (size_t)g.n_idx), hoff(U * (C + 1)), hne(U, 0);
+  std::vector<unsigned char> seen;
+  if (cudaMemcpy(hc.data(), counts, hc.size() * 4, cudaMemcpyDefault) != cudaSuccess ||
+      cudaMemcpy(hp.data(), perm, hp.size() * 4, cudaMemcpyDefault) != cudaSuccess) {
+    cudaGetLastError();
+    destroy(ix);
+    return fail(WI_EINVAL, "counts / perm are not readable (host or device memory expected)");
+  }
+  for (size_t u = 0; u < U; ++u) {
+    long long run = g.n_sink;
+    seen.assign((size_t)g.n, 0);
+    for (size_t c = 0; c < C; ++c) {
+      const int m = hc[u * C + c];
+      if (m < 0) { destroy(ix); return fail(WI_EINVAL, "negative count (unit %zu, cluster %zu)", u, c); }
+      hoff[u * (C + 1) + c] = (int)run;
+      const int s = (int)(c / g.Cs);
+      for (int t = 0; t < m; ++t) {
+        const long long slot = run + t - g.n_sink;
+        if (slot >= g.n_idx) { destroy(ix); return fail(WI_EINVAL, "counts exceed the clustered tokens (unit %zu)", u); }
+        const long long p = hp[u * g.n_idx + slot];
+        if (p < g.n_sink || p >= g.n - g.W || p / g.S != s || seen[p]) {
+          destroy(ix);
+          return fail(WI_EINVAL, "perm is not a bijection on the clustered positions of each segment (unit %zu)", u);
+        }
+        seen[p] = 1;
+      }
+      run += m;
+      if (m > 0) hne[u]++;
+    }
+    if (run != g.n - g.W) { destroy(ix); return fail(WI_EINVAL, "counts of unit %zu do not cover the clustered tokens", u); }
+    hoff[u * (C + 1) + C] = (int)run;
+  }
+  if ((rc = alloc_index(ix, st)) != WI_OK) { destroy(ix); return rc; }
+  WI_LAUNCH(cudaMemcpyAsync(ix->cnt, hc.data(), hc.size() * 4, cudaMemcpyHostToDevice, st));
+  WI_LAUNCH(cudaMemcpyAsync(ix->perm, hp.data(), hp.size() * 4, cudaMemcpyHostToDevice, st));
+  WI_LAUNCH(cudaMemcpyAsync(ix->off, hoff.data(), hoff.size() * 4, cudaMemcpyHostToDevice, st));
+  WI_LAUNCH(cudaMemcpyAsync(ix->nonempty, hne.data(), hne.size() * 4, cudaMemcpyHostToDevice, st));
+  WI_LAUNCH(cudaMemcpyAsync(ix->mu, mu, U * C * 128 * 2, cudaMemcpyDefault, st));
+  WI_LAUNCH(cudaMemcpyAsync(ix->valsum, valsum, U * C * 128 * 4, cudaMemcpyDefault, st));
+  if ((rc = permute_kv(ix, st)) != WI_OK) goto done;
+  // the host vectors above are pageable: finish the copies before they go away
+  WI_LAUNCH(cudaStreamSynchronize(st));
+  *out = ix;
+  return WI_OK;
+done:
+  cudaStreamSynchronize(st);
+  destroy(ix);
+  return rc;
+}
+
+int wi_index_export(const wi_index* ix, int32_t* counts, int32_t* offsets, int32_t* perm, uint16_t* mu,
+                    float* valsum, void* stream) {
+  g_err[0] = 0;
+  if (!ix) return fail(WI_EINVAL, "index is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WiGeom& g = ix->g;
+  const size_t U = g.U, C = g.C;
+  if (counts) WI_CUDA(cudaMemcpyAsync(counts, ix->cnt, U * C * 4, cudaMemcpyDefault, st));
+  if (offsets) WI_CUDA(cudaMemcpyAsync(offsets, ix->off, U * (C + 1) * 4, cudaMemcpyDefault, st));
+  if (perm) WI_CUDA(cudaMemcpyAsync(perm, ix->perm, U * (size_t)g.n_idx * 4, cudaMemcpyDefault, st));
+  if (mu) WI_CUDA(cudaMemcpyAsync(mu, ix->mu, U * C * 128 * 2, cudaMemcpyDefault, st));
+  if (valsum) WI_CUDA(cudaMemcpyAsync(valsum, ix->valsum, U * C * 128 * 4, cudaMemcpyDefault, st));
+  return WI_OK;
+}
+
+int wi_decode_step(wi_index* ix, const void* q, const void* k_new, const void* v_new, float* out, void* stream) {
+  g_err[0] = 0;
+  if (!ix || !q || !out) return fail(WI_EINVAL, "index, q and out must be non-NULL");
+  if ((k_new == nullptr) != (v_new == nullptr)) return fail(WI_EINVAL, "k_new and v_new must both be set or both NULL");
+  if (k_new && ix->appended >= ix->g.max_append)
+    return fail(WI_EFULL, "append buffer full (%d tokens)", ix->g.max_append);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ix->last_stream = st;
+  const cudaEvent_t* ev = nullptr;
+  if (ix->prof_slots > 0) {
+    ev = ix->prof_ev.data() + (size_t)(ix->prof_steps % ix->prof_slots) * (WI_DECODE_KERNELS + 1);
+    ix->prof_steps++;
+  }
+  cudaError_t e = wi_launch_decode(ix->g, ix->b, q, out, st, ev);
+  if (e != cudaSuccess) return fail(WI_ECUDA, "decode launch: %s", cudaGetErrorString(e));
+  if (k_new) {
+    e = wi_launch_append(ix->g, ix->b, k_new, v_new, ix->appended, st);
+    if (e != cudaSuccess) return fail(WI_ECUDA, "append launch: %s", cudaGetErrorString(e));
+    ix->appended++;
+  }
+  return WI_OK;
+}
+
+int wi_decode_step_host(wi_index* ix, const void* q_host, const void* k_new_host, const void* v_new_host,
+                        float* out_host, void* stream) {
+  g_err[0] = 0;
+  if (!ix || !q_host || !out_host) return fail(WI_EINVAL, "index, q and out must be non-NULL");
+  if ((k_new_host == nullptr) != (v_new_host == nullptr))
+    return fail(WI_EINVAL, "k_new and v_new must both be set or both NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WiGeom& g = ix->g;
+  const size_t qb = (size_t)g.U * g.G * 128 * 2, kb = (size_t)g.U * 128 * 2, ob = (size_t)g.U * g.G * 128 * 4;
+  WI_CUDA(cudaMemcpyAsync(ix->q_dev, q_host, qb, cudaMemcpyHostToDevice, st));
+  if (k_new_host) {
+    WI_CUDA(cudaMemcpyAsync(ix->kn_dev, k_new_host, kb, cudaMemcpyHostToDevice, st));
+    WI_CUDA(cudaMemcpyAsync(ix->vn_dev, v_new_host, kb, cudaMemcpyHostToDevice, st));
+  }
+  int rc = wi_decode_step(ix, ix->q_dev, k_new_host ? ix->kn_dev : nullptr, k_new_host ? ix->vn_dev : nullptr,
+                          ix->out_dev, stream);
+  if (rc != WI_OK) return rc;
+  WI_CUDA(cudaMemcpyAsync(out_host, ix->out_dev, ob, cudaMemcpyDeviceToHost, st));
+  WI_CUDA(cudaStreamSynchronize(st));
+  return WI_OK;
+}
+
+int wi_last_selection(const wi_index* ix, int32_t* ids, int32_t* counts, void* stream) {
+  g_err[0] = 0;
+  if (!ix || !ids) return fail(WI_EINVAL, "index and ids must be non-NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const WiGeom& g = ix->g;
+  WI_CUDA(cudaMemcpyAsync(ids, ix->b.sel, (size_t)g.U * g.G * g.kmax * 4, cudaMemcpyDefault, st));
+  if (counts) WI_CUDA(cudaMemcpyAsync(counts, ix->b.selcnt, (size_t)g.U * g.G * 4, cudaMemcpyDefault, st));
+  return WI_OK;
+}
+
+int wi_index_shape(const wi_index* ix, int* units, int* clusters, int* k_max, int* group, int* appended) {
+  g_err[0] = 0;
+  if (!ix) return fail(WI_EINVAL, "index is NULL");
+  if (units) *units = ix->g.U;
+  if (clusters) *clusters = ix->g.C;
+  if (k_max) *k_max = ix->g.kmax;
+  if (group) *group = ix->g.G;
+  if (appended) *appended = ix->appended;
+  return WI_OK;
+}
+
+int wi_kmeans_step(const wi_config* cfg, const void* k, const void* centroids, int32_t* assign, void* new_centroids,
+                   void* stream) {
+  g_err[0] = 0;
+  WiGeom g;
+  int rc = wi_geom_from_config(cfg, &g, g_err, sizeof(g_err));
+  if (rc != WI_OK) return rc;
+  if (!k || !centroids || !assign || !new_centroids)
+    return fail(WI_EINVAL, "k, centroids, assign and new_centroids must be non-NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  BuildScratch s;
+  int* err = nullptr;
+  if ((rc = scratch_alloc(g, &s, st)) != WI_OK) {
+    scratch_free(&s, st);
+    return rc;
+  }
+  if (cudaMallocAsync(reinterpret_cast<void**>(&err), 4, st) != cudaSuccess) {
+    cudaGetLastError();
+    scratch_free(&s, st);
+    return fail(WI_ENOMEM, "allocation failed");
+  }
+  const size_t cb = (size_t)g.U * g.nseg * g.Cs * 128 * 2;
+  WI_LAUNCH(cudaMemsetAsync(err, 0, 4, st));
+  WI_LAUNCH(wi_launch_invnorm(k, s.invnorm, (long long)g.U * g.n, st));
+  WI_LAUNCH(cudaMemcpyAsync(s.chat, centroids, cb, cudaMemcpyDeviceToDevice, st));
+  WI_LAUNCH(wi_launch_assign(g, k, s.chat, assign, err, st));
+  WI_LAUNCH(wi_launch_segment_sort(g, assign, s.seg_counts, s.seg_offsets, s.slots, err, st));
+  WI_LAUNCH(wi_launch_centroid_update(g, k, s.invnorm, s.seg_counts, s.seg_offsets, s.slots, s.chat, st));
+  WI_LAUNCH(cudaMemcpyAsync(new_centroids, s.chat, cb, cudaMemcpyDeviceToDevice, st));
+  {
+    int herr = 0;
+    WI_LAUNCH(cudaMemcpyAsync(&herr, err, 4, cudaMemcpyDeviceToHost, st));
+    WI_LAUNCH(cudaStreamSynchronize(st));
+    if (herr) rc = fail(WI_EDEVICE, "device invariant violated (flags 0x%x)", herr);
+  }
+done:
+  scratch_free(&s, st);
+  if (err) cudaFreeAsync(err, st);
+  return rc;
+}
+
+int wi_profile_begin(wi_index* ix, int max_steps) {
+  g_err[0] = 0;
+  if (!ix || max_steps < 0) return fail(WI_EINVAL, "index is NULL or max_steps < 0");
+  for (cudaEvent_t e : ix->prof_ev) cudaEventDestroy(e);
+  ix->prof_ev.clear();
+  ix->prof_slots = 0;
+  ix->prof_steps = 0;
+  const size_t n = (size_t)max_steps * (WI_DECODE_KERNELS + 1);
+  for (size_t i = 0; i < n; ++i) {
+    cudaEvent_t e;
+    WI_CUDA(cudaEventCreate(&e));
+    ix->prof_ev.push_back(e);
+  }
+  ix->prof_slots = max_steps;
+  return WI_OK;
+}
+
+int wi_profile_read(wi_index* ix, double* kernel_ms, int* steps, unsigned long long* exact_rows) {
+  g_err[0] = 0;
+  if (!ix) return fail(WI_EINVAL, "index is NULL");
+  WI_CUDA(cudaDeviceSynchronize());
+  const int filled = (int)(ix->prof_steps < ix->prof_slots ? ix->prof_steps : ix->prof_slots);
+  if (kernel_ms) {
+    for (int k = 0; k < WI_DECODE_KERNELS; ++k) kernel_ms[k] = 0.0;
+    for (int sl = 0; sl < filled; ++sl) {
+      const cudaEvent_t* ev = ix->prof_ev.data() + (size_t)sl * (WI_DECODE_KERNELS + 1);
+      for (int k = 0; k < WI_DECODE_KERNELS; ++k) {
+        float ms = 0.f;
+        WI_CUDA(cudaEventElapsedTime(&ms, ev[k], ev[k + 1]));
+        kernel_ms[k] += ms;
+      }
+    }
+  }
+  if (steps) *steps = filled;
+  if (exact_rows) WI_CUDA(cudaMemcpy(exact_rows, ix->b.rows_total, 8, cudaMemcpyDeviceToHost));
+  return WI_OK;
+}
+
+int wi_check_device(wi_index* ix) {
+  g_err[0] = 0;
+  if (!ix) return fail(WI_EINVAL, "index is NULL");
+  WI_CUDA(cudaStreamSynchronize(ix->last_stream));
+  int herr = 0;
+  WI_CUDA(cudaMemcpy(&herr, ix->err, 4, cudaMemcpyDeviceToHost));
+  if (herr) {
+    WI_CUDA(cudaMemset(ix->err, 0, 4));
+    return fail(WI_EDEVICE, "device invariant violated (flags 0x%x)", herr);
+  }
+  return WI_OK;
+}
+
+void wi_free(wi_index* ix) {
+  if (!ix) return;
+  cudaDeviceSynchronize();
+  destroy(ix);
+}
+
+}  // extern "C"

@@ -1,0 +1,411 @@
+// wi_build.cu -- index build (prefill): segmented spherical k-means and the
+// cluster-contiguous index.
+//
+// RetroInfer summaries de/fr/zh 2.A: segmented clustering cuts the context
+// into segments that are clustered independently; fr 2.A.2 names spherical
+// k-means; zh 2.A names the precomputed per-cluster value sum that the
+// estimation zone reads.  Kernels here:
+//   invnorm          1/|K_i| per token (fp32)
+//   init_centroids   c_j = bf16(K_p / |K_p|), p = segment start + stride * j
+//   assign (SIMT)    a_i = argmax_j K_i . c_j, ties to the lowest j
+//   segment_sort     counting sort of a segment's tokens by (cluster, position)
+//   centroid_update  c_j = bf16(u_j / |u_j|), u_j = sum of member K_i / |K_i|
+//   final_reduce     counts, row offsets, perm, mu_j = bf16(mean K), valsum_j
+//   permute          in-place cluster-contiguous reorder of K and V rows
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "wi_common.cuh"
+#include "wi_internal.h"
+
+namespace {
+
+__device__ __forceinline__ bool is_steady(long long p, long long n, int n_sink, int W) {
+  return p < n_sink || p >= n - W;
+}
+
+// Row of the first slot of segment s: n_sink + clustered positions before s.
+__device__ __forceinline__ long long seg_slot_base(int s, int S, long long n, int n_sink, int W) {
+  const long long a = (long long)s * S;
+  const long long steady_before = (a < n_sink ? a : n_sink) + (a > n - W ? a - (n - W) : 0);
+  return n_sink + a - steady_before;
+}
+
+__global__ void k_invnorm(const bf16* __restrict__ K, float* __restrict__ invnorm, long long rows) {
+  const int lane = threadIdx.x & 31;
+  const long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  float x[4];
+  load_bf16x4(K + r * WI_D + 4 * lane, x);
+  const float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
+  if (lane == 0) invnorm[r] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+}
+
+__global__ void k_init_centroids(const bf16* __restrict__ K, bf16* __restrict__ chat, int total, int nseg, int S,
+                                 int Cs, long long n) {
+  const int lane = threadIdx.x & 31;
+  const int gid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (gid >= total) return;
+  const int u = gid / (nseg * Cs), s = (gid / Cs) % nseg, j = gid % Cs;
+  const long long row = (long long)u * n + (long long)s * S + (long long)j * (S / Cs);
+  float x[4];
+  load_bf16x4(K + row * WI_D + 4 * lane, x);
+  const float nrm = sqrtf(warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]));
+  bf16* o = chat + (size_t)gid * WI_D + 4 * lane;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) o[e] = __float2bfloat16_rn(nrm > 0.f ? x[e] / nrm : 0.f);
+}
+
+// SIMT assignment: a CTA scores 32 tokens of one segment against all of the
+// segment's centroids (fp32 FMA over e = 0..127 in order), then takes the
+// row argmax.  Shared memory: centroids as 32-bit words in rows padded to 65
+// words (conflict-free per-thread row reads), tokens fp32 [32][128], scores
+// fp32 [32][Cs].
+constexpr int kAsgTok = 32;
+constexpr int kAsgRowWords = WI_D / 2 + 1;
+
+__global__ void __launch_bounds__(256) k_assign_simt(const bf16* __restrict__ K, const bf16* __restrict__ chat,
+                                                     int32_t* __restrict__ assign, int S, int Cs, int nseg,
+                                                     long long n, int n_sink, int W, int* err) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  uint32_t* cw = reinterpret_cast<uint32_t*>(smem_raw);                  // [Cs][65]
+  float* tok = reinterpret_cast<float*>(cw + (size_t)Cs * kAsgRowWords);  // [32][128]
+  float* sc = tok + kAsgTok * WI_D;                                       // [32][Cs]
+  const int u = blockIdx.z, s = blockIdx.y, tile = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t* cg = reinterpret_cast<const uint32_t*>(chat + ((size_t)u * nseg + s) * Cs * WI_D);
+  for (int i = tid; i < Cs * (WI_D / 2); i += blockDim.x) {
+    const int j = i / (WI_D / 2), w = i % (WI_D / 2);
+    cw[j * kAsgRowWords + w] = __ldg(cg + i);
+  }
+  const long long p0 = (long long)s * S + (long long)tile * kAsgTok;
+  const bf16* kt = K + ((long long)u * n + p0) * WI_D;
+  for (int i = tid; i < kAsgTok * WI_D; i += blockDim.x) tok[i] = __bfloat162float(kt[i]);
+  __syncthreads();
+  for (int j = tid; j < Cs; j += blockDim.x) {
+    float acc[kAsgTok];
+#pragma unroll
+    for (int i = 0; i < kAsgTok; ++i) acc[i] = 0.f;
+    const uint32_t* row = cw + j * kAsgRowWords;
+    for (int w = 0; w < WI_D / 2; ++w) {
+      const uint32_t cv = row[w];
+      const float c0 = bf16_lo(cv), c1 = bf16_hi(cv);
+#pragma unroll
+      for (int i = 0; i < kAsgTok; ++i) {
+        const float2 t = *reinterpret_cast<const float2*>(tok + i * WI_D + 2 * w);
+        acc[i] = fmaf(t.x, c0, acc[i]);
+        acc[i] = fmaf(t.y, c1, acc[i]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kAsgTok; ++i) sc[i * Cs + j] = acc[i];
+  }
+  __syncthreads();
+  for (int i = warp; i < kAsgTok; i += (blockDim.x >> 5)) {
+    float best = -INFINITY;
+    int bj = 0x7fffffff;
+    for (int j = lane; j < Cs; j += 32) {
+      const float v = sc[i * Cs + j];
+      if (v > best) { best = v; bj = j; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+      if (ov > best || (ov == best && oj < bj)) { best = ov; bj = oj; }
+    }
+    if (lane == 0) {
+      const long long p = p0 + i;
+      int a = -1;
+      if (!is_steady(p, n, n_sink, W)) {
+        if (bj < 0 || bj >= Cs) { atomicOr(err, WI_DEVERR_BAD_CLUSTER); bj = 0; }
+        a = s * Cs + bj;
+      }
+      assign[(long long)u * n + p] = a;
+    }
+  }
+}
+
+// Counting sort of one segment's clustered tokens by (cluster, position).
+// Outputs per segment-unit: counts [Cs], offsets [Cs+1] (local slots),
+// slots [S] (position relative to the segment start, in slot order).
+__global__ void __launch_bounds__(512) k_segment_sort(const int32_t* __restrict__ assign,
+                                                      int* __restrict__ seg_counts, int* __restrict__ seg_offsets,
+                                                      int* __restrict__ slots, int S, int Cs, int nseg, long long n,
+                                                      int* err) {
+  extern __shared__ __align__(16) int ss_raw[];
+  int* cnt = ss_raw;          // [Cs]
+  int* off = cnt + Cs;        // [Cs + 1]
+  int* cur = off + Cs + 1;    // [Cs]
+  int* tmp = cur + Cs;        // [32]
+  int* sa = tmp + 32;         // [S]
+  int* sb = sa + S;           // [S]
+  const int su = blockIdx.x, u = su / nseg, s = su % nseg;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int32_t* a = assign + (long long)u * n + (long long)s * S;
+  for (int j = tid; j < Cs; j += blockDim.x) { cnt[j] = 0; cur[j] = 0; }
+  __syncthreads();
+  for (int i = tid; i < S; i += blockDim.x) {
+    const int c = a[i];
+    if (c >= 0) {
+      const int cl = c - s * Cs;
+      if (cl < 0 || cl >= Cs) atomicOr(err, WI_DEVERR_BAD_CLUSTER);
+      else atomicAdd(&cnt[cl], 1);
+    }
+  }
+  __syncthreads();
+  int running = 0;
+  for (int base = 0; base < Cs; base += blockDim.x) {
+    const int j = base + tid;
+    const int v = j < Cs ? cnt[j] : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, tmp, &tot);
+    if (j < Cs) off[j] = running + ex;
+    running += tot;
+  }
+  if (tid == 0) off[Cs] = running;
+  __syncthreads();
+  for (int i = tid; i < S; i += blockDim.x) {
+    const int c = a[i];
+    if (c >= 0) {
+      const int cl = c - s * Cs;
+      if (cl >= 0 && cl < Cs) sa[off[cl] + atomicAdd(&cur[cl], 1)] = i;
+    }
+  }
+  __syncthreads();
+  // order each cluster's slots by position: rank of every member among its cluster
+  for (int cl = warp; cl < Cs; cl += nw) {
+    const int b = off[cl], m = cnt[cl];
+    for (int e = lane; e < m; e += 32) {
+      const int v = sa[b + e];
+      int r = 0;
+      for (int x = 0; x < m; ++x) r += sa[b + x] < v;
+      sb[b + r] = v;
+    }
+  }
+  __syncthreads();
+  const int total = off[Cs];
+  for (int i = tid; i < total; i += blockDim.x) slots[(long long)su * S + i] = sb[i];
+  for (int j = tid; j < Cs; j += blockDim.x) seg_counts[(long long)su * Cs + j] = cnt[j];
+  for (int j = tid; j <= Cs; j += blockDim.x) seg_offsets[(long long)su * (Cs + 1) + j] = off[j];
+}
+
+// One warp per cluster: c_j = bf16(u_j / |u_j|), u_j = sum over members (in
+// position order) of K_i * (1/|K_i|).  Empty clusters keep c_j.
+__global__ void k_centroid_update(const bf16* __restrict__ K, const float* __restrict__ invnorm,
+                                  const int* __restrict__ seg_counts, const int* __restrict__ seg_offsets,
+                                  const int* __restrict__ slots, bf16* __restrict__ chat, int total, int S, int Cs,
+                                  int nseg, long long n) {
+  const int lane = threadIdx.x & 31;
+  const int gid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (gid >= total) return;
+  const int su = gid / Cs, cl = gid % Cs, u = su / nseg, s = su % nseg;
+  const int m = seg_counts[gid];
+  if (m == 0) return;
+  const int b = seg_offsets[(long long)su * (Cs + 1) + cl];
+  const int* sl = slots + (long long)su * S + b;
+  const long long rowbase = (long long)u * n + (long long)s * S;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  int t = 0;
+  for (; t + 4 <= m; t += 4) {
+    long long r[4];
+    uint2 w[4];
+    float iv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = rowbase + sl[t + i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[i] = ldg_u2(K + r[i] * WI_D + 4 * lane);
+      iv[i] = __ldg(invnorm + r[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float x[4];
+      unpack_bf16x4(w[i], x);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] = fmaf(x[e], iv[i], acc[e]);
+    }
+  }
+  for (; t < m; ++t) {
+    const long long r = rowbase + sl[t];
+    float x[4];
+    load_bf16x4(K + r * WI_D + 4 * lane, x);
+    const float iv = __ldg(invnorm + r);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] = fmaf(x[e], iv, acc[e]);
+  }
+  const float nrm = sqrtf(warp_sum(acc[0] * acc[0] + acc[1] * acc[1] + acc[2] * acc[2] + acc[3] * acc[3]));
+  bf16* o = chat + (size_t)gid * WI_D + 4 * lane;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) o[e] = __float2bfloat16_rn(nrm > 0.f ? acc[e] / nrm : 0.f);
+}
+
+// One warp per cluster of the final assignment: count, row offset, perm,
+// mu = bf16(sum K / count), valsum = sum V (fp32), in position order.
+__global__ void k_final_reduce(const bf16* __restrict__ K, const bf16* __restrict__ V,
+                               const int* __restrict__ seg_counts, const int* __restrict__ seg_offsets,
+                               const int* __restrict__ slots, bf16* __restrict__ mu, float* __restrict__ valsum,
+                               int* __restrict__ cnt, int* __restrict__ off, int* __restrict__ perm,
+                               int* __restrict__ nonempty, int U, int C, int S, int Cs, int nseg, long long n,
+                               int n_sink, int W, int n_idx) {
+  const int lane = threadIdx.x & 31;
+  const long long gid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (gid >= (long long)U * C) return;
+  const int u = (int)(gid / C), c = (int)(gid % C), s = c / Cs, cl = c % Cs;
+  const long long su = (long long)u * nseg + s;
+  const int m = seg_counts[su * Cs + cl];
+  const int b = seg_offsets[su * (Cs + 1) + cl];
+  const long long slot0 = seg_slot_base(s, S, n, n_sink, W) + b;
+  if (lane == 0) {
+    off[(long long)u * (C + 1) + c] = (int)slot0;
+    if (c == C - 1) off[(long long)u * (C + 1) + C] = (int)(n - W);
+    cnt[gid] = m;
+    if (m > 0) atomicAdd(&nonempty[u], 1);
+  }
+  const int* sl = slots + su * S + b;
+  const long long rowbase = (long long)u * n;
+  for (int t = lane; t < m; t += 32) perm[(long long)u * n_idx + (slot0 - n_sink) + t] = s * S + sl[t];
+  float ak[4] = {0.f, 0.f, 0.f, 0.f}, av[4] = {0.f, 0.f, 0.f, 0.f};
+  int t = 0;
+  for (; t + 4 <= m; t += 4) {
+    uint2 wk[4], wv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const long long r = rowbase + (long long)s * S + sl[t + i];
+      wk[i] = ldg_u2(K + r * WI_D + 4 * lane);
+      wv[i] = ldg_u2(V + r * WI_D + 4 * lane);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float xk[4], xv[4];
+      unpack_bf16x4(wk[i], xk);
+      unpack_bf16x4(wv[i], xv);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) { ak[e] += xk[e]; av[e] += xv[e]; }
+    }
+  }
+  for (; t < m; ++t) {
+    const long long r = rowbase + (long long)s * S + sl[t];
+    float xk[4], xv[4];
+    load_bf16x4(K + r * WI_D + 4 * lane, xk);
+    load_bf16x4(V + r * WI_D + 4 * lane, xv);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) { ak[e] += xk[e]; av[e] += xv[e]; }
+  }
+  bf16* mo = mu + gid * WI_D + 4 * lane;
+  float4 vo;
+  const float fm = (float)m;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) mo[e] = __float2bfloat16_rn(m > 0 ? ak[e] / fm : 0.f);
+  vo.x = av[0]; vo.y = av[1]; vo.z = av[2]; vo.w = av[3];
+  *reinterpret_cast<float4*>(valsum + gid * WI_D + 4 * lane) = vo;
+}
+
+// Cluster-contiguous reorder, through a scratch copy of units [u0, u0+nu):
+// tmp[r] = rows[perm[r]] for every clustered slot r, then copied back.
+__global__ void k_gather_rows(const bf16* __restrict__ K, const bf16* __restrict__ V, const int* __restrict__ perm,
+                              bf16* __restrict__ tK, bf16* __restrict__ tV, int u0, long long n, int n_idx) {
+  const int lane = threadIdx.x & 31;
+  const long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int u = u0 + blockIdx.y;
+  if (r >= n_idx) return;
+  const long long src = (long long)u * n + perm[(long long)u * n_idx + r];
+  const long long dst = (long long)blockIdx.y * n_idx + r;
+  reinterpret_cast<uint2*>(tK + dst * WI_D)[lane] = ldg_u2(K + src * WI_D + 4 * lane);
+  reinterpret_cast<uint2*>(tV + dst * WI_D)[lane] = ldg_u2(V + src * WI_D + 4 * lane);
+}
+
+__global__ void k_scatter_back(bf16* __restrict__ K, bf16* __restrict__ V, const bf16* __restrict__ tK,
+                               const bf16* __restrict__ tV, int u0, long long n, int n_sink, int n_idx) {
+  const long long words = (long long)n_idx * WI_D / 8;  // 16-byte words per unit
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= words) return;
+  const int u = u0 + blockIdx.y;
+  const uint4* sk = reinterpret_cast<const uint4*>(tK + (long long)blockIdx.y * n_idx * WI_D);
+  const uint4* sv = reinterpret_cast<const uint4*>(tV + (long long)blockIdx.y * n_idx * WI_D);
+  uint4* dk = reinterpret_cast<uint4*>(K + ((long long)u * n + n_sink) * WI_D);
+  uint4* dv = reinterpret_cast<uint4*>(V + ((long long)u * n + n_sink) * WI_D);
+  dk[i] = sk[i];
+  dv[i] = sv[i];
+}
+
+}  // namespace
+
+cudaError_t wi_launch_invnorm(const void* K, float* invnorm, long long rows, cudaStream_t st) {
+  const long long blocks = (rows + 7) / 8;
+  k_invnorm<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const bf16*>(K), invnorm, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t wi_launch_init_centroids(const WiGeom& g, const void* K, void* chat, cudaStream_t st) {
+  const int total = g.U * g.nseg * g.Cs;
+  k_init_centroids<<<(total + 7) / 8, 256, 0, st>>>(static_cast<const bf16*>(K), static_cast<bf16*>(chat), total,
+                                                     g.nseg, g.S, g.Cs, g.n);
+  return cudaGetLastError();
+}
+
+size_t wi_assign_smem_bytes(const WiGeom& g) {
+  return (size_t)g.Cs * kAsgRowWords * 4 + (size_t)kAsgTok * WI_D * 4 + (size_t)kAsgTok * g.Cs * 4;
+}
+
+cudaError_t wi_launch_assign(const WiGeom& g, const void* K, const void* chat, int32_t* assign, int* err,
+                             cudaStream_t st) {
+  if (wi_assign_tc_supported(g)) return wi_launch_assign_tc(g, K, chat, assign, err, st);
+  const size_t smem = wi_assign_smem_bytes(g);
+  static int smem_set = 0;
+  cudaError_t e = wi_ensure_smem(k_assign_simt, smem, &smem_set);
+  if (e != cudaSuccess) return e;
+  dim3 grid(g.S / kAsgTok, g.nseg, g.U);
+  k_assign_simt<<<grid, 256, smem, st>>>(static_cast<const bf16*>(K), static_cast<const bf16*>(chat), assign, g.S,
+                                         g.Cs, g.nseg, g.n, g.n_sink, g.W, err);
+  return cudaGetLastError();
+}
+
+cudaError_t wi_launch_segment_sort(const WiGeom& g, const int32_t* assign, int* seg_counts, int* seg_offsets,
+                                   int* slots, int* err, cudaStream_t st) {
+  const size_t smem = sizeof(int) * ((size_t)3 * g.Cs + 1 + 32 + 2 * (size_t)g.S);
+  static int smem_set = 0;
+  cudaError_t e = wi_ensure_smem(k_segment_sort, smem, &smem_set);
+  if (e != cudaSuccess) return e;
+  k_segment_sort<<<g.U * g.nseg, 512, smem, st>>>(assign, seg_counts, seg_offsets, slots, g.S, g.Cs, g.nseg, g.n,
+                                                   err);
+  return cudaGetLastError();
+}
+
+cudaError_t wi_launch_centroid_update(const WiGeom& g, const void* K, const float* invnorm, const int* seg_counts,
+                                      const int* seg_offsets, const int* slots, void* chat, cudaStream_t st) {
+  const int total = g.U * g.nseg * g.Cs;
+  k_centroid_update<<<(total + 7) / 8, 256, 0, st>>>(static_cast<const bf16*>(K), invnorm, seg_counts, seg_offsets,
+                                                      slots, static_cast<bf16*>(chat), total, g.S, g.Cs, g.nseg,
+                                                      g.n);
+  return cudaGetLastError();
+}
+
+cudaError_t wi_launch_final_reduce(const WiGeom& g, const void* K, const void* V, const int* seg_counts,
+                                   const int* seg_offsets, const int* slots, void* mu, float* valsum, int* cnt,
+                                   int* off, int* perm, int* nonempty, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(nonempty, 0, sizeof(int) * g.U, st);
+  if (e != cudaSuccess) return e;
+  const long long total = (long long)g.U * g.C;
+  k_final_reduce<<<(unsigned)((total + 7) / 8), 256, 0, st>>>(
+      static_cast<const bf16*>(K), static_cast<const bf16*>(V), seg_counts, seg_offsets, slots,
+      static_cast<bf16*>(mu), valsum, cnt, off, perm, nonempty, g.U, g.C, g.S, g.Cs, g.nseg, g.n, g.n_sink, g.W,
+      g.n_idx);
+  return cudaGetLastError();
+}
+
+cudaError_t wi_launch_permute(const WiGeom& g, void* K, void* V, const int* perm, void* tmpK, void* tmpV, int u0,
+                              int nu, cudaStream_t st) {
+  if (g.n_idx == 0 || nu == 0) return cudaSuccess;
+  dim3 g1((unsigned)((g.n_idx + 7) / 8), nu);
+  k_gather_rows<<<g1, 256, 0, st>>>(static_cast<const bf16*>(K), static_cast<const bf16*>(V), perm,
+                                    static_cast<bf16*>(tmpK), static_cast<bf16*>(tmpV), u0, g.n, g.n_idx);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long words = (long long)g.n_idx * WI_D / 8;
+  dim3 g2((unsigned)((words + 255) / 256), nu);
+  k_scatter_back<<<g2, 256, 0, st>>>(static_cast<bf16*>(K), static_cast<bf16*>(V), static_cast<const bf16*>(tmpK),
+                                     static_cast<const bf16*>(tmpV), u0, g.n, g.n_sink, g.n_idx);
+  return cudaGetLastError();
+}

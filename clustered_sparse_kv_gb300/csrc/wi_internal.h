@@ -1,0 +1,77 @@
+// wi_internal.h -- host-side declarations shared by the wave-index sources.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "wave_index.h"
+
+// Geometry of one build / index, derived from wi_config.
+struct WiGeom {
+  int U;          // units = batch * layers * n_kv_heads
+  int G;          // query heads per kv head
+  int S, Cs;      // segment length, clusters per segment
+  int nseg;       // segments per unit
+  int C;          // clusters per unit
+  long long n;    // built tokens per unit
+  int n_sink, W;  // steady zone
+  int n_idx;      // clustered tokens per unit = n - n_sink - W
+  int iters;
+  int kmax;       // retrieval budget
+  int max_append;
+};
+
+int wi_geom_from_config(const wi_config* cfg, WiGeom* g, char* msg, size_t msglen);
+
+// ---- build kernels (wi_build.cu); all enqueue on `st` and return the launch status
+cudaError_t wi_launch_invnorm(const void* K, float* invnorm, long long rows, cudaStream_t st);
+cudaError_t wi_launch_init_centroids(const WiGeom& g, const void* K, void* chat, cudaStream_t st);
+cudaError_t wi_launch_assign(const WiGeom& g, const void* K, const void* chat, int32_t* assign, int* err,
+                             cudaStream_t st);
+cudaError_t wi_launch_segment_sort(const WiGeom& g, const int32_t* assign, int* seg_counts, int* seg_offsets,
+                                   int* slots, int* err, cudaStream_t st);
+cudaError_t wi_launch_centroid_update(const WiGeom& g, const void* K, const float* invnorm, const int* seg_counts,
+                                      const int* seg_offsets, const int* slots, void* chat, cudaStream_t st);
+cudaError_t wi_launch_final_reduce(const WiGeom& g, const void* K, const void* V, const int* seg_counts,
+                                   const int* seg_offsets, const int* slots, void* mu, float* valsum, int* cnt,
+                                   int* off, int* perm, int* nonempty, cudaStream_t st);
+cudaError_t wi_launch_permute(const WiGeom& g, void* K, void* V, const int* perm, void* tmpK, void* tmpV,
+                              int u0, int nu, cudaStream_t st);
+size_t wi_assign_smem_bytes(const WiGeom& g);
+
+// ---- tensor-core assignment (wi_assign_tc.cu)
+bool wi_assign_tc_supported(const WiGeom& g);
+cudaError_t wi_launch_assign_tc(const WiGeom& g, const void* K, const void* chat, int32_t* assign, int* err,
+                                cudaStream_t st);
+
+// ---- decode kernels (wi_decode.cu)
+struct WiDecodeBufs {
+  const void* mu;
+  const float* valsum;
+  const int* cnt;
+  const int* off;
+  const int* nonempty;
+  const void* K;
+  const void* V;
+  void* appK;
+  void* appV;
+  int* app_count;
+  float* scores;   // [U][G][C]
+  float* part1;    // [U][G][nchunk][WI_PART]
+  int* sel;        // [U][G][kmax]
+  int* selcnt;     // [U][G]
+  uint32_t* rows;  // [U][rows_cap] packed (row << 8 | head mask)
+  int* rcount;     // [U]
+  unsigned long long* rows_total;  // running sum of exact rows over all steps
+  float* part3;    // [U][G][nsplit][WI_PART]
+  int* err;
+  int nchunk, chunk, nsplit;
+  long long rows_cap;
+};
+#define WI_PART 132  // floats per zone partial: m, Z, 2 pad, N[128]
+
+#define WI_DECODE_KERNELS 5  // D1 score+estimate, D2 top-k, D2b union, D3 exact, D5 merge
+cudaError_t wi_launch_decode(const WiGeom& g, const WiDecodeBufs& b, const void* q, float* out, cudaStream_t st,
+                             const cudaEvent_t* ev /* NULL or WI_DECODE_KERNELS + 1 events */);
+cudaError_t wi_launch_append(const WiGeom& g, const WiDecodeBufs& b, const void* k_new, const void* v_new, int t,
+                             cudaStream_t st);
+size_t wi_union_smem_bytes(const WiGeom& g);

@@ -1,0 +1,192 @@
+/*
+ * wave_index.h -- C ABI of the GB300 wave-index hot path.
+ *
+ * RetroInfer treats the KV cache as a vector store that each decode step
+ * queries (RetroInfer abstract; summaries de/fr/zh section 2.A).  This library
+ * builds that store's index at prefill -- segmented spherical k-means over
+ * the keys of every (sequence, layer, kv head), with per-cluster counts, mean
+ * keys and value sums -- and runs the decode-time tripartite attention:
+ * steady zone (sinks + local window) and the top-k retrieved clusters exactly,
+ * every other cluster estimated from its mean key, count and value sum, the
+ * zones merged by log-sum-exp.
+ *
+ * Conventions for every entry point:
+ *   - All tensors are row-major and contiguous.  bf16 tensors are passed as
+ *     raw 16-bit patterns (uint16_t / void*).
+ *   - "device" pointers must be CUDA device memory of the current device
+ *     (cudaMalloc / torch); "host" pointers plain host memory; "any" pointers
+ *     either (copied with cudaMemcpyDefault, so they must be UVA-addressable).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     enqueued on it; outputs are valid once the stream has been synchronised,
+ *     unless stated otherwise.
+ *   - Every call returns WI_OK (0) or a negative WI_E* code and then leaves a
+ *     thread-local message readable with wi_last_error().  No call aborts,
+ *     exits, throws across the ABI or traps on the device.  On error an
+ *     output handle is set to NULL.
+ *   - Head size d must be 128.  Query head h attends with kv head h / g,
+ *     g = n_q_heads / n_kv_heads.  A "unit" is one (sequence b, layer l,
+ *     kv head h), numbered u = (b * layers + l) * n_kv_heads + h.
+ */
+#ifndef WAVE_INDEX_H
+#define WAVE_INDEX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  WI_OK = 0,
+  WI_EINVAL = -1,       /* bad argument: shape, null pointer, d != 128, k > C, ... */
+  WI_ENOMEM = -2,       /* a device or host allocation failed */
+  WI_ECUDA = -3,        /* a CUDA runtime call failed (message names it) */
+  WI_EUNSUPPORTED = -4, /* valid but not supported by this build */
+  WI_EDEVICE = -5,      /* a kernel reported a violated invariant */
+  WI_EFULL = -6         /* the append buffer is full */
+};
+
+typedef struct wi_index wi_index; /* opaque, library-owned */
+
+/*
+ * Shapes and method parameters.  Zones (summaries de/fr/zh 2.A): the steady
+ * zone is positions [0, n_sink) and [n_ctx - local_window, n_ctx) plus every
+ * token appended during decode; all other positions are clustered.
+ * Segmented clustering (same sections): each run of seg_len positions is
+ * clustered on its own into clusters_per_seg clusters (global id =
+ * segment * clusters_per_seg + local id) by `iters` rounds of spherical
+ * k-means (summary fr 2.A.2).  Retrieval budget (summary zh section 3):
+ * k = budget_k if > 0, else ceil(budget_frac * C), C = all clusters of a unit;
+ * capped at the unit's non-empty clusters at decode time.
+ */
+typedef struct {
+  int batch, layers, n_q_heads, n_kv_heads, head_dim; /* head_dim == 128 */
+  long long n_ctx;        /* tokens per unit at build; a multiple of seg_len */
+  int seg_len;            /* a multiple of 128, >= 128 */
+  int clusters_per_seg;   /* multiple of 16, 16..512, <= seg_len / 2 */
+  int iters;              /* k-means rounds (assignments), >= 1 */
+  int n_sink, local_window;
+  int max_append;         /* capacity of the decode-time append buffer, >= 0 */
+  double budget_frac;
+  int budget_k;
+  int reserved[3];        /* must be zero */
+} wi_config;
+
+/*
+ * Build the index (prefill).  k, v: device bf16 [batch][layers][n_kv_heads]
+ * [n_ctx][128], caller-owned.  The library permutes their clustered rows IN
+ * PLACE into cluster-contiguous order (cluster by cluster, by position inside
+ * a cluster; steady rows stay where they are) and keeps pointing at them: the
+ * caller keeps both alive and unmodified until wi_free.
+ * init_centroids: NULL for the default seeding (the normalised key at the
+ * start of each stride-(seg_len/clusters_per_seg) block of a segment), or
+ * device bf16 [units][n_ctx/seg_len][clusters_per_seg][128] used as the
+ * centroids of the first round (rows should be unit-norm).
+ * Enqueues the build on `stream` and returns; *out is usable on that stream.
+ */
+int wi_build_index(const wi_config* cfg, void* k, void* v, const void* init_centroids, void* stream,
+                   wi_index** out);
+
+/*
+ * Adopt an index computed elsewhere instead of clustering (e.g. by a CPU
+ * reference).  counts: [units][C] int32; perm: [units][n_ctx - n_sink -
+ * local_window] int32, the original position of every clustered slot in
+ * cluster-contiguous order (slots of cluster j follow those of cluster j-1;
+ * slot numbering starts at row n_sink); mu: bf16 [units][C][128] mean keys;
+ * valsum: fp32 [units][C][128] value sums.  All four are "any" pointers and
+ * are copied.  k, v as in wi_build_index (permuted in place by perm).
+ * Returns WI_EINVAL if perm is not a bijection on the clustered positions
+ * consistent with counts and segments (checked on the host).
+ */
+int wi_index_import(const wi_config* cfg, void* k, void* v, const int32_t* counts, const int32_t* perm,
+                    const uint16_t* mu, const float* valsum, void* stream, wi_index** out);
+
+/*
+ * Copy the index out ("any" pointers; any of them may be NULL to skip it).
+ * counts [units][C], offsets [units][C+1] (row of the first slot of each
+ * cluster; offsets[C] = n_ctx - local_window), perm as in wi_index_import,
+ * mu bf16 [units][C][128], valsum fp32 [units][C][128].  Asynchronous.
+ */
+int wi_index_export(const wi_index* ix, int32_t* counts, int32_t* offsets, int32_t* perm, uint16_t* mu,
+                    float* valsum, void* stream);
+
+/*
+ * One decode step.  q: device bf16 [batch][layers][n_q_heads][128], the
+ * queries of the step (already rotated); out: device fp32 [batch][layers]
+ * [n_q_heads][128], attention output per query head.  Attention runs over
+ * the current context: the n_ctx built tokens plus every token appended so
+ * far.  If k_new and v_new (device bf16 [batch][layers][n_kv_heads][128]) are
+ * non-NULL, that token is appended AFTER this step's attention; returns
+ * WI_EFULL (nothing enqueued) when max_append tokens are already appended.
+ * Uses only library-owned scratch: no allocation and no host synchronisation.
+ * Steps without append replay correctly from a captured CUDA graph.
+ */
+int wi_decode_step(wi_index* ix, const void* q, const void* k_new, const void* v_new, float* out, void* stream);
+
+/*
+ * wi_decode_step with HOST q / k_new / v_new / out: copies the inputs to the
+ * device, runs the step, copies the output back and synchronises `stream`
+ * before returning (out is valid on return).  Pinned host memory makes the
+ * copies asynchronous DMA; pageable memory works but is slower.
+ */
+int wi_decode_step_host(wi_index* ix, const void* q_host, const void* k_new_host, const void* v_new_host,
+                        float* out_host, void* stream);
+
+/*
+ * Clusters retrieved by the last decode step: ids [units][g][k_max] int32
+ * ("any"), ascending within each head, padded with -1; counts [units][g]
+ * int32 ("any", may be NULL).  k_max is reported by wi_index_shape.
+ */
+int wi_last_selection(const wi_index* ix, int32_t* ids, int32_t* counts, void* stream);
+
+/* Sizes of an index: units, clusters per unit, k_max (the budget), group g,
+ * tokens appended so far (host-side count).  Any output pointer may be NULL. */
+int wi_index_shape(const wi_index* ix, int* units, int* clusters, int* k_max, int* group, int* appended);
+
+/*
+ * One spherical k-means round on every segment, for per-round checking:
+ * assignment of each clustered token against `centroids` (device bf16
+ * [units][n_segments][clusters_per_seg][128]) written to assign (device int32
+ * [units][n_ctx], global cluster id, -1 for steady positions), then the
+ * updated centroids bf16(normalise(sum of normalised member keys)), empty
+ * clusters unchanged, to new_centroids (device, same shape; may alias
+ * centroids).  k: device bf16 keys as in wi_build_index (not modified).
+ * Allocates and frees its own scratch on `stream`.
+ */
+int wi_kmeans_step(const wi_config* cfg, const void* k, const void* centroids, int32_t* assign,
+                   void* new_centroids, void* stream);
+
+/*
+ * Per-kernel timing of decode steps (benchmarking aid).  After
+ * wi_profile_begin(ix, max_steps), every decode step on this index records
+ * CUDA events around each of its WI_NUM_DECODE_KERNELS kernels (score +
+ * estimate, top-k, union, exact attention, merge) into slot
+ * (step number % max_steps); steps captured into a CUDA graph record them on
+ * every replay.  wi_profile_read synchronises the device and returns, per
+ * kernel, the summed duration in milliseconds over the filled slots
+ * (kernel_ms[WI_NUM_DECODE_KERNELS], may be NULL), the number of filled
+ * slots, and the exact-zone rows processed by all decode steps since the
+ * index was created (the byte count of exact attention is rows * 512).
+ * wi_profile_begin with max_steps = 0 turns recording off.
+ */
+#define WI_NUM_DECODE_KERNELS 5
+int wi_profile_begin(wi_index* ix, int max_steps);
+int wi_profile_read(wi_index* ix, double* kernel_ms, int* steps, unsigned long long* exact_rows);
+
+/* Synchronise the index's last stream and report a device-side invariant
+ * violation recorded by any kernel since the last call (WI_EDEVICE). */
+int wi_check_device(wi_index* ix);
+
+/* Release the index and everything it owns (not k / v).  NULL is a no-op.
+ * Synchronises the device first. */
+void wi_free(wi_index* ix);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* wi_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WAVE_INDEX_H */

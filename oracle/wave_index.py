@@ -104,6 +104,8 @@ def assign(k_idx: np.ndarray, c_hat: np.ndarray) -> np.ndarray:
     product equals argmax of the cosine because |K_i| is fixed per token.
     np.argmax returns the first maximum, i.e. the lowest j on ties.
     """
+    if k_idx.shape[0] == 0:          # a segment that lies wholly in the steady zone
+        return np.zeros(0, np.int64)
     scores = k_idx @ c_hat.T
     return np.argmax(scores, axis=1)
 

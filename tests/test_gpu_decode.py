@@ -1,0 +1,199 @@
+"""Decode parity: the CUDA decode step against the float64 oracle, both given
+the oracle's index (wi_index_import), on the same seeded input bytes."""
+import numpy as np
+import pytest
+import torch
+
+import kvsynth
+import oracle
+from helpers import (OUT_REL_L2, check_topk, gen, index_arrays, params_of, rel_l2, small)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def wi():
+    import clustered_sparse_kv_gb300 as m
+    return m
+
+
+def dev16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(DEV)
+
+
+def run_case(wi, w, idx=None, steps=1, append=False, kv=None):
+    """Import the oracle index, decode `steps` steps (with append if asked), compare every step."""
+    k, v, q, K, V, Q = gen(w)
+    if kv is not None:
+        k, v = kv
+        K = oracle.bf16_from_bits(k).reshape(w.units, w.n_ctx, 128)
+        V = oracle.bf16_from_bits(v).reshape(w.units, w.n_ctx, 128)
+    p = params_of(w)
+    if idx is None:
+        idx = oracle.build_index(K, V, p)
+    cfg = wi.config_from_workload(w, max_append=steps if append else 0)
+    kt, vt = dev16(k), dev16(v)
+    ix = wi.WaveIndex.adopt(cfg, kt, vt, *index_arrays(idx))
+    worst = 0.0
+    if append:
+        ka, va = kvsynth.kv_cache(w, p0=w.n_ctx, p1=w.n_ctx + steps)
+        KA = oracle.bf16_from_bits(ka).reshape(w.units, steps, 128)
+        VA = oracle.bf16_from_bits(va).reshape(w.units, steps, 128)
+    for t in range(steps):
+        qb = kvsynth.queries(w, step=t)
+        Qt = oracle.bf16_from_bits(qb).reshape(w.units, w.group, 128)
+        kn = vn = None
+        if append:
+            kn, vn = dev16(ka[:, :, :, t]), dev16(va[:, :, :, t])
+        out = ix.decode(dev16(qb), kn, vn)
+        ids, cnt = ix.selection()
+        torch.cuda.synchronize()
+        ix.check()
+        got = out.cpu().numpy().reshape(w.units, w.group, 128).astype(np.float64)
+        kap = KA[:, :t] if append else None
+        vap = VA[:, :t] if append else None
+        ref, info = oracle.decode(Qt, K, V, idx, p, w.group, k_app=kap, v_app=vap, details=True)
+        err = rel_l2(got, ref)
+        assert err.max() <= OUT_REL_L2, (t, err.max())
+        worst = max(worst, float(err.max()))
+        ids, cnt = ids.cpu().numpy(), cnt.cpu().numpy()
+        for u in range(w.units):
+            ne = idx[u]["counts"] > 0
+            kk = oracle.budget_k(w.clusters, p)
+            for h in range(w.group):
+                check_topk(ids[u, h], cnt[u, h], info[u][h]["scores"], ne, kk)
+    ix.free()
+    return worst
+
+
+@pytest.mark.parametrize("g", [1, 4, 7])
+def test_decode_parity_group_sizes(wi, g):
+    w = small(n_ctx=4096, seg_len=1024, clusters_per_seg=64, iters=3, n_q_heads=g, n_kv_heads=1, budget_k=6)
+    assert run_case(wi, w) < 1e-4
+
+
+def test_decode_parity_multi_unit(wi):
+    w = small(batch=2, layers=2, n_q_heads=8, n_kv_heads=2, n_ctx=2048, seg_len=512, clusters_per_seg=32, iters=2,
+              budget_k=5, seed=11)
+    assert run_case(wi, w) < 1e-4
+
+
+def test_decode_tiny_workload_full_size(wi):
+    w = kvsynth.get_workload("tiny-8k")
+    assert run_case(wi, w) < 1e-4
+
+
+def test_all_clusters_selected_is_full_attention(wi):
+    w = small(n_ctx=2048, seg_len=512, clusters_per_seg=32, iters=2, n_q_heads=4, budget_k=128)
+    k, v, q, K, V, Q = gen(w)
+    p = params_of(w)
+    idx = oracle.build_index(K, V, p)
+    cfg = wi.config_from_workload(w)
+    ix = wi.WaveIndex.adopt(cfg, dev16(k), dev16(v), *index_arrays(idx))
+    out = ix.decode(dev16(q)).cpu().numpy().reshape(1, 4, 128)
+    for h in range(4):
+        l = K[0] @ Q[0, h] / np.sqrt(128)
+        wgt = np.exp(l - l.max())
+        full = wgt @ V[0] / wgt.sum()
+        assert rel_l2(out[0, h], full) < 1e-5
+    ix.free()
+
+
+def degenerate_kv(w, lo, hi):
+    """Generator cache with positions [lo, hi) overwritten by copies of one key row:
+    one giant cluster, duplicated seeds (ties to the lowest id) and many empty clusters."""
+    k, v = kvsynth.kv_cache(w)
+    k[:, :, :, lo:hi] = k[:, :, :, lo:lo + 1]
+    return k, v
+
+
+def test_decode_ragged_clusters(wi):
+    w = small(n_ctx=2048, seg_len=1024, clusters_per_seg=64, iters=4, n_q_heads=4, budget_k=7, seed=21)
+    k, v = degenerate_kv(w, 100, 900)
+    K = oracle.bf16_from_bits(k).reshape(1, w.n_ctx, 128)
+    V = oracle.bf16_from_bits(v).reshape(1, w.n_ctx, 128)
+    idx = oracle.build_index(K, V, params_of(w))
+    c = idx[0]["counts"]
+    assert (c == 0).sum() > 40 and c.max() >= 800
+    assert run_case(wi, w, idx=idx, kv=(k, v)) < 1e-4
+
+
+def test_decode_budget_above_nonempty(wi):
+    w = small(n_ctx=2048, seg_len=1024, clusters_per_seg=64, iters=4, n_q_heads=4, budget_k=100, seed=22)
+    k, v = degenerate_kv(w, 50, 1000)
+    K = oracle.bf16_from_bits(k).reshape(1, w.n_ctx, 128)
+    V = oracle.bf16_from_bits(v).reshape(1, w.n_ctx, 128)
+    idx = oracle.build_index(K, V, params_of(w))
+    assert (idx[0]["counts"] > 0).sum() < 100
+    assert run_case(wi, w, idx=idx, kv=(k, v)) < 1e-4
+
+
+@pytest.mark.parametrize("n_sink,window", [(0, 16), (8, 0), (4, 64)])
+def test_decode_steady_zone_shapes(wi, n_sink, window):
+    w = small(n_ctx=2048, seg_len=512, clusters_per_seg=32, iters=2, n_q_heads=4, n_sink=n_sink,
+              local_window=window, budget_k=4, seed=31)
+    assert run_case(wi, w) < 1e-4
+
+
+def test_decode_with_append(wi):
+    w = small(batch=2, n_ctx=2048, seg_len=512, clusters_per_seg=32, iters=2, n_q_heads=7, n_kv_heads=1,
+              budget_k=5, append=True, decode_steps=6, seed=41)
+    assert run_case(wi, w, steps=6, append=True) < 1e-4
+
+
+def test_append_buffer_full(wi):
+    w = small(n_ctx=1024, seg_len=512, clusters_per_seg=32, iters=1, n_q_heads=1, budget_k=2)
+    k, v, q, K, V, Q = gen(w)
+    cfg = wi.config_from_workload(w, max_append=1)
+    ix = wi.WaveIndex.build(cfg, dev16(k), dev16(v))
+    kn = torch.zeros((1, 1, 1, 128), dtype=torch.int16, device=DEV)
+    ix.decode(dev16(q), kn, kn)
+    with pytest.raises(wi.WiError) as e:
+        ix.decode(dev16(q), kn, kn)
+    assert e.value.code == wi.WI_EFULL
+    ix.decode(dev16(q))  # without append still fine
+    torch.cuda.synchronize()
+    ix.free()
+
+
+def test_host_buffer_variant_matches(wi):
+    w = small(n_ctx=2048, seg_len=512, clusters_per_seg=32, iters=2, n_q_heads=4, budget_k=4, seed=51)
+    k, v, q, K, V, Q = gen(w)
+    cfg = wi.config_from_workload(w)
+    ix = wi.WaveIndex.build(cfg, dev16(k), dev16(v))
+    ref = ix.decode(dev16(q)).cpu()
+    qh = torch.from_numpy(q.view(np.int16)).pin_memory()
+    oh = torch.empty((1, 1, 4, 128), dtype=torch.float32).pin_memory()
+    wi.wi_decode_step_host(ix.handle, qh, oh)
+    assert torch.equal(oh, ref)
+    ix.free()
+
+
+def test_graph_replay_matches_direct(wi):
+    w = small(n_ctx=4096, seg_len=1024, clusters_per_seg=64, iters=2, n_q_heads=4, budget_k=6, seed=61)
+    k, v, q, K, V, Q = gen(w)
+    cfg = wi.config_from_workload(w)
+    ix = wi.WaveIndex.build(cfg, dev16(k), dev16(v))
+    qbuf = dev16(q)
+    out = torch.empty((1, 1, 4, 128), dtype=torch.float32, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ix.decode(qbuf, out=out, stream=s)  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        ix.decode(qbuf, out=out, stream=s)
+    for t in range(3):
+        qn = kvsynth.queries(w, step=t + 1)
+        qbuf.copy_(dev16(qn))
+        graph.replay()
+        torch.cuda.synchronize()
+        got = out.clone()
+        direct = ix.decode(dev16(qn))
+        torch.cuda.synchronize()
+        assert torch.equal(got, direct)
+    ix.free()
