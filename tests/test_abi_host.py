@@ -6,9 +6,10 @@ import re
 
 import pytest
 
-from clustered_sparse_kv_gb300 import _build
+import __graft_entry__
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+_build = __graft_entry__._load_build_module()
 HEADER = os.path.join(ROOT, "include", "wave_index.h")
 
 
