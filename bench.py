@@ -299,7 +299,7 @@ def main():
     g_full = capture(L) if full else None
     g_rest = capture(rest) if rest else None
     stream.synchronize()
-    rows0 = [wi.wi_profile_read(ix.handle)[2] for ix in replicas]
+    rows0 = [wi.wi_profile_read(ix.handle, times=False)[2] for ix in replicas]
 
     barrier()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -174,12 +174,14 @@ def wi_profile_begin(ix: int, max_steps: int):
     _check(lib.wi_profile_begin(ix, max_steps))
 
 
-def wi_profile_read(ix: int):
+def wi_profile_read(ix: int, times: bool = True):
+    """(per-kernel summed ms, filled slots, exact rows).  times=False skips the event
+    timings (use it before the recorded steps have run, e.g. right after a graph capture)."""
     ms = (ctypes.c_double * WI_NUM_DECODE_KERNELS)()
     steps = ctypes.c_int()
     rows = ctypes.c_ulonglong()
-    _check(lib.wi_profile_read(ix, ms, ctypes.byref(steps), ctypes.byref(rows)))
-    return dict(zip(DECODE_KERNELS, list(ms))), steps.value, rows.value
+    _check(lib.wi_profile_read(ix, ms if times else None, ctypes.byref(steps), ctypes.byref(rows)))
+    return dict(zip(DECODE_KERNELS, list(ms))) if times else None, steps.value, rows.value
 
 
 def wi_free(ix: int):

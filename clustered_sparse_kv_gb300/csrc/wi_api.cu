@@ -28,7 +28,10 @@ int fail(int code, const char* fmt, ...) {
 #define WI_CUDA(call)                                                                          \
   do {                                                                                         \
     cudaError_t e_ = (call);                                                                   \
-    if (e_ != cudaSuccess) return fail(WI_ECUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+    if (e_ != cudaSuccess) {                                                                   \
+      cudaGetLastError(); /* clear a non-sticky error so later launch checks stay clean */    \
+      return fail(WI_ECUDA, "%s: %s", #call, cudaGetErrorString(e_));                         \
+    }                                                                                          \
   } while (0)
 
 int env_int(const char* name, int dflt) {
@@ -291,6 +294,7 @@ void scratch_free(BuildScratch* s, cudaStream_t st) {
   do {                                                                                              \
     cudaError_t e_ = (call);                                                                        \
     if (e_ != cudaSuccess) {                                                                        \
+      cudaGetLastError();                                                                           \
       rc = fail(WI_ECUDA, "%s: %s", #call, cudaGetErrorString(e_));                                 \
       goto done;                                                                                    \
     }                                                                                               \

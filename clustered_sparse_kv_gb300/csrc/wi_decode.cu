@@ -367,6 +367,8 @@ __global__ void __launch_bounds__(kD3Threads) k_d3_exact(const bf16* __restrict_
     for (int i = 0; i < 8; ++i) {
       const uint32_t e = __shfl_sync(0xffffffffu, mine, i);
       mk[i] = i < nr ? (e & 0xFFu) : 0u;
+      kw[i] = make_uint2(0u, 0u);  // rows past the range contribute p = 0 times a finite value
+      vw[i] = make_uint2(0u, 0u);
       if (i < nr) {
         const long long row = e >> 8;
         const bf16* kp;
