@@ -57,6 +57,7 @@ _SIGS = {
     "wi_last_selection": [_vp, _vp, _vp, _vp],
     "wi_index_shape": [_vp, _ip, _ip, _ip, _ip, _ip],
     "wi_kmeans_step": [_cfgp, _vp, _vp, _vp, _vp, _vp],
+    "wi_kmeans_step_noalloc": [_cfgp, _vp, _vp, _vp, _vp, _vp],
     "wi_check_device": [_vp],
     "wi_profile_begin": [_vp, ctypes.c_int],
     "wi_profile_read": [_vp, ctypes.POINTER(ctypes.c_double), _ip, ctypes.POINTER(ctypes.c_ulonglong)],
@@ -160,6 +161,12 @@ def wi_index_shape(ix: int) -> dict:
 def wi_kmeans_step(cfg: wi_config, k, centroids, assign, new_centroids, stream=None):
     _check(lib.wi_kmeans_step(ctypes.byref(cfg), _ptr(k), _ptr(centroids), _ptr(assign), _ptr(new_centroids),
                               _stream(stream)))
+
+
+def wi_kmeans_step_noalloc(cfg: wi_config, k, centroids, assign, new_centroids, stream=None):
+    """wi_kmeans_step with its scratch in the library's fixed device array (no allocation)."""
+    _check(lib.wi_kmeans_step_noalloc(ctypes.byref(cfg), _ptr(k), _ptr(centroids), _ptr(assign),
+                                      _ptr(new_centroids), _stream(stream)))
 
 
 def wi_check_device(ix: int):

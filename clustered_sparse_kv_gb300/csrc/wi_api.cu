@@ -302,6 +302,8 @@ void scratch_free(BuildScratch* s, cudaStream_t st) {
 
 }  // namespace
 
+void wi_set_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
 extern "C" {
 
 const char* wi_last_error(void) { return g_err; }

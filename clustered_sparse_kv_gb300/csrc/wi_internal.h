@@ -21,6 +21,7 @@ struct WiGeom {
 };
 
 int wi_geom_from_config(const wi_config* cfg, WiGeom* g, char* msg, size_t msglen);
+void wi_set_error(const char* msg);  // sets the thread-local message of wi_last_error()
 
 // ---- build kernels (wi_build.cu); all enqueue on `st` and return the launch status
 cudaError_t wi_launch_invnorm(const void* K, float* invnorm, long long rows, cudaStream_t st);

@@ -174,6 +174,24 @@ int wi_kmeans_step(const wi_config* cfg, const void* k, const void* centroids, i
 int wi_profile_begin(wi_index* ix, int max_steps);
 int wi_profile_read(wi_index* ix, double* kernel_ms, int* steps, unsigned long long* exact_rows);
 
+/*
+ * wi_kmeans_step without any device allocation (the paper has no
+ * counterpart; this is an interface for callers that may not allocate).
+ * A serving process usually gives nearly all GPU memory to its KV-cache
+ * pool, and some hosts allow device memory only through their own arena;
+ * such callers cannot let a clustering round call cudaMalloc.  Same
+ * arguments, same results as wi_kmeans_step; its scratch is a fixed 8 MiB
+ * device array that every GPU loading this library holds until the process
+ * exits.  Problems that need more scratch (about 340K tokens in total at 512
+ * clusters per 8192-token segment) return WI_EINVAL with a message.
+ * All calls share the array: calls whose work overlaps on the GPU race on it
+ * (order them on one stream).  The first call on a device looks up the
+ * array's device address with that device current.  Synchronises `stream`
+ * before returning.
+ */
+int wi_kmeans_step_noalloc(const wi_config* cfg, const void* k, const void* centroids, int32_t* assign,
+                           void* new_centroids, void* stream);
+
 /* Synchronise the index's last stream and report a device-side invariant
  * violation recorded by any kernel since the last call (WI_EDEVICE). */
 int wi_check_device(wi_index* ix);
