@@ -173,8 +173,8 @@ def wi_check_device(ix: int):
     _check(lib.wi_check_device(ix))
 
 
-WI_NUM_DECODE_KERNELS = 5
-DECODE_KERNELS = ["score_estimate", "topk", "union", "exact", "merge"]
+WI_NUM_DECODE_KERNELS = 3
+DECODE_KERNELS = ["score_estimate", "topk_sub", "exact_merge"]
 
 
 def wi_profile_begin(ix: int, max_steps: int):

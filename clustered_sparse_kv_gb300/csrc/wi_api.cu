@@ -121,6 +121,10 @@ int wi_geom_from_config(const wi_config* c, WiGeom* g, char* msg, size_t msglen)
     snprintf(msg, msglen, "query heads per kv head must be <= 8 (got %d)", g->G);
     return WI_EUNSUPPORTED;
   }
+  if (g->kmax > 4096) {
+    snprintf(msg, msglen, "retrieval budget must be <= 4096 clusters (got %d)", g->kmax);
+    return WI_EUNSUPPORTED;
+  }
   if (g->S > 16384) {
     snprintf(msg, msglen, "seg_len must be <= 16384 (got %d)", g->S);
     return WI_EUNSUPPORTED;
@@ -168,25 +172,31 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   A(ix->app_count, 4);
   A(ix->err, 4);
   WiDecodeBufs& b = ix->b;
-  b.chunk = env_int("WI_D1_CHUNK", 256);
-  if (b.chunk < 32) b.chunk = 32;
-  b.nchunk = (int)((C + b.chunk - 1) / b.chunk);
+  int sms = 0;
+  WI_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ix->device));
+  const int tiles = (int)((C + 15) / 16);  // score_estimate splits a unit's clusters on multiples of 16
+  int p1 = env_int("WI_D1_CTAS_PER_UNIT", 0);
+  if (p1 <= 0) p1 = (int)((sms + U - 1) / U);
+  if (p1 > tiles) p1 = tiles;
+  if (p1 > 256) p1 = 256;
+  if (p1 < 1) p1 = 1;
+  b.p1 = p1;
+  // exact attention: (splits + 1 steady CTA) per head, sized to fill two CTAs per SM in one wave
   int ns = env_int("WI_D3_SPLITS", 0);
-  if (ns <= 0) {
-    ns = (int)((4 * 152 + U - 1) / U);
-    if (ns > 64) ns = 64;
-    if (ns < 1) ns = 1;
-  }
+  if (ns <= 0) ns = (int)((2 * (size_t)sms) / (U * G)) - 1;
+  if (ns > 64) ns = 64;
+  if (ns < 1) ns = 1;
   b.nsplit = ns;
-  b.rows_cap = g.n + app;
   A(b.scores, U * G * C * 4);
-  A(b.part1, U * G * (size_t)b.nchunk * WI_PART * 4);
+  A(b.part1, U * G * (size_t)b.p1 * WI_PART * 4);
   A(b.sel, U * G * (size_t)g.kmax * 4);
   A(b.selcnt, U * G * 4);
-  A(b.rows, U * (size_t)b.rows_cap * 4);
-  A(b.rcount, U * 4);
+  A(b.subpart, U * G * WI_PART * 4);
+  A(b.runs, U * G * (size_t)g.kmax * 8);
+  A(b.splits, U * G * (size_t)(b.nsplit + 1) * 16);
+  A(b.part3, U * G * (size_t)(b.nsplit + 1) * WI_PART * 4);
+  A(b.ticket, U * G * 4);
   A(b.rows_total, 8);
-  A(b.part3, U * G * (size_t)b.nsplit * WI_PART * 4);
   A(ix->q_dev, U * G * 128 * 2);
   A(ix->out_dev, U * G * 128 * 4);
   A(ix->kn_dev, U * 128 * 2);
@@ -206,7 +216,7 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   WI_CUDA(cudaMemsetAsync(ix->app_count, 0, 4, st));
   WI_CUDA(cudaMemsetAsync(ix->err, 0, 4, st));
   WI_CUDA(cudaMemsetAsync(b.selcnt, 0, U * G * 4, st));
-  WI_CUDA(cudaMemsetAsync(b.rcount, 0, U * 4, st));
+  WI_CUDA(cudaMemsetAsync(b.ticket, 0, U * G * 4, st));
   WI_CUDA(cudaMemsetAsync(b.rows_total, 0, 8, st));
   return WI_OK;
 }

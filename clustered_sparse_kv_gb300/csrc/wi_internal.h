@@ -56,23 +56,25 @@ struct WiDecodeBufs {
   void* appK;
   void* appV;
   int* app_count;
-  float* scores;   // [U][G][C]
-  float* part1;    // [U][G][nchunk][WI_PART]
-  int* sel;        // [U][G][kmax]
-  int* selcnt;     // [U][G]
-  uint32_t* rows;  // [U][rows_cap] packed (row << 8 | head mask)
-  int* rcount;     // [U]
-  unsigned long long* rows_total;  // running sum of exact rows over all steps
-  float* part3;    // [U][G][nsplit][WI_PART]
+  float* scores;          // [U][G][C]
+  float* part1;           // [U][G][p1][WI_PART]  estimation partials of score_estimate
+  int* sel;               // [U][G][kmax]
+  int* selcnt;            // [U][G]
+  float* subpart;         // [U][G][WI_PART]      estimation terms of the selected clusters
+  int2* runs;             // [U][G][kmax]  (first row, rows) of each selected cluster
+  int4* splits;           // [U][G][nsplit+1]  row-balanced split starts over the selected rows
+  float* part3;           // [U][G][nsplit+1][WI_PART]  exact partials (the last split: steady rows)
+  unsigned int* ticket;   // [U][G]  CTAs of exact_merge finished, per head
+  unsigned long long* rows_total;  // running sum of exact rows loaded over all steps
   int* err;
-  int nchunk, chunk, nsplit;
-  long long rows_cap;
+  int p1;                 // score_estimate CTAs per unit
+  int nsplit;             // exact_merge CTAs per head over the selected rows (plus one for steady rows)
 };
 #define WI_PART 132  // floats per zone partial: m, Z, 2 pad, N[128]
 
-#define WI_DECODE_KERNELS 5  // D1 score+estimate, D2 top-k, D2b union, D3 exact, D5 merge
+#define WI_DECODE_KERNELS 3  // score_estimate, topk_sub, exact_merge
 cudaError_t wi_launch_decode(const WiGeom& g, const WiDecodeBufs& b, const void* q, float* out, cudaStream_t st,
                              const cudaEvent_t* ev /* NULL or WI_DECODE_KERNELS + 1 events */);
 cudaError_t wi_launch_append(const WiGeom& g, const WiDecodeBufs& b, const void* k_new, const void* v_new, int t,
                              cudaStream_t st);
-size_t wi_union_smem_bytes(const WiGeom& g);
+

@@ -64,7 +64,7 @@ typedef struct {
   int batch, layers, n_q_heads, n_kv_heads, head_dim; /* head_dim == 128 */
   long long n_ctx;        /* tokens per unit at build; a multiple of seg_len */
   int seg_len;            /* a multiple of 128, >= 128 */
-  int clusters_per_seg;   /* multiple of 16, 16..512, <= seg_len / 2 */
+  int clusters_per_seg;   /* multiple of 16 in [16, 512] dividing seg_len */
   int iters;              /* k-means rounds (assignments), >= 1 */
   int n_sink, local_window;
   int max_append;         /* capacity of the decode-time append buffer, >= 0 */
@@ -161,16 +161,18 @@ int wi_kmeans_step(const wi_config* cfg, const void* k, const void* centroids, i
  * Per-kernel timing of decode steps (benchmarking aid).  After
  * wi_profile_begin(ix, max_steps), every decode step on this index records
  * CUDA events around each of its WI_NUM_DECODE_KERNELS kernels (score +
- * estimate, top-k, union, exact attention, merge) into slot
+ * estimate, top-k with the retrieved clusters' estimation terms, exact
+ * attention with the final merge) into slot
  * (step number % max_steps); steps captured into a CUDA graph record them on
  * every replay.  wi_profile_read synchronises the device and returns, per
  * kernel, the summed duration in milliseconds over the filled slots
  * (kernel_ms[WI_NUM_DECODE_KERNELS], may be NULL), the number of filled
  * slots, and the exact-zone rows processed by all decode steps since the
- * index was created (the byte count of exact attention is rows * 512).
+ * index was created, counted per query head (the bytes the exact-attention
+ * kernel loads are rows * 512).
  * wi_profile_begin with max_steps = 0 turns recording off.
  */
-#define WI_NUM_DECODE_KERNELS 5
+#define WI_NUM_DECODE_KERNELS 3
 int wi_profile_begin(wi_index* ix, int max_steps);
 int wi_profile_read(wi_index* ix, double* kernel_ms, int* steps, unsigned long long* exact_rows);
 
