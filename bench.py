@@ -268,10 +268,18 @@ def main():
             ix.check()
             if r == 1 and not args.no_build_timing:   # replica 0 is the warm-up build
                 secs = e0.elapsed_time(e1) / 1e3
+                st_ = wi.wi_index_build_stats(ix.handle)
                 n_idx = w.n_ctx - w.n_sink - w.local_window
                 flops = 2.0 * w.iters * w.units * n_idx * w.clusters_per_seg * 128
-                build = {"seconds": secs, "assign_flop": flops, "assign_tflops_over_build": flops / secs / 1e12,
-                         "segment_units_per_s": w.units * w.n_segments / secs}
+                assign_s = st_["assign_ms"] / 1e3
+                tf = flops / assign_s / 1e12
+                build = {"seconds": secs, "segment_units_per_s": w.units * w.n_segments / secs,
+                         "assign_flop": flops, "assign_seconds": assign_s,
+                         "assign_launches": st_["assign_launches"], "assign_tflops": tf,
+                         "assign_roofline": {"bound": "tensor", "achieved": tf, "peak": peaks()[1],
+                                             "unit": "TFLOP/s", "frac": tf / peaks()[1],
+                                             "peak_kind": peaks()[3]},
+                         "assign_tflops_over_build": flops / secs / 1e12}
             replicas.append(ix)
     del k_dev, v_dev
 

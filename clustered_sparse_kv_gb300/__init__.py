@@ -60,6 +60,7 @@ _SIGS = {
     "wi_kmeans_step_noalloc": [_cfgp, _vp, _vp, _vp, _vp, _vp],
     "wi_check_device": [_vp],
     "wi_profile_begin": [_vp, ctypes.c_int],
+    "wi_index_build_stats": [_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), _ip],
     "wi_profile_read": [_vp, ctypes.POINTER(ctypes.c_double), _ip, ctypes.POINTER(ctypes.c_ulonglong)],
 }
 for _name, _args in _SIGS.items():
@@ -189,6 +190,12 @@ def wi_profile_read(ix: int, times: bool = True):
     rows = ctypes.c_ulonglong()
     _check(lib.wi_profile_read(ix, ms if times else None, ctypes.byref(steps), ctypes.byref(rows)))
     return dict(zip(DECODE_KERNELS, list(ms))) if times else None, steps.value, rows.value
+
+
+def wi_index_build_stats(ix: int) -> dict:
+    b, a, n = ctypes.c_double(), ctypes.c_double(), ctypes.c_int()
+    _check(lib.wi_index_build_stats(ix, ctypes.byref(b), ctypes.byref(a), ctypes.byref(n)))
+    return {"build_ms": b.value, "assign_ms": a.value, "assign_launches": n.value}
 
 
 def wi_free(ix: int):

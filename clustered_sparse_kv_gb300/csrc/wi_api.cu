@@ -69,6 +69,8 @@ struct wi_index {
   float* out_dev = nullptr;
   cudaStream_t last_stream = nullptr;
   std::vector<void*> allocs;
+  // build timing: events around the whole build and around every assignment launch
+  std::vector<cudaEvent_t> build_ev;  // [0] start, [1] end, then (before, after) per assignment
   // decode profiling
   std::vector<cudaEvent_t> prof_ev;  // (WI_DECODE_KERNELS + 1) per slot
   int prof_slots = 0;
@@ -149,6 +151,7 @@ int alloc(wi_index* ix, void** p, size_t bytes) {
 void destroy(wi_index* ix) {
   if (!ix) return;
   for (cudaEvent_t e : ix->prof_ev) cudaEventDestroy(e);
+  for (cudaEvent_t e : ix->build_ev) cudaEventDestroy(e);
   for (void* p : ix->allocs) cudaFree(p);
   delete ix;
 }
@@ -333,13 +336,21 @@ int wi_build_index(const wi_config* cfg, void* k, void* v, const void* init_cent
     destroy(ix);
     return rc;
   }
+  for (int i = 0; i < 2 + 2 * g.iters; ++i) {
+    cudaEvent_t e;
+    WI_LAUNCH(cudaEventCreate(&e));
+    ix->build_ev.push_back(e);
+  }
+  WI_LAUNCH(cudaEventRecord(ix->build_ev[0], st));
   WI_LAUNCH(wi_launch_invnorm(k, s.invnorm, (long long)g.U * g.n, st));
   if (init_centroids)
     WI_LAUNCH(cudaMemcpyAsync(s.chat, init_centroids, (size_t)g.U * g.nseg * g.Cs * 128 * 2, cudaMemcpyDefault, st));
   else
     WI_LAUNCH(wi_launch_init_centroids(g, k, s.chat, st));
   for (int t = 0; t < g.iters; ++t) {
+    WI_LAUNCH(cudaEventRecord(ix->build_ev[2 + 2 * t], st));
     WI_LAUNCH(wi_launch_assign(g, k, s.chat, s.assign, ix->err, st));
+    WI_LAUNCH(cudaEventRecord(ix->build_ev[3 + 2 * t], st));
     WI_LAUNCH(wi_launch_segment_sort(g, s.assign, s.seg_counts, s.seg_offsets, s.slots, ix->err, st));
     if (t + 1 < g.iters)
       WI_LAUNCH(wi_launch_centroid_update(g, k, s.invnorm, s.seg_counts, s.seg_offsets, s.slots, s.chat, st));
@@ -349,6 +360,7 @@ int wi_build_index(const wi_config* cfg, void* k, void* v, const void* init_cent
   scratch_free(&s, st);
   s = BuildScratch();
   if ((rc = permute_kv(ix, st)) != WI_OK) goto done;
+  WI_LAUNCH(cudaEventRecord(ix->build_ev[1], st));
   *out = ix;
   return WI_OK;
 done:
@@ -578,6 +590,29 @@ int wi_profile_read(wi_index* ix, double* kernel_ms, int* steps, unsigned long l
   }
   if (steps) *steps = filled;
   if (exact_rows) WI_CUDA(cudaMemcpy(exact_rows, ix->b.rows_total, 8, cudaMemcpyDeviceToHost));
+  return WI_OK;
+}
+
+int wi_index_build_stats(wi_index* ix, double* build_ms, double* assign_ms, int* assign_launches) {
+  g_err[0] = 0;
+  if (!ix) return fail(WI_EINVAL, "index is NULL");
+  if (ix->build_ev.size() < 2) return fail(WI_EUNSUPPORTED, "the index was not built by wi_build_index");
+  WI_CUDA(cudaEventSynchronize(ix->build_ev[1]));
+  float ms = 0.f;
+  if (build_ms) {
+    WI_CUDA(cudaEventElapsedTime(&ms, ix->build_ev[0], ix->build_ev[1]));
+    *build_ms = ms;
+  }
+  const int n = (int)(ix->build_ev.size() - 2) / 2;
+  if (assign_ms) {
+    double acc = 0.0;
+    for (int t = 0; t < n; ++t) {
+      WI_CUDA(cudaEventElapsedTime(&ms, ix->build_ev[2 + 2 * t], ix->build_ev[3 + 2 * t]));
+      acc += ms;
+    }
+    *assign_ms = acc;
+  }
+  if (assign_launches) *assign_launches = n;
   return WI_OK;
 }
 

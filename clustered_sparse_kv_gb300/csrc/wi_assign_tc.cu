@@ -1,8 +1,367 @@
-// wi_assign_tc.cu -- tensor-core (tcgen05) spherical assignment.
+// wi_assign_tc.cu -- spherical k-means assignment on the 5th-generation
+// tensor cores: a_i = argmax_j K_i . c_j over a segment's centroids.
+//
+// Spherical k-means (RetroInfer summary fr 2.A.2) inside segmented
+// clustering (summaries de/fr/zh 2.A): every segment of S tokens is assigned
+// to its own Cs centroids.  Per segment this is the dense contraction
+// [S x 128] . [128 x Cs] (bf16 operands, fp32 accumulation) followed by a row
+// argmax, ties to the lowest centroid id.
+//
+// Kernel structure (one persistent CTA per SM, 1 CTA / SM):
+//   warp 0       TMA producer: the segment's centroids (B, Cs x 128, K-major,
+//                128-byte swizzle) once per segment, token tiles (A, 128 x 128)
+//                through a 2-stage ring;
+//   warp 1       allocates the 512 TMEM columns and issues tcgen05.mma
+//                (M = 128, N = min(Cs, 256), K = 16 per instruction) into one
+//                of two accumulator halves, so that the argmax of one half
+//                overlaps the products of the other;
+//   warps 2..9   epilogue: tcgen05.ld of the accumulator rows (warp w reads
+//                TMEM lanes 32*(w%4)..+31), running argmax over its column
+//                share, pairwise combine through shared memory, store.
+// Every mbarrier wait is bounded (wi_pipe.cuh); on a timeout the kernel
+// records WI_DEVERR_MBAR_TIMEOUT, waits for its own copies and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "wi_common.cuh"
 #include "wi_internal.h"
+#include "wi_pipe.cuh"
 
-bool wi_assign_tc_supported(const WiGeom&) { return false; }
+namespace {
 
-cudaError_t wi_launch_assign_tc(const WiGeom&, const void*, const void*, int32_t*, int*, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int kTM = 128;                 // tokens per tile (MMA M)
+constexpr int kStagesA = 2;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kATileBytes = kTM * WI_D * 2;  // 32 KB: two 16 KB halves of 64 columns
+constexpr int kMaxCs = 512;
+constexpr int kBBytes = kMaxCs * WI_D * 2;   // 128 KB
+
+struct TcSmem {
+  // 1024-byte aligned regions for the 128-byte swizzle
+  unsigned char b[kBBytes];                 // [k half][Cs rows][128 B]
+  unsigned char a[kStagesA][kATileBytes];   // [k half][128 rows][128 B]
+  float best_v[2][kTM];                     // epilogue combine: column group x row
+  int best_j[2][kTM];
+  uint64_t full_a[kStagesA], empty_a[kStagesA];
+  uint64_t full_b, b_free;
+  uint64_t tmem_full[2], tmem_empty[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// ---- tcgen05 / TMA helpers (inline PTX)
+
+// Shared-memory matrix descriptor, K-major operand with the 128-byte swizzle:
+// start address >> 4, leading-dimension offset (unused for this layout: 1),
+// stride between 8-row core-matrix groups (1024 B) >> 4, descriptor version 1
+// (bits 46-47), swizzle mode 2 = 128-byte (bits 61-63).
+__device__ __forceinline__ uint64_t make_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
+// and B (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at
+// bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+// 32 consecutive 32-bit accumulator columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct TcParams {
+  int32_t* assign;
+  int* err;
+  long long n;      // tokens per unit
+  int S, Cs, nseg;  // segment length, centroids per segment, segments per unit
+  int n_sink, W;
+  int total_tiles;  // (units * nseg) * (S / 128)
+  int N, halves;    // MMA N and number of accumulator halves (Cs = N * halves)
+};
+
+__global__ void __launch_bounds__(kThreads, 1) k_assign_tc(const __grid_constant__ CUtensorMap map_k,
+                                                          const __grid_constant__ CUtensorMap map_c,
+                                                          TcParams P) {
+  extern __shared__ unsigned char tc_raw[];
+  TcSmem& sm = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tiles_per_seg = P.S / kTM;
+  const int t0 = (int)((long long)P.total_tiles * blockIdx.x / gridDim.x);
+  const int t1 = (int)((long long)P.total_tiles * (blockIdx.x + 1) / gridDim.x);
+  const uint32_t idesc = make_idesc(kTM, P.N);
+  if (tid == 0) {
+    for (int s = 0; s < kStagesA; ++s) {
+      mbar_init(&sm.full_a[s], 1);
+      mbar_init(&sm.empty_a[s], 1);
+    }
+    mbar_init(&sm.full_b, 1);
+    mbar_init(&sm.b_free, 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&sm.tmem_full[h], 1);
+      mbar_init(&sm.tmem_empty[h], kEpiWarps);
+    }
+    sm.abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {  // the whole warp allocates all 512 columns
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_addr(&sm.tmem_base))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_k)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_c)) : "memory");
+      int cur_su = -1, bloads = 0, issued = 0;
+      bool ok = true;
+      const uint32_t bbytes = (uint32_t)P.Cs * WI_D * 2;
+      for (int t = t0; t < t1 && ok; ++t) {
+        const int su = t / tiles_per_seg, mt = t % tiles_per_seg;
+        if (su != cur_su) {
+          if (bloads > 0 && !mbar_wait(&sm.b_free, (bloads - 1) & 1, P.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(&sm.full_b, bbytes);
+          for (int r0 = 0; r0 < P.Cs; r0 += 256) {
+            const int rows = P.Cs - r0 < 256 ? P.Cs - r0 : 256;
+            (void)rows;
+            // k half 0 region: rows at r0 * 128 B; k half 1 region after all Cs rows
+            tma_load_2d(sm.b + r0 * 128, &map_c, 0, su * P.Cs + r0, &sm.full_b);
+            tma_load_2d(sm.b + P.Cs * 128 + r0 * 128, &map_c, 64, su * P.Cs + r0, &sm.full_b);
+          }
+          cur_su = su;
+          ++bloads;
+        }
+        const int it = t - t0, s = it % kStagesA, r = it / kStagesA;
+        if (r > 0 && !mbar_wait(&sm.empty_a[s], (r - 1) & 1, P.err)) { ok = false; break; }
+        mbar_arrive_expect_tx(&sm.full_a[s], kATileBytes);
+        const long long row0 = (long long)(su / P.nseg) * P.n + (long long)(su % P.nseg) * P.S + (long long)mt * kTM;
+        tma_load_2d(sm.a[s], &map_k, 0, (int)row0, &sm.full_a[s]);
+        tma_load_2d(sm.a[s] + kATileBytes / 2, &map_k, 64, (int)row0, &sm.full_a[s]);
+        issued = it + 1;
+      }
+      if (!ok) {
+        sm.abort_flag = 1;
+        for (int s = 0; s < kStagesA && s < issued; ++s) {
+          const int last = ((issued - 1 - s) / kStagesA) * kStagesA + s;
+          mbar_wait(&sm.full_a[s], (last / kStagesA) & 1, P.err);
+        }
+        if (bloads > 0) mbar_wait(&sm.full_b, (bloads - 1) & 1, P.err);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (one lane)
+    if (lane == 0) {
+      int cur_su = -1, bloads = 0;
+      bool ok = true;
+      for (int t = t0; t < t1 && ok; ++t) {
+        const int su = t / tiles_per_seg;
+        if (su != cur_su) {
+          if (!mbar_wait(&sm.full_b, bloads & 1, P.err)) { ok = false; break; }
+          cur_su = su;
+          ++bloads;
+          tc_fence_after();
+        }
+        const int it = t - t0, s = it % kStagesA, r = it / kStagesA;
+        if (!mbar_wait(&sm.full_a[s], r & 1, P.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a0 = smem_addr(sm.a[s]);
+        const uint32_t b0 = smem_addr(sm.b);
+        for (int h = 0; h < P.halves; ++h) {
+          if (it > 0 && !mbar_wait(&sm.tmem_empty[h], (it - 1) & 1, P.err)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < WI_D / 16; ++kk) {
+            // k step kk: 16 columns = 32 bytes inside the 128-byte swizzle row of k half kk / 4
+            const uint32_t aoff = (uint32_t)(kk >> 2) * (kATileBytes / 2) + (uint32_t)(kk & 3) * 32;
+            const uint32_t boff = (uint32_t)(kk >> 2) * (uint32_t)(P.Cs * 128) + (uint32_t)h * (uint32_t)(P.N * 128) +
+                                  (uint32_t)(kk & 3) * 32;
+            mma_bf16(tmem + (uint32_t)(h * P.N), make_desc_sw128(a0 + aoff), make_desc_sw128(b0 + boff), idesc,
+                     kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&sm.tmem_full[h]);
+        }
+        if (!ok) break;
+        mma_commit(&sm.empty_a[s]);  // the A stage is free once these products are done
+        const bool last_of_seg = (t + 1 == t1) || ((t + 1) / tiles_per_seg != su);
+        if (last_of_seg) mma_commit(&sm.b_free);
+      }
+      if (!ok) sm.abort_flag = 1;
+    }
+  } else {
+    // ---------------- epilogue: warps 2..9
+    const int ew = warp - 2;            // 0..7
+    const int quarter = warp & 3;       // TMEM lane quarter this warp may access
+    const int cgroup = ew >> 2;         // column group: 0 -> first half of each N block, 1 -> second
+    const int row = quarter * 32 + lane;
+    const int cols = P.N / 2;           // columns per group per half (multiple of 32)
+    bool ok = true;                     // after one timed-out wait the warp stops waiting but keeps
+                                        // meeting the epilogue barriers, so no warp is left behind
+    for (int t = t0; t < t1; ++t) {
+      const int it = t - t0;
+      const int su = t / tiles_per_seg, mt = t % tiles_per_seg;
+      float bv = -INFINITY;
+      int bj = 0x7fffffff;
+      for (int h = 0; h < P.halves && ok; ++h) {
+        if (!mbar_wait(&sm.tmem_full[h], it & 1, P.err)) { ok = false; sm.abort_flag = 1; break; }
+        tc_fence_after();
+        for (int c0 = 0; c0 < cols; c0 += 32) {
+          const int col = h * P.N + cgroup * cols + c0;
+          float v[32];
+          tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)col, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (v[i] > bv) { bv = v[i]; bj = col + i; }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.tmem_empty[h]);
+      }
+      sm.best_v[cgroup][row] = bv;
+      sm.best_j[cgroup][row] = bj;
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+      if (cgroup == 0) {
+        const float ov = sm.best_v[1][row];
+        const int oj = sm.best_j[1][row];
+        if (ov > bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
+        const int u = su / P.nseg, sg = su % P.nseg;
+        const long long p = (long long)sg * P.S + (long long)mt * kTM + row;
+        int a = -1;
+        if (!(p < P.n_sink || p >= P.n - P.W)) {
+          if (bj < 0 || bj >= P.Cs) { atomicOr(P.err, WI_DEVERR_BAD_CLUSTER); bj = 0; }
+          a = sg * P.Cs + bj;
+        }
+        if (ok) P.assign[(long long)u * P.n + p] = a;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over rows of 128 elements (256 B), box = 64 columns x box_rows rows, 128-byte swizzle.
+bool encode_rows(CUtensorMap* map, const void* base, unsigned long long rows, unsigned box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)WI_D, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)WI_D * 2};
+  const cuuint32_t box[2] = {64u, box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool wi_assign_tc_supported(const WiGeom& g) {
+  if (!(g.Cs == 64 || g.Cs == 128 || g.Cs == 256 || g.Cs == 512)) return false;
+  if (g.S % kTM) return false;
+  if ((long long)g.U * g.n >= (1LL << 31)) return false;  // TMA row coordinates are 32-bit
+  return get_encode() != nullptr;
+}
+
+cudaError_t wi_launch_assign_tc(const WiGeom& g, const void* K, const void* chat, int32_t* assign, int* err,
+                                cudaStream_t st) {
+  CUtensorMap map_k, map_c;
+  const int box_c = g.Cs < 256 ? g.Cs : 256;
+  if (!encode_rows(&map_k, K, (unsigned long long)g.U * g.n, kTM) ||
+      !encode_rows(&map_c, chat, (unsigned long long)g.U * g.nseg * g.Cs, (unsigned)box_c))
+    return cudaErrorInvalidValue;
+  TcParams P;
+  P.assign = assign;
+  P.err = err;
+  P.n = g.n;
+  P.S = g.S;
+  P.Cs = g.Cs;
+  P.nseg = g.nseg;
+  P.n_sink = g.n_sink;
+  P.W = g.W;
+  P.total_tiles = g.U * g.nseg * (g.S / kTM);
+  P.N = g.Cs < 256 ? g.Cs : 256;
+  P.halves = g.Cs / P.N;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = P.total_tiles < sms ? P.total_tiles : sms;
+  const size_t smem = sizeof(TcSmem) + 1024;
+  static int smem_set = 0;
+  cudaError_t e = wi_ensure_smem(k_assign_tc, smem, &smem_set);
+  if (e != cudaSuccess) return e;
+  k_assign_tc<<<grid, kThreads, smem, st>>>(map_k, map_c, P);
+  return cudaGetLastError();
 }

@@ -194,6 +194,14 @@ int wi_profile_read(wi_index* ix, double* kernel_ms, int* steps, unsigned long l
 int wi_kmeans_step_noalloc(const wi_config* cfg, const void* k, const void* centroids, int32_t* assign,
                            void* new_centroids, void* stream);
 
+/*
+ * Timing of the build that made this index (CUDA events recorded on its
+ * stream): whole build in ms, summed duration of its `iters` assignment
+ * launches in ms, and their number.  Waits for the build to finish.  Returns
+ * WI_EUNSUPPORTED for an index made by wi_index_import.  Any output may be NULL.
+ */
+int wi_index_build_stats(wi_index* ix, double* build_ms, double* assign_ms, int* assign_launches);
+
 /* Synchronise the index's last stream and report a device-side invariant
  * violation recorded by any kernel since the last call (WI_EDEVICE). */
 int wi_check_device(wi_index* ix);
