@@ -373,7 +373,9 @@ def main():
     hbm, tf_burst, tf_sust, peak_kind = peaks()
     bytes_d1 = w.units * w.clusters * INDEX_BYTES_PER_CLUSTER
     bytes_d3 = rows_per_step * dedup * ROW_BYTES
-    cand = {"score_estimate": bytes_d1, "exact_merge": bytes_d3}
+    cand = {"scores": w.units * w.clusters * (128 * 2 + 4),              # mu + count
+            "select_estimate": w.units * w.clusters * (128 * 4 + 4),     # value sums + count
+            "exact_merge": bytes_d3}
     dom = max(cand, key=lambda n: mean_us[n])
     achieved = cand[dom] / (mean_us[dom] * 1e-6) / 1e9 if mean_us[dom] > 0 else 0.0
     step_bytes = bytes_d1 + bytes_d3 + w.units * w.group * 128 * (2 + 4)

@@ -175,7 +175,7 @@ def wi_check_device(ix: int):
 
 
 WI_NUM_DECODE_KERNELS = 3
-DECODE_KERNELS = ["score_estimate", "topk_sub", "exact_merge"]
+DECODE_KERNELS = ["scores", "select_estimate", "exact_merge"]
 
 
 def wi_profile_begin(ix: int, max_steps: int):

@@ -72,7 +72,7 @@ struct wi_index {
   // build timing: events around the whole build and around every assignment launch
   std::vector<cudaEvent_t> build_ev;  // [0] start, [1] end, then (before, after) per assignment
   // decode profiling
-  std::vector<cudaEvent_t> prof_ev;  // (WI_DECODE_KERNELS + 1) per slot
+  std::vector<cudaEvent_t> prof_ev;  // WI_DECODE_EVENTS per slot
   int prof_slots = 0;
   long long prof_steps = 0;
 };
@@ -184,6 +184,13 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   if (p1 > 256) p1 = 256;
   if (p1 < 1) p1 = 1;
   b.p1 = p1;
+  // the estimation CTAs share a launch with the U*G top-k CTAs (one CTA per SM each)
+  int pe = env_int("WI_ESTIMATE_CTAS_PER_UNIT", 0);
+  if (pe <= 0) pe = (size_t)U * G < (size_t)sms ? (int)((sms - U * G) / U) : p1;
+  if (pe > tiles) pe = tiles;
+  if (pe > 256) pe = 256;
+  if (pe < 1) pe = 1;
+  b.p_es = pe;
   // exact attention: (splits + 1 steady CTA) per head, sized to fill two CTAs per SM in one wave
   int ns = env_int("WI_D3_SPLITS", 0);
   if (ns <= 0) ns = (int)((2 * (size_t)sms) / (U * G)) - 1;
@@ -191,13 +198,15 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   if (ns < 1) ns = 1;
   b.nsplit = ns;
   A(b.scores, U * G * C * 4);
-  A(b.part1, U * G * (size_t)b.p1 * WI_PART * 4);
+  A(b.ghist, U * G * 2048 * 4);
+  A(b.part1, U * G * (size_t)b.p_es * WI_PART * 4);
   A(b.sel, U * G * (size_t)g.kmax * 4);
   A(b.selcnt, U * G * 4);
   A(b.subpart, U * G * WI_PART * 4);
-  A(b.runs, U * G * (size_t)g.kmax * 8);
+  A(b.runs, U * G * (size_t)g.kmax * 16);
   A(b.splits, U * G * (size_t)(b.nsplit + 1) * 16);
   A(b.part3, U * G * (size_t)(b.nsplit + 1) * WI_PART * 4);
+  A(b.subn, U * G * (size_t)(b.nsplit + 1) * WI_PART * 4);
   A(b.ticket, U * G * 4);
   A(b.rows_total, 8);
   A(ix->q_dev, U * G * 128 * 2);
@@ -205,6 +214,8 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   A(ix->kn_dev, U * 128 * 2);
   A(ix->vn_dev, U * 128 * 2);
 #undef A
+  if (!wi_encode_rows_sw128(&b.map_mu, ix->mu, (unsigned long long)U * C, 128))
+    return fail(WI_EUNSUPPORTED, "could not encode the tensor map of the centroid table");
   b.mu = ix->mu;
   b.valsum = ix->valsum;
   b.cnt = ix->cnt;
@@ -220,6 +231,8 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   WI_CUDA(cudaMemsetAsync(ix->err, 0, 4, st));
   WI_CUDA(cudaMemsetAsync(b.selcnt, 0, U * G * 4, st));
   WI_CUDA(cudaMemsetAsync(b.ticket, 0, U * G * 4, st));
+  WI_CUDA(cudaMemsetAsync(b.ghist, 0, U * G * 2048 * 4, st));
+
   WI_CUDA(cudaMemsetAsync(b.rows_total, 0, 8, st));
   return WI_OK;
 }
@@ -453,13 +466,15 @@ int wi_decode_step(wi_index* ix, const void* q, const void* k_new, const void* v
   g_err[0] = 0;
   if (!ix || !q || !out) return fail(WI_EINVAL, "index, q and out must be non-NULL");
   if ((k_new == nullptr) != (v_new == nullptr)) return fail(WI_EINVAL, "k_new and v_new must both be set or both NULL");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+    return fail(WI_EINVAL, "q, k_new and v_new must be 16-byte aligned");
   if (k_new && ix->appended >= ix->g.max_append)
     return fail(WI_EFULL, "append buffer full (%d tokens)", ix->g.max_append);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   ix->last_stream = st;
   const cudaEvent_t* ev = nullptr;
   if (ix->prof_slots > 0) {
-    ev = ix->prof_ev.data() + (size_t)(ix->prof_steps % ix->prof_slots) * (WI_DECODE_KERNELS + 1);
+    ev = ix->prof_ev.data() + (size_t)(ix->prof_steps % ix->prof_slots) * WI_DECODE_EVENTS;
     ix->prof_steps++;
   }
   cudaError_t e = wi_launch_decode(ix->g, ix->b, q, out, st, ev);
@@ -562,7 +577,7 @@ int wi_profile_begin(wi_index* ix, int max_steps) {
   ix->prof_ev.clear();
   ix->prof_slots = 0;
   ix->prof_steps = 0;
-  const size_t n = (size_t)max_steps * (WI_DECODE_KERNELS + 1);
+  const size_t n = (size_t)max_steps * WI_DECODE_EVENTS;
   for (size_t i = 0; i < n; ++i) {
     cudaEvent_t e;
     WI_CUDA(cudaEventCreate(&e));
@@ -580,7 +595,7 @@ int wi_profile_read(wi_index* ix, double* kernel_ms, int* steps, unsigned long l
   if (kernel_ms) {
     for (int k = 0; k < WI_DECODE_KERNELS; ++k) kernel_ms[k] = 0.0;
     for (int sl = 0; sl < filled; ++sl) {
-      const cudaEvent_t* ev = ix->prof_ev.data() + (size_t)sl * (WI_DECODE_KERNELS + 1);
+      const cudaEvent_t* ev = ix->prof_ev.data() + (size_t)sl * WI_DECODE_EVENTS;
       for (int k = 0; k < WI_DECODE_KERNELS; ++k) {
         float ms = 0.f;
         WI_CUDA(cudaEventElapsedTime(&ms, ev[k], ev[k + 1]));

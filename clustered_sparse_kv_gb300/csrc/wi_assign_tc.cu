@@ -24,16 +24,18 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <cstddef>
 #include <mutex>
 
 #include "wi_common.cuh"
 #include "wi_internal.h"
 #include "wi_pipe.cuh"
+#include "wi_tc.cuh"
 
 namespace {
 
 constexpr int kTM = 128;                 // tokens per tile (MMA M)
-constexpr int kStagesA = 2;
+constexpr int kStagesA = 3;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kATileBytes = kTM * WI_D * 2;  // 32 KB: two 16 KB halves of 64 columns
@@ -41,9 +43,7 @@ constexpr int kMaxCs = 512;
 constexpr int kBBytes = kMaxCs * WI_D * 2;   // 128 KB
 
 struct TcSmem {
-  // 1024-byte aligned regions for the 128-byte swizzle
-  unsigned char b[kBBytes];                 // [k half][Cs rows][128 B]
-  unsigned char a[kStagesA][kATileBytes];   // [k half][128 rows][128 B]
+  // small state first (3 KB), then the 1024-byte aligned tiles for the 128-byte swizzle
   float best_v[2][kTM];                     // epilogue combine: column group x row
   int best_j[2][kTM];
   uint64_t full_a[kStagesA], empty_a[kStagesA];
@@ -51,73 +51,11 @@ struct TcSmem {
   uint64_t tmem_full[2], tmem_empty[2];
   uint32_t tmem_base;
   int abort_flag;
+  unsigned char pad[3072 - 2 * kTM * 8 - (2 * kStagesA + 6) * 8 - 8];
+  unsigned char b[kBBytes];                 // [k half][Cs rows][128 B]
+  unsigned char a[kStagesA][kATileBytes];   // [k half][128 rows][128 B]
 };
-
-// ---- tcgen05 / TMA helpers (inline PTX)
-
-// Shared-memory matrix descriptor, K-major operand with the 128-byte swizzle:
-// start address >> 4, leading-dimension offset (unused for this layout: 1),
-// stride between 8-row core-matrix groups (1024 B) >> 4, descriptor version 1
-// (bits 46-47), swizzle mode 2 = 128-byte (bits 61-63).
-__device__ __forceinline__ uint64_t make_desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
-  d |= (uint64_t)1 << 16;
-  d |= (uint64_t)(1024 >> 4) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
-// and B (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at
-// bits 17-22, M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-      "[%4];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on `bar` once every tcgen05 operation issued so far by this thread has completed.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-
-// 32 consecutive 32-bit accumulator columns of this warp's 32 TMEM lanes.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
+static_assert(offsetof(TcSmem, b) == 3072, "tile region must start 1024-byte aligned");
 
 struct TcParams {
   int32_t* assign;
@@ -132,9 +70,13 @@ struct TcParams {
 __global__ void __launch_bounds__(kThreads, 1) k_assign_tc(const __grid_constant__ CUtensorMap map_k,
                                                           const __grid_constant__ CUtensorMap map_c,
                                                           TcParams P) {
-  extern __shared__ unsigned char tc_raw[];
-  TcSmem& sm = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) unsigned char tc_raw[];
+  TcSmem& sm = *reinterpret_cast<TcSmem*>(tc_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (smem_addr(sm.b) & 1023u) {  // the swizzled tiles need 1024-byte alignment; never run misaligned
+    if (tid == 0) atomicOr(P.err, WI_DEVERR_BAD_ROW);
+    return;
+  }
   const int tiles_per_seg = P.S / kTM;
   const int t0 = (int)((long long)P.total_tiles * blockIdx.x / gridDim.x);
   const int t1 = (int)((long long)P.total_tiles * (blockIdx.x + 1) / gridDim.x);
@@ -259,13 +201,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_assign_tc(const __grid_constant
       for (int h = 0; h < P.halves && ok; ++h) {
         if (!mbar_wait(&sm.tmem_full[h], it & 1, P.err)) { ok = false; sm.abort_flag = 1; break; }
         tc_fence_after();
-        for (int c0 = 0; c0 < cols; c0 += 32) {
+        for (int c0 = 0; c0 < cols; c0 += 64) {
+          // two 32-column loads in flight, then one wait
           const int col = h * P.N + cgroup * cols + c0;
-          float v[32];
-          tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)col, v);
+          const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)col;
+          uint32_t r0[32], r1[32];
+          tmem_ld32_nowait(ta, r0);
+          if (c0 + 32 < cols) tmem_ld32_nowait(ta + 32, r1);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (v[i] > bv) { bv = v[i]; bj = col + i; }
+          for (int i = 0; i < 32; ++i) {
+            const float v = __uint_as_float(r0[i]);
+            if (v > bv) { bv = v; bj = col + i; }
+          }
+          if (c0 + 32 < cols) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float v = __uint_as_float(r1[i]);
+              if (v > bv) { bv = v; bj = col + 32 + i; }
+            }
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -298,6 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_assign_tc(const __grid_constant
   }
 }
 
+}  // namespace
+
+
+namespace {
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -314,7 +273,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 // 2-D bf16 tensor map over rows of 128 elements (256 B), box = 64 columns x box_rows rows, 128-byte swizzle.
-bool encode_rows(CUtensorMap* map, const void* base, unsigned long long rows, unsigned box_rows) {
+bool encode_rows_impl(CUtensorMap* map, const void* base, unsigned long long rows, unsigned box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
   if (!enc) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)WI_D, (cuuint64_t)rows};
@@ -328,19 +287,25 @@ bool encode_rows(CUtensorMap* map, const void* base, unsigned long long rows, un
 
 }  // namespace
 
+bool wi_encode_rows_sw128(CUtensorMap* map, const void* base, unsigned long long rows, unsigned box_rows) {
+  return encode_rows_impl(map, base, rows, box_rows);
+}
+
+bool wi_tensor_maps_available() { return get_encode() != nullptr; }
+
 bool wi_assign_tc_supported(const WiGeom& g) {
   if (!(g.Cs == 64 || g.Cs == 128 || g.Cs == 256 || g.Cs == 512)) return false;
   if (g.S % kTM) return false;
   if ((long long)g.U * g.n >= (1LL << 31)) return false;  // TMA row coordinates are 32-bit
-  return get_encode() != nullptr;
+  return wi_tensor_maps_available();
 }
 
 cudaError_t wi_launch_assign_tc(const WiGeom& g, const void* K, const void* chat, int32_t* assign, int* err,
                                 cudaStream_t st) {
   CUtensorMap map_k, map_c;
   const int box_c = g.Cs < 256 ? g.Cs : 256;
-  if (!encode_rows(&map_k, K, (unsigned long long)g.U * g.n, kTM) ||
-      !encode_rows(&map_c, chat, (unsigned long long)g.U * g.nseg * g.Cs, (unsigned)box_c))
+  if (!wi_encode_rows_sw128(&map_k, K, (unsigned long long)g.U * g.n, kTM) ||
+      !wi_encode_rows_sw128(&map_c, chat, (unsigned long long)g.U * g.nseg * g.Cs, (unsigned)box_c))
     return cudaErrorInvalidValue;
   TcParams P;
   P.assign = assign;
@@ -358,7 +323,7 @@ cudaError_t wi_launch_assign_tc(const WiGeom& g, const void* K, const void* chat
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = P.total_tiles < sms ? P.total_tiles : sms;
-  const size_t smem = sizeof(TcSmem) + 1024;
+  const size_t smem = sizeof(TcSmem);
   static int smem_set = 0;
   cudaError_t e = wi_ensure_smem(k_assign_tc, smem, &smem_set);
   if (e != cudaSuccess) return e;

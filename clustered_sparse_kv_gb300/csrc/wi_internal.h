@@ -1,5 +1,6 @@
 // wi_internal.h -- host-side declarations shared by the wave-index sources.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -39,6 +40,8 @@ cudaError_t wi_launch_permute(const WiGeom& g, void* K, void* V, const int* perm
                               int u0, int nu, cudaStream_t st);
 size_t wi_assign_smem_bytes(const WiGeom& g);
 
+bool wi_encode_rows_sw128(CUtensorMap* map, const void* base, unsigned long long rows, unsigned box_rows);
+
 // ---- tensor-core assignment (wi_assign_tc.cu)
 bool wi_assign_tc_supported(const WiGeom& g);
 cudaError_t wi_launch_assign_tc(const WiGeom& g, const void* K, const void* chat, int32_t* assign, int* err,
@@ -46,6 +49,7 @@ cudaError_t wi_launch_assign_tc(const WiGeom& g, const void* K, const void* chat
 
 // ---- decode kernels (wi_decode.cu)
 struct WiDecodeBufs {
+  CUtensorMap map_mu;     // mu as rows of 128 bf16, 128-row boxes, 128-byte swizzle (tensor-core scores)
   const void* mu;
   const float* valsum;
   const int* cnt;
@@ -57,24 +61,28 @@ struct WiDecodeBufs {
   void* appV;
   int* app_count;
   float* scores;          // [U][G][C]
-  float* part1;           // [U][G][p1][WI_PART]  estimation partials of score_estimate
+  int* ghist;             // [U][G][2048] first radix digit of the score keys (built by k_scores)
+  float* part1;           // [U][G][p_es][WI_PART]  estimation partials
   int* sel;               // [U][G][kmax]
   int* selcnt;            // [U][G]
   float* subpart;         // [U][G][WI_PART]      estimation terms of the selected clusters
-  int2* runs;             // [U][G][kmax]  (first row, rows) of each selected cluster
+  int4* runs;             // [U][G][kmax]  (first row, rows, weight bits, id) of each selected cluster
   int4* splits;           // [U][G][nsplit+1]  row-balanced split starts over the selected rows
   float* part3;           // [U][G][nsplit+1][WI_PART]  exact partials (the last split: steady rows)
+  float* subn;            // [U][G][nsplit+1][WI_PART]  retrieved clusters' value-sum terms per split
   unsigned int* ticket;   // [U][G]  CTAs of exact_merge finished, per head
   unsigned long long* rows_total;  // running sum of exact rows loaded over all steps
   int* err;
-  int p1;                 // score_estimate CTAs per unit
+  int p1;                 // k_scores CTAs per unit
+  int p_es;               // estimation CTAs per unit (= estimation partials per head)
   int nsplit;             // exact_merge CTAs per head over the selected rows (plus one for steady rows)
 };
 #define WI_PART 132  // floats per zone partial: m, Z, 2 pad, N[128]
 
-#define WI_DECODE_KERNELS 3  // score_estimate, topk_sub, exact_merge
+#define WI_DECODE_KERNELS 3  // scores, select_estimate (top-k + estimation CTAs), exact_merge
+#define WI_DECODE_EVENTS 4   // per profiled step: before the first kernel, then after each kernel
 cudaError_t wi_launch_decode(const WiGeom& g, const WiDecodeBufs& b, const void* q, float* out, cudaStream_t st,
-                             const cudaEvent_t* ev /* NULL or WI_DECODE_KERNELS + 1 events */);
+                             const cudaEvent_t* ev);
 cudaError_t wi_launch_append(const WiGeom& g, const WiDecodeBufs& b, const void* k_new, const void* v_new, int t,
                              cudaStream_t st);
 

@@ -91,3 +91,10 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[NV]) {
 // no-ops for a kernel launched without the attribute.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Device-scope acquire-release fetch-and-add (returns the old value).
+__device__ __forceinline__ unsigned ticket_acq_rel(unsigned* p) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+  return old;
+}

@@ -113,7 +113,7 @@ int wi_index_export(const wi_index* ix, int32_t* counts, int32_t* offsets, int32
 
 /*
  * One decode step.  q: device bf16 [batch][layers][n_q_heads][128], the
- * queries of the step (already rotated); out: device fp32 [batch][layers]
+ * queries of the step (already rotated), 16-byte aligned; out: device fp32 [batch][layers]
  * [n_q_heads][128], attention output per query head.  Attention runs over
  * the current context: the n_ctx built tokens plus every token appended so
  * far.  If k_new and v_new (device bf16 [batch][layers][n_kv_heads][128]) are
@@ -160,9 +160,10 @@ int wi_kmeans_step(const wi_config* cfg, const void* k, const void* centroids, i
 /*
  * Per-kernel timing of decode steps (benchmarking aid).  After
  * wi_profile_begin(ix, max_steps), every decode step on this index records
- * CUDA events around each of its WI_NUM_DECODE_KERNELS kernels (score +
- * estimate, top-k with the retrieved clusters' estimation terms, exact
- * attention with the final merge) into slot
+ * CUDA events around each of its WI_NUM_DECODE_KERNELS kernels (centroid
+ * scores; top-k with the retrieved clusters' estimation terms, sharing one
+ * launch with the estimation over all clusters; exact attention with the
+ * final merge) into slot
  * (step number % max_steps); steps captured into a CUDA graph record them on
  * every replay.  wi_profile_read synchronises the device and returns, per
  * kernel, the summed duration in milliseconds over the filled slots
