@@ -127,6 +127,10 @@ int wi_geom_from_config(const wi_config* c, WiGeom* g, char* msg, size_t msglen)
     snprintf(msg, msglen, "retrieval budget must be <= 4096 clusters (got %d)", g->kmax);
     return WI_EUNSUPPORTED;
   }
+  if (g->C > 65536) {
+    snprintf(msg, msglen, "at most 65536 clusters per kv head (got %d)", g->C);
+    return WI_EUNSUPPORTED;
+  }
   if (g->S > 16384) {
     snprintf(msg, msglen, "seg_len must be <= 16384 (got %d)", g->S);
     return WI_EUNSUPPORTED;

@@ -38,7 +38,7 @@ namespace {
 constexpr int kSWarps = 16;
 constexpr int kSTile = 8 * kSWarps;
 constexpr int kSThreads = 32 * (kSWarps + 1);
-constexpr int kTopkBins = 2048;  // first radix digit: the top 11 bits of the score key
+constexpr int kTopkBins = 2048;  // histogram bins of the top-k passes
 
 // G query heads per kv head, in blocks of 4 heads (HB blocks); GP = heads per
 // block rounded up to a power of two; NV = values per transpose-reduction
@@ -66,14 +66,13 @@ __device__ void drain_stages(uint64_t* full, int issued, int* err) {
   }
 }
 
-// ---- k_scores: s_hj = q_h . mu_j for every cluster on the tensor cores, and
-// the histogram of the first radix digit of the score keys per head (for the
-// top-k).  Per 128-cluster tile: TMA loads the mean keys (A, 128 x 128 bf16,
-// K-major, 128-byte swizzle) and the counts; one thread issues eight
-// tcgen05.mma (M = 128 clusters, N = 16 heads (G used, the rest zero), K = 16)
-// into one of two 16-column TMEM accumulators; four epilogue warps read one
-// cluster row each per lane (tcgen05.ld 32x32b.x16) and store the G scores.
-// Warp 0: TMA producer; warp 1: TMEM allocation + MMA; warps 2..5: epilogue.
+// ---- k_scores: s_hj = q_h . mu_j for every cluster on the tensor cores.
+// Per 128-cluster tile: TMA loads the mean keys (A, 128 x 128 bf16, K-major,
+// 128-byte swizzle); one thread issues eight tcgen05.mma (M = 128 clusters,
+// N = 16 heads (G used, the rest zero), K = 16) into one of two 16-column TMEM
+// accumulators; four epilogue warps read one cluster row each per lane
+// (tcgen05.ld 32x32b.x16) and store the G scores.  Warp 0: TMA producer;
+// warp 1: TMEM allocation + MMA; warps 2..5: epilogue.
 constexpr int kScTile = 128;
 constexpr int kScEpiWarps = 4;
 constexpr int kScThreads = 32 * (2 + kScEpiWarps);
@@ -83,26 +82,22 @@ constexpr int kScQBytes = kScN * WI_D * 2;      // 4 KB, the B operand
 
 template <int G>
 struct ScCfg {
-  static constexpr int STAGES = G > 4 ? 4 : 5;
+  static constexpr int STAGES = 6;
   static constexpr size_t A_OFF = kScQBytes;
-  static constexpr size_t HIST_OFF = A_OFF + (size_t)STAGES * kScATile;
-  static constexpr size_t CNT_OFF = HIST_OFF + sizeof(int) * G * kTopkBins;
-  static constexpr size_t BAR_OFF = CNT_OFF + sizeof(int) * STAGES * kScTile;
+  static constexpr size_t BAR_OFF = A_OFF + (size_t)STAGES * kScATile;
   static constexpr size_t SMEM = BAR_OFF + sizeof(uint64_t) * (2 * STAGES + 4) + 16;
 };
 
 template <int G>
 __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant__ CUtensorMap map_mu,
-                                                         const bf16* __restrict__ q, const int* __restrict__ cnt,
-                                                         float* __restrict__ scores, int* __restrict__ ghist, int C,
+                                                         const bf16* __restrict__ q,
+                                                         float* __restrict__ scores, int C,
                                                          int P, int* err) {
   using CF = ScCfg<G>;
   constexpr int STAGES = CF::STAGES;
   extern __shared__ __align__(1024) unsigned char sc_raw[];
   unsigned char* qB = sc_raw;                                              // [k half][16 rows][128 B]
   unsigned char* A = sc_raw + CF::A_OFF;                                   // [stage][k half][128 rows][128 B]
-  int* hist = reinterpret_cast<int*>(sc_raw + CF::HIST_OFF);              // [G][kTopkBins]
-  int* cnts = reinterpret_cast<int*>(sc_raw + CF::CNT_OFF);               // [stage][128]
   uint64_t* full = reinterpret_cast<uint64_t*>(sc_raw + CF::BAR_OFF);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
@@ -122,7 +117,7 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + kScEpiWarps);  // the MMA commit and every epilogue warp
+      mbar_init(&empty[s], 1);  // the MMA commit: the tile has been read
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -144,10 +139,9 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
   auto issue = [&](int it) {
     const int s = it % STAGES;
     const int j0 = c0 + it * kScTile, nj = min(kScTile, c1 - j0);
-    mbar_arrive_expect_tx(&full[s], (uint32_t)(kScATile + nj * 4));
+    mbar_arrive_expect_tx(&full[s], (uint32_t)kScATile);
     tma_load_2d(A + (size_t)s * kScATile, &map_mu, 0, u * C + j0, &full[s]);
     tma_load_2d(A + (size_t)s * kScATile + kScATile / 2, &map_mu, 64, u * C + j0, &full[s]);
-    bulk_g2s(cnts + s * kScTile, cnt + (size_t)u * C + j0, nj * 4, &full[s]);
   };
   if (warp == 0 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_mu)) : "memory");
@@ -156,7 +150,6 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
   // the queries may come from the previous kernel: B operand = q of the G heads, rows >= G zero,
   // written in the 128-byte-swizzled K-major layout (row n, 16-byte chunk c at chunk c ^ (n & 7))
   pdl_wait();
-  for (int i = tid; i < G * kTopkBins; i += kScThreads) hist[i] = 0;
   for (int i = tid; i < kScN * 16; i += kScThreads) {
     const int n = i >> 4, c = i & 15;  // head row, 16-byte chunk over the 256-byte row
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -202,12 +195,12 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
     const int quarter = warp & 3;
     bool ok = true;
     for (int it = 0; it < ntile; ++it) {
-      const int s = it % STAGES, r = it / STAGES, b = it & 1;
+      const int b = it & 1;
       const int j0 = c0 + it * kScTile, nj = min(kScTile, c1 - j0);
       const int row = quarter * 32 + lane;
       uint32_t rr[16];
       if (ok) {
-        if (!mbar_wait(&tfull[b], (it >> 1) & 1, err) || !mbar_wait(&full[s], r & 1, err)) {
+        if (!mbar_wait(&tfull[b], (it >> 1) & 1, err)) {
           ok = false;
           *s_abort = 1;
         }
@@ -220,17 +213,10 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[b]);
-      const int cn = (ok && row < nj) ? cnts[s * kScTile + row] : 0;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
       const bool valid = ok && row < nj;
+      if (valid) {
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float sdot = __uint_as_float(rr[h]);
-        if (valid) scores[((size_t)u * G + h) * C + j0 + row] = sdot;
-        const int slot = (valid && cn > 0) ? h * kTopkBins + (int)(float_key(sdot) >> 21) : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, slot);  // lanes of one digit add once
-        if (slot >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[slot], __popc(peers));
+        for (int h = 0; h < G; ++h) scores[((size_t)u * G + h) * C + j0 + row] = __uint_as_float(rr[h]);
       }
     }
   }
@@ -239,11 +225,6 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"(tmem) : "memory");
-  }
-  if (*s_abort) return;
-  for (int i = tid; i < G * kTopkBins; i += kScThreads) {
-    const int c = hist[i];
-    if (c) atomicAdd(&ghist[((size_t)u * G + i / kTopkBins) * kTopkBins + (i % kTopkBins)], c);
   }
 }
 
@@ -411,28 +392,47 @@ __device__ void estimate_role(unsigned char* raw, const float* __restrict__ vals
   }
 }
 
-// -- select role: top-k of one head.  KPT consecutive clusters per thread
-// (threads 0..511; the remaining warp only meets the barriers), held as
-// order-preserving keys in registers (0 = empty cluster / padding).  Three
-// radix passes (11, 11, 10 bits) find the k-th largest key T -- the first
-// digit's histogram comes from k_scores -- then the keys > T and the first (in
-// id order) keys == T are written in id order, with each selected cluster's
-// row run and weight (first row, rows, e^{lam s_j - m_sub}, id), m_sub =
-// lam * s_max, and the starts of NS row-balanced splits of the selected rows.
-// Also Z_sub = sum n_j e^{lam s_j - m_sub} over the selected clusters; their
-// value-sum terms are summed where their rows are loaded (exact attention),
-// and both are subtracted from the estimate at the merge.
-constexpr int kSelThreads = 512;
+// -- select role: top-k of one head.  The k largest keys (order-preserving
+// bits of the scores; 0 = empty cluster) are the k smallest distances
+// d = key_max - key.  One pass counts d on a logarithmic scale (2048 bins: the
+// position of d's leading one, then its next 6 bits; monotone in d), which
+// finds the bin holding the k-th key; the few keys in that bin are ranked by
+// (key descending, id ascending) to pin the k-th one exactly (a radix select
+// over (d, id) takes over when the bin holds more keys than threads).  The
+// selected clusters are then listed in id order (a ballot per 32 ids and a
+// prefix over those counts), each with its row run and weight (first row,
+// rows, e^{lam s_j - m_sub}, id), m_sub = lam * s_max, together with the
+// starts of NS row-balanced splits of the selected rows and
+// Z_sub = sum n_j e^{lam s_j - m_sub} over them; their value-sum terms are
+// summed where their rows are loaded (exact attention), and both are
+// subtracted from the estimate at the merge.
+//
+// Every loop runs over the clusters with the CTA's stride and is kept rolled:
+// the role runs once per CTA, from a cold instruction cache, so code size is
+// latency.  The keys are cached in shared memory when C <= kSelKeysMax, else
+// recomputed from the (L2-resident) scores and counts at every pass.
+constexpr int kSelThreads = 512;  // ranking capacity: candidates in the threshold bin
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kBinsPerLane = kTopkBins / kSelThreads;  // 4
+constexpr int kSelKeysMax = 32768;
+constexpr int kSNW = kSThreads / 32;  // warps of the CTA
 
 // Inverse of float_key for finite scores.
 __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
+// Logarithmic bin of a distance: 64 * (position of the leading one) + the next
+// six bits (d = 0 and 1 share bin 0).  Non-decreasing in d; within a bin of
+// leading position m >= 6 only the low m - 6 bits of d vary.
+__device__ __forceinline__ int log_bin(uint32_t d) {
+  if (d == 0u) return 0;
+  const int m = 31 - __clz(d);
+  const uint32_t sub = m >= 6 ? (d >> (m - 6)) & 63u : (d << (6 - m)) & 63u;
+  return m * 64 + (int)sub;
+}
+
 struct TopkArgs {
-  int* ghist;    // [U][G][kTopkBins] first-digit histogram from k_scores; cleared here after use
   const float* scores;
   const int* cnt;
   const int* off;
@@ -449,242 +449,335 @@ struct TopkArgs {
   float lam;
 };
 
-// Inclusive warp scan of 64-bit counts.
-__device__ __forceinline__ unsigned long long warp_scan_u64(unsigned long long v) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long t = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += t;
-  }
-  return v;
+struct alignas(16) SelSmem {
+  int hist[2][kTopkBins];
+  int s_wsum[32];
+  uint32_t s_wmax[32];
+  int s_bin, s_above, s_ncand, s_found;
+  uint32_t s_tkey;
+  int s_tid;
+  int s_wt[32];
+  float s_wf[32];
+  uint32_t ckey[kSelThreads];
+  int cid[kSelThreads];
+};
+
+static_assert(sizeof(SelSmem) % 16 == 0, "the cached keys follow SelSmem 16-byte aligned");
+// Shared memory of the select role beyond SelSmem (a multiple of 16 bytes):
+// the keys (16-byte aligned, when cached), then per 32-id chunk the take bits
+// and their prefix, then the selected ids in position order and their first
+// rows among the selected rows.
+__host__ __device__ inline size_t sel_keys_bytes(int C) { return C <= kSelKeysMax ? (size_t)C * 4 : 0; }
+__host__ __device__ inline size_t sel_smem_bytes(int C, int kmax) {
+  const size_t nch = ((size_t)C + 31) / 32;
+  return sizeof(SelSmem) + sel_keys_bytes(C) + nch * 8 + (size_t)kmax * 8;
 }
 
-// Exclusive block-wide prefix of a 64-bit count per thread, one barrier: warp
-// totals go through `wt` (>= 32 entries); returns the prefix, sets *total.
-__device__ __forceinline__ unsigned long long block_prefix_u64(unsigned long long v, unsigned long long* wt,
-                                                               unsigned long long* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const unsigned long long inc = warp_scan_u64(v);
-  if (lane == 31) wt[warp] = inc;
+// Block-wide search over 2048 ascending bins (thread t < 512 owns bins 4t..4t+3):
+// the bin where the running count first reaches `target` and the count below
+// it.  Block-uniform result; false if the counts never reach `target`.
+__device__ __forceinline__ bool find_bin(const int* hist, int target, SelSmem& sm, int* bin, int* above) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int c[kBinsPerLane] = {0, 0, 0, 0};
+  if (warp < kSelWarps) {
+    const int4 h4 = *reinterpret_cast<const int4*>(hist + kBinsPerLane * tid);
+    c[0] = h4.x; c[1] = h4.y; c[2] = h4.z; c[3] = h4.w;
+  }
+  const int lsum = c[0] + c[1] + c[2] + c[3];
+  const int inc = warp_inclusive_scan(lsum);
+  if (lane == 31 && warp < kSelWarps) sm.s_wsum[warp] = inc;
   __syncthreads();
-  const unsigned long long x = lane < nw ? wt[lane] : 0ull;
-  unsigned long long before = lane < warp ? x : 0ull, all = x;
+  const int ws = lane < kSelWarps ? sm.s_wsum[lane] : 0;
+  const int wincl = warp_inclusive_scan(ws);
+  const unsigned hit = __ballot_sync(0xffffffffu, wincl >= target);
+  if (hit == 0u) return false;  // uniform: every warp sees the same totals
+  const int wstar = __ffs(hit) - 1;
+  if (warp == wstar) {
+    int ex = __shfl_sync(0xffffffffu, wincl - ws, wstar) + inc - lsum;
+#pragma unroll
+    for (int i = 0; i < kBinsPerLane; ++i) {
+      if (ex < target && target <= ex + c[i]) { sm.s_bin = kBinsPerLane * tid + i; sm.s_above = ex; }
+      ex += c[i];
+    }
+  }
+  __syncthreads();
+  *bin = sm.s_bin;
+  *above = sm.s_above;
+  return true;
+}
+
+// Exclusive prefix, in place, of n ints in shared memory (each thread sums a
+// contiguous run); returns the total.  Ends with a barrier.
+__device__ __forceinline__ int block_excl_scan(int* v, int n, SelSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (n + kSThreads - 1) / kSThreads;
+  const int b0 = min(n, tid * per), b1 = min(n, b0 + per);
+  int sum = 0;
+  for (int i = b0; i < b1; ++i) sum += v[i];
+  const int inc = warp_inclusive_scan(sum);
+  if (lane == 31) sm.s_wt[warp] = inc;
+  __syncthreads();
+  const int x = lane < kSNW ? sm.s_wt[lane] : 0;
+  int before = lane < warp ? x : 0, total = x;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     before += __shfl_xor_sync(0xffffffffu, before, o);
-    all += __shfl_xor_sync(0xffffffffu, all, o);
+    total += __shfl_xor_sync(0xffffffffu, total, o);
   }
-  *total = all;
-  return before + inc - v;
+  int run = before + inc - sum;
+  for (int i = b0; i < b1; ++i) {
+    const int t = v[i];
+    v[i] = run;
+    run += t;
+  }
+  __syncthreads();
+  return total;
 }
 
-struct SelSmem {
-  int hist[2][kTopkBins];
-  int s_wsum[32];
-  int s_bin, s_above;
-  uint32_t s_maxkey;
-  int pad;
-  unsigned long long s_wt[3][32];
-  float zred[32];
+struct KeySrc {
+  const uint32_t* ks;  // cached keys, or null
+  const float* s;
+  const int* cn;
+  __device__ __forceinline__ uint32_t operator()(int j) const {
+    if (ks) return ks[j];
+    return __ldg(cn + j) > 0 ? float_key(__ldcg(s + j)) : 0u;
+  }
 };
 
-template <int KPT>
-__device__ void select_role(unsigned char* raw, const TopkArgs& a, int u, int h) {
-  static_assert(KPT % 4 == 0, "vector loads of 4");
+__device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& a, int u, int h) {
   SelSmem& sm = *reinterpret_cast<SelSmem*>(raw);
-  int* s_row = reinterpret_cast<int*>(raw + sizeof(SelSmem));  // [kmax + 1] row prefix in selection order
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t uh = (size_t)u * a.G + h;
-  const int C = a.C;
+  const int C = a.C, nch = (C + 31) / 32;
+  uint32_t* ks = reinterpret_cast<uint32_t*>(raw + sizeof(SelSmem));                 // [C] if cached
+  uint32_t* tmask = reinterpret_cast<uint32_t*>(raw + sizeof(SelSmem) + sel_keys_bytes(C));  // [nch]
+  int* cpre = reinterpret_cast<int*>(tmask + nch);                                     // [nch]
+  int* sel_s = cpre + nch;                                                             // [kmax]
   const float* s = a.scores + uh * C;
   const int* cn = a.cnt + (size_t)u * C;
   int* out = a.sel + uh * a.kmax;
-  // every global read this CTA needs is issued here, before the first use (all of it is in L2:
-  // the scores and the histogram were just written, the counts just read, by k_scores)
-  uint32_t key[KPT];
-  int nc[KPT];
-  int4 g4 = make_int4(0, 0, 0, 0);
-  const bool scan_lane = warp < kSelWarps;
-  const int rb0 = kBinsPerLane * tid;  // this lane's reversed bins rb0 .. rb0+3 (bins 2047-rb0 .. 2044-rb0)
-  int* gh = a.ghist + uh * kTopkBins;
-  if (scan_lane) g4 = __ldcg(reinterpret_cast<const int4*>(gh + kTopkBins - kBinsPerLane - rb0));
-  const int base = tid * KPT;
-  if (base + KPT <= C) {
-#pragma unroll
-    for (int e = 0; e < KPT; e += 4) {
-      const int4 c4 = __ldg(reinterpret_cast<const int4*>(cn + base + e));
-      const float4 f4 = __ldcg(reinterpret_cast<const float4*>(s + base + e));
-      nc[e] = c4.x; nc[e + 1] = c4.y; nc[e + 2] = c4.z; nc[e + 3] = c4.w;
-      key[e] = float_key(f4.x); key[e + 1] = float_key(f4.y);
-      key[e + 2] = float_key(f4.z); key[e + 3] = float_key(f4.w);
+  const bool cached = C <= kSelKeysMax;
+  const KeySrc key_of{cached ? ks : nullptr, s, cn};
+  int kk = min(a.kmax, a.nonempty[u]);
+  for (int i = tid; i < 2 * kTopkBins; i += kSThreads) (&sm.hist[0][0])[i] = 0;
+  if (tid == 0) { sm.s_ncand = 0; sm.s_found = 0; }
+  // ---- keys (C is a multiple of 16) and their maximum
+  uint32_t kmx = 0u;
+  if (cached) {
+#pragma unroll 4
+    for (int i = tid; i < C / 4; i += kSThreads) {
+      const float4 f4 = __ldcg(reinterpret_cast<const float4*>(s) + i);
+      const int4 c4 = __ldg(reinterpret_cast<const int4*>(cn) + i);
+      uint4 k4;
+      k4.x = c4.x > 0 ? float_key(f4.x) : 0u;
+      k4.y = c4.y > 0 ? float_key(f4.y) : 0u;
+      k4.z = c4.z > 0 ? float_key(f4.z) : 0u;
+      k4.w = c4.w > 0 ? float_key(f4.w) : 0u;
+      reinterpret_cast<uint4*>(ks)[i] = k4;
+      kmx = max(kmx, max(max(k4.x, k4.y), max(k4.z, k4.w)));
     }
   } else {
-#pragma unroll
-    for (int e = 0; e < KPT; ++e) {
-      const int j = base + e;
-      nc[e] = j < C ? __ldg(cn + j) : 0;
-      key[e] = j < C ? float_key(__ldcg(s + j)) : 0u;
-    }
-  }
-  int kk = min(a.kmax, a.nonempty[u]);
-#pragma unroll
-  for (int e = 0; e < KPT; ++e)
-    if (nc[e] <= 0) key[e] = 0u;  // empty clusters are never candidates
-  if (scan_lane) *reinterpret_cast<int4*>(gh + kTopkBins - kBinsPerLane - rb0) = make_int4(0, 0, 0, 0);
-  for (int i = tid; i < a.kmax; i += kSThreads) out[i] = -1;
-  for (int i = tid; i < kTopkBins; i += kSThreads) sm.hist[1][i] = 0;
-  if (tid == 0) { a.selcnt[uh] = kk; sm.s_maxkey = 0u; }
-  // ---- radix select: three passes of (count, barrier, scan, barrier, pick, barrier)
-  uint32_t prefix = 0, pmask = 0;
-  int remaining = kk;
-  bool found = true;
-#pragma unroll 1
-  for (int pass = 0; pass < 3 && kk > 0; ++pass) {
-    const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const uint32_t dmask = pass == 2 ? 1023u : 2047u;
-    int* hc = sm.hist[pass & 1];
-    int* hn = sm.hist[(pass + 1) & 1];
-    if (pass > 0) {
-#pragma unroll
-      for (int e = 0; e < KPT; ++e)
-        if (key[e] != 0u && (key[e] & pmask) == prefix) atomicAdd(&hc[(key[e] >> sh) & dmask], 1);
-    }
-    __syncthreads();
-    int c[kBinsPerLane];
-    if (pass == 0) {  // the first digit's counts came from k_scores, in ascending bin order
-      c[0] = g4.w; c[1] = g4.z; c[2] = g4.y; c[3] = g4.x;
-    } else {
-#pragma unroll
-      for (int i = 0; i < kBinsPerLane; ++i) c[i] = scan_lane ? hc[kTopkBins - 1 - rb0 - i] : 0;
-    }
-    int lsum = 0;
-#pragma unroll
-    for (int i = 0; i < kBinsPerLane; ++i) lsum += c[i];
-    const int inc = warp_inclusive_scan(lsum);
-    if (lane == 31) sm.s_wsum[warp] = inc;
-    if (pass + 1 < 3)
-      for (int i = tid; i < kTopkBins; i += kSThreads) hn[i] = 0;
-    __syncthreads();
-    const int ws = lane < kSelWarps ? sm.s_wsum[lane] : 0;
-    const int wincl = warp_inclusive_scan(ws);
-    const unsigned hit = __ballot_sync(0xffffffffu, wincl >= remaining);
-    const int wstar = __ffs(hit) - 1;  // warp whose bins hold the remaining-th largest key
-    if (wstar < 0) {                   // inconsistent counts: select nothing, report it
-      found = false;
-      break;
-    }
-    if (warp == wstar) {
-      int ex = __shfl_sync(0xffffffffu, wincl - ws, wstar) + inc - lsum;
-#pragma unroll
-      for (int i = 0; i < kBinsPerLane; ++i) {
-        if (ex < remaining && remaining <= ex + c[i]) { sm.s_bin = kTopkBins - 1 - rb0 - i; sm.s_above = ex; }
-        ex += c[i];
-      }
-    }
-    __syncthreads();
-    remaining -= sm.s_above;
-    prefix |= (uint32_t)sm.s_bin << sh;
-    pmask |= dmask << sh;
-  }
-  if (!found) {
-    if (tid == 0) atomicOr(a.err, WI_DEVERR_TOPK);
-    kk = 0;
-    if (tid == 0) a.selcnt[uh] = 0;
-  }
-  const uint32_t T = kk > 0 ? prefix : 0xffffffffu;  // nothing is taken when kk == 0
-  // ---- compaction in id order
-  uint32_t kmx = 0u;
-  int cgt = 0, ceq = 0;
-#pragma unroll
-  for (int e = 0; e < KPT; ++e) {
-    kmx = max(kmx, key[e]);
-    cgt += key[e] > T;
-    ceq += (key[e] != 0u && key[e] == T);
+#pragma unroll 4
+    for (int j = tid; j < C; j += kSThreads) kmx = max(kmx, key_of(j));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) kmx = max(kmx, __shfl_xor_sync(0xffffffffu, kmx, o));
-  if (lane == 0) atomicMax(&sm.s_maxkey, kmx);
-  unsigned long long tot;
-  const unsigned long long pre =
-      block_prefix_u64(((unsigned long long)cgt << 32) | (unsigned)ceq, sm.s_wt[0], &tot);
-  const int pre_gt = (int)(pre >> 32), pre_eq = (int)(pre & 0xffffffffu);
-  const int tot_gt = (int)(tot >> 32), tot_eq = (int)(tot & 0xffffffffu);
-  const float m_sub = kk > 0 ? a.lam * key_float(sm.s_maxkey) : -INFINITY;
-  int eq_seen = pre_eq, my_rows = 0;
-  uint32_t takemask = 0u;
+  if (lane == 0) sm.s_wmax[warp] = kmx;
+  __syncthreads();
+  uint32_t K0 = lane < kSNW ? sm.s_wmax[lane] : 0u;
 #pragma unroll
-  for (int e = 0; e < KPT; ++e) {
-    const bool is_eq = key[e] != 0u && key[e] == T;
-    const bool take = key[e] > T || (is_eq && eq_seen < remaining);
-    eq_seen += is_eq ? 1 : 0;
-    if (take) { takemask |= 1u << e; my_rows += nc[e]; }
-  }
-  unsigned long long rtot, ctot;
-  const int row_pre = (int)block_prefix_u64((unsigned long long)my_rows, sm.s_wt[1], &rtot);
-  // a cluster's first row = n_sink + the counts of all lower ids (the cluster-contiguous layout)
-  int csum = 0;
-#pragma unroll
-  for (int e = 0; e < KPT; ++e) csum += nc[e];
-  int of = a.n_sink + (int)block_prefix_u64((unsigned long long)csum, sm.s_wt[2], &ctot);
-  int pos = pre_gt + min(pre_eq, remaining);
-  int rp = row_pre;
-  float zpart = 0.f;
-  int4* runs = a.runs + uh * a.kmax;
-#pragma unroll
-  for (int e = 0; e < KPT; ++e) {
-    if (takemask & (1u << e)) {
-      if (pos < kk) {
-        const int j = base + e;
-        const float w = __expf(a.lam * key_float(key[e]) - m_sub);
-        out[pos] = j;
-        s_row[pos] = rp;
-        runs[pos] = make_int4(of, nc[e], __float_as_int(w), j);
-        zpart = fmaf((float)nc[e], w, zpart);
-      }
-      rp += nc[e];
-      ++pos;
+  for (int o = 16; o > 0; o >>= 1) K0 = max(K0, __shfl_xor_sync(0xffffffffu, K0, o));
+  if (K0 == 0u) kk = 0;  // no non-empty cluster at all
+  // ---- logarithmic histogram of d = K0 - key.  Keys at d >= 2^30 (in practice the negative
+  // scores, often half of all keys) fall into a handful of bins where shared-memory atomics
+  // would serialize; they are counted only if the nearer keys number fewer than k.
+  if (kk > 0) {
+#pragma unroll 4
+    for (int j = tid; j < C; j += kSThreads) {
+      const uint32_t k = key_of(j);
+      if (k != 0u && K0 - k < (1u << 30)) atomicAdd(&sm.hist[0][log_bin(K0 - k)], 1);
     }
-    of += nc[e];
   }
-  if (tid == 0) {
-    s_row[kk] = (int)rtot;
-    if (tot_gt + min(tot_eq, remaining) != kk) atomicOr(a.err, WI_DEVERR_TOPK);
+  __syncthreads();
+  bool found = kk == 0;
+  int bstar = -1, remaining = 0;
+  if (kk > 0) {
+    int above = 0;
+    found = find_bin(sm.hist[0], kk, sm, &bstar, &above);
+    if (!found) {  // the k-th key is a far one: add the far keys and search again
+      for (int j = tid; j < C; j += kSThreads) {
+        const uint32_t k = key_of(j);
+        if (k != 0u && K0 - k >= (1u << 30)) atomicAdd(&sm.hist[0][log_bin(K0 - k)], 1);
+      }
+      __syncthreads();
+      found = find_bin(sm.hist[0], kk, sm, &bstar, &above);
+    }
+    remaining = kk - above;
   }
+  uint32_t Tk = 0xffffffffu;
+  int Tid = -1;
+  if (kk > 0 && found) {
+    // ---- the keys of the threshold bin
+#pragma unroll 4
+    for (int j = tid; j < C; j += kSThreads) {
+      const uint32_t k = key_of(j);
+      if (k != 0u && log_bin(K0 - k) == bstar) {
+        const int slot = atomicAdd(&sm.s_ncand, 1);
+        if (slot < kSelThreads) { sm.ckey[slot] = k; sm.cid[slot] = j; }
+      }
+    }
+    __syncthreads();
+    const int ncand = sm.s_ncand;
+    if (ncand <= kSelThreads) {
+      // rank of candidate tid in (key descending, id ascending) order; rank remaining-1 is the k-th key
+      if (tid < ncand) {
+        const uint32_t mk = sm.ckey[tid];
+        const int mi = sm.cid[tid];
+        int rank = 0;
+        for (int j = 0; j < ncand; ++j) {
+          const uint32_t kj = sm.ckey[j];
+          rank += (kj > mk || (kj == mk && sm.cid[j] < mi)) ? 1 : 0;
+        }
+        if (rank == remaining - 1) { sm.s_tkey = mk; sm.s_tid = mi; sm.s_found = 1; }
+      }
+    } else {
+      // ---- many keys in one bin: radix select (11-bit digits, ascending) over the 48-bit
+      // composite (d << 16) | id of the bin's keys; ids are < 65536.
+      unsigned long long cpfx = 0ull, cmask = 0ull;
+      int rem = remaining;
+      bool ok = true;
+      for (int pass = 0; pass < 5 && ok; ++pass) {
+        const int sh = pass < 4 ? 37 - 11 * pass : 0;
+        const unsigned long long dmask = pass < 4 ? 2047ull : 15ull;
+        int* hc = sm.hist[(pass + 1) & 1];
+        int* hn = sm.hist[pass & 1];
+        for (int j = tid; j < C; j += kSThreads) {
+          const uint32_t k = key_of(j);
+          if (k == 0u) continue;
+          const uint32_t d = K0 - k;
+          const unsigned long long comp = ((unsigned long long)d << 16) | (unsigned)j;
+          if (log_bin(d) == bstar && (comp & cmask) == cpfx) atomicAdd(&hc[(comp >> sh) & dmask], 1);
+        }
+        __syncthreads();
+        for (int i = tid; i < kTopkBins; i += kSThreads) hn[i] = 0;
+        int bin = 0, above = 0;
+        ok = find_bin(hc, rem, sm, &bin, &above);
+        rem -= above;
+        cpfx |= (unsigned long long)bin << sh;
+        cmask |= dmask << sh;
+      }
+      if (ok && tid == 0) {
+        sm.s_tkey = K0 - (uint32_t)(cpfx >> 16);
+        sm.s_tid = (int)(cpfx & 0xffffull);
+        sm.s_found = 1;
+      }
+    }
+    __syncthreads();
+    found = sm.s_found != 0;
+    Tk = sm.s_tkey;
+    Tid = sm.s_tid;
+  }
+  if (!found) {  // inconsistent counts: select nothing, report it
+    if (tid == 0) atomicOr(a.err, WI_DEVERR_TOPK);
+    kk = 0;
+  }
+  // ---- the selection in id order: cluster j is taken iff (key, -id) >= (Tk, -Tid)
+  for (int c = warp; c < nch; c += kSNW) {
+    const int j = c * 32 + lane;
+    const uint32_t k = j < C ? key_of(j) : 0u;
+    const bool take = kk > 0 && k != 0u && (k > Tk || (k == Tk && j <= Tid));
+    const unsigned m = __ballot_sync(0xffffffffu, take);
+    if (lane == 0) {
+      tmask[c] = m;
+      cpre[c] = __popc(m);
+    }
+  }
+  __syncthreads();
+  const int total = block_excl_scan(cpre, nch, sm);
+  if (total != kk) {  // uniform; cannot happen with consistent counts
+    if (tid == 0) atomicOr(a.err, WI_DEVERR_TOPK);
+    kk = min(kk, total);  // every position below kk gets an id
+  }
+  for (int c = warp; c < nch; c += kSNW) {
+    const unsigned m = tmask[c];
+    if (m & (1u << lane)) {
+      const int pos = cpre[c] + __popc(m & ((1u << lane) - 1u));
+      if (pos < kk) sel_s[pos] = c * 32 + lane;
+    }
+  }
+  __syncthreads();
+  // ---- per selected cluster (position p = tid + rounds of kSThreads): rows and their prefix
+  int* rp_s = sel_s + a.kmax;  // [kmax] first row of position p among the selected rows
+  int R = 0;
+  for (int r0 = 0; r0 < kk; r0 += kSThreads) {  // uniform
+    const int p = r0 + tid;
+    const int nc = p < kk ? __ldg(cn + sel_s[p]) : 0;
+    const int inc = warp_inclusive_scan(nc);
+    if (lane == 31) sm.s_wt[warp] = inc;
+    __syncthreads();
+    const int x = lane < kSNW ? sm.s_wt[lane] : 0;
+    int b = lane < warp ? x : 0, t = x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      b += __shfl_xor_sync(0xffffffffu, b, o);
+      t += __shfl_xor_sync(0xffffffffu, t, o);
+    }
+    if (p < kk) rp_s[p] = R + b + inc - nc;
+    R += t;
+    __syncthreads();  // s_wt is reused by the next round
+  }
+  // ---- row run, weight and split starts per selected cluster
+  const float m_sub = kk > 0 ? a.lam * key_float(K0) : -INFINITY;
+  const int NS = a.NS;
+  int4* runs = a.runs + uh * a.kmax;
+  int4* splits = a.splits + uh * (NS + 1);
+  float zpart = 0.f;
+  // split b starts at row floor(R b / NS); the cluster holding that row records it
+  const unsigned long long Rl = (unsigned long long)R;
+  auto split_row = [&](int b) -> int { return (int)((Rl * (unsigned)b) / (unsigned)NS); };
+  for (int p = tid; p < kk; p += kSThreads) {
+    const int j = sel_s[p], rp = rp_s[p];
+    const int nc = __ldg(cn + j), of = __ldg(a.off + (size_t)u * (C + 1) + j);
+    const float w = __expf(a.lam * key_float(key_of(j)) - m_sub);
+    out[p] = j;
+    runs[p] = make_int4(of, nc, __float_as_int(w), j);
+    zpart = fmaf((float)nc, w, zpart);
+    if (R == 0) continue;
+    int b = (int)(((unsigned long long)rp * (unsigned)NS) / Rl);
+    while (b < NS && split_row(b) < rp) ++b;
+    for (; b < NS; ++b) {
+      const int rb = split_row(b);
+      if (rb >= rp + nc) break;
+      splits[b] = make_int4(p, rb - rp, rb, 0);
+    }
+  }
+  for (int i = kk + tid; i < a.kmax; i += kSThreads) out[i] = -1;
+  if (R == 0)  // nothing selected: every split is empty
+    for (int b = tid; b < NS; b += kSThreads) splits[b] = make_int4(0, 0, 0, 0);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) zpart += __shfl_xor_sync(0xffffffffu, zpart, o);
-  if (lane == 0) sm.zred[warp] = zpart;
+  if (lane == 0) sm.s_wf[warp] = zpart;
   __syncthreads();
-  // split s starts at row b_s = R * s / NS: (position of its first cluster, row inside it, b_s)
-  if (tid <= a.NS) {
-    const int R = s_row[kk];
-    const int b = (int)((long long)R * tid / a.NS);
-    int lo = 0, hi = kk;  // largest position with s_row[pos] <= b
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_row[mid] <= b) lo = mid; else hi = mid - 1;
-    }
-    if (b >= R) lo = kk;
-    a.splits[uh * (a.NS + 1) + tid] = make_int4(lo, b - (lo < kk ? s_row[lo] : R), b, 0);
-  }
   // the retrieved clusters' value-sum terms are summed by the exact-attention CTAs that load them
   if (tid == 0) {
-    float* sp = a.subpart + uh * WI_PART;
+    a.selcnt[uh] = kk;
+    splits[NS] = make_int4(kk, 0, R, 0);
     float zz = 0.f;
-    for (int w = 0; w < kSelWarps; ++w) zz += sm.zred[w];
+    for (int w = 0; w < kSNW; ++w) zz += sm.s_wf[w];
+    float* sp = a.subpart + uh * WI_PART;
     sp[0] = m_sub;
     sp[1] = zz;
   }
 }
 
-template <int G, int KPT>
+template <int G>
 __global__ void __launch_bounds__(kSThreads, 1) k_select_estimate(TopkArgs a) {
   extern __shared__ __align__(128) unsigned char se_raw[];
   pdl_trigger();
   pdl_wait();
   const int nsel = a.U * a.G;
   if ((int)blockIdx.x < nsel) {
-    select_role<KPT>(se_raw, a, blockIdx.x / a.G, blockIdx.x % a.G);
+    select_role(se_raw, a, blockIdx.x / a.G, blockIdx.x % a.G);
   } else {
     const int e = blockIdx.x - nsel;
     estimate_role<G>(se_raw, a.valsum, a.cnt, a.scores, a.part1, a.C, e / a.PE, e % a.PE, a.PE, a.lam, a.err);
@@ -710,7 +803,7 @@ struct D3Stage {
   bf16 v[kD3Rows * WI_D];
 };
 constexpr size_t kD3Smem = sizeof(D3Stage) * kD3Stages + 2 * kD3Stages * sizeof(uint64_t) +
-                           4 * kD3Stages * sizeof(int) + sizeof(float) * kD3Warps * WI_PART + 32;
+                           4 * kD3Stages * sizeof(int) + sizeof(float) * kD3Warps * (WI_PART + WI_D) + 32;
 
 struct ExactArgs {
   const bf16* q;
@@ -792,7 +885,8 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
   uint64_t* empty = full + kD3Stages;
   int* nrows = reinterpret_cast<int*>(empty + kD3Stages);        // [4 * stages]
   float* red = reinterpret_cast<float*>(nrows + 4 * kD3Stages);  // [warps][WI_PART]
-  int* flags = reinterpret_cast<int*>(red + kD3Warps * WI_PART);  // abort, last CTA, kk, non-empty
+  float* vred = red + kD3Warps * WI_PART;                         // [warps][WI_D] value-sum terms
+  int* flags = reinterpret_cast<int*>(vred + kD3Warps * WI_D);    // abort, last CTA, kk, non-empty
   const int split = blockIdx.x, h = blockIdx.y, u = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t uh = (size_t)u * a.G + h;
@@ -813,6 +907,23 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
     const bf16* Vu = a.V + (size_t)u * a.n * WI_D;
     RunPacker pk{st, full, empty, nrows, a.err};
     bool ok = true;
+    // Close the open stage and send the end marker (a stage with no rows); on failure, wait for
+    // the copies already in flight so that none lands after the CTA has left.
+    auto finish = [&]() {
+      if (lane != 0) return;
+      if (ok && pk.opened) pk.close();
+      if (ok) ok = pk.open();
+      if (ok) pk.close();
+      if (!ok) {
+        flags[0] = 1;
+        const int issued = pk.stage_it;
+        for (int s = 0; s < kD3Stages && s < issued; ++s) {
+          const int last = ((issued - 1 - s) / kD3Stages) * kD3Stages + s;
+          mbar_wait(&full[s], (last / kD3Stages) & 1, a.err);
+        }
+      }
+      atomicAdd(a.rows_total, (unsigned long long)pk.rows_done);
+    };
     if (split == a.NS) {
       // ---- steady rows: sinks and local window are fixed since the build; appended rows after the wait
       if (lane == 0) {
@@ -820,11 +931,11 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
         ok = ok && pk.push(Ku + (size_t)(a.n - a.W) * WI_D, Vu + (size_t)(a.n - a.W) * WI_D, a.W);
       }
       pdl_wait();
-      reinterpret_cast<float4*>(a.subn + (uh * nsp + split) * WI_PART + 4)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (lane == 0) {
         const int amax = a.max_append > 0 ? a.max_append : 1;
         ok = ok && pk.push(a.appK + (size_t)u * amax * WI_D, a.appV + (size_t)u * amax * WI_D, *a.app_count);
       }
+      finish();
     } else {
       // ---- selected clusters: rows [b_s, b_{s+1}) of the head's row-balanced split
       pdl_wait();
@@ -834,14 +945,10 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
       int rows_left = sb.z - sa.z;
       int pos = max(sa.x, 0), in = sa.y;
       const int4* runs = a.runs + uh * a.kmax;
-      const float4* vsu = reinterpret_cast<const float4*>(a.valsum + (size_t)u * a.C * WI_D) + lane;
-      float4 sub = make_float4(0.f, 0.f, 0.f, 0.f);  // value-sum terms of the clusters that start here
       while (rows_left > 0 && pos < kk) {
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
         const int4 rr = (pos + lane < kk) ? runs[pos + lane] : make_int4(0, 0, 0, 0);
         const int nb = min(32, kk - pos);
-        int used = 0;
-        const int first_in = in;
         for (int i = 0; i < nb && rows_left > 0; ++i) {
           const int o = __shfl_sync(0xffffffffu, rr.x, i);
           const int z = __shfl_sync(0xffffffffu, rr.y, i);
@@ -857,45 +964,10 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
             ok = pk.push(Ku + (size_t)(o + in) * WI_D, Vu + (size_t)(o + in) * WI_D, take);
           rows_left -= take;
           in = 0;
-          used = i + 1;
-        }
-        // clusters of this batch whose first row lies in this split: four value rows in flight
-        for (int i0 = (first_in > 0 ? 1 : 0); i0 < used; i0 += 4) {
-          float4 vv[4];
-          float ww[4];
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const int i = min(i0 + x, used - 1);
-            int j = __shfl_sync(0xffffffffu, rr.w, i);
-            j = (j >= 0 && j < a.C) ? j : 0;
-            ww[x] = i0 + x < used ? __int_as_float(__shfl_sync(0xffffffffu, rr.z, i)) : 0.f;
-            vv[x] = __ldg(vsu + (size_t)j * (WI_D / 4));
-          }
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            sub.x = fmaf(ww[x], vv[x].x, sub.x);
-            sub.y = fmaf(ww[x], vv[x].y, sub.y);
-            sub.z = fmaf(ww[x], vv[x].z, sub.z);
-            sub.w = fmaf(ww[x], vv[x].w, sub.w);
-          }
         }
         pos += nb;
       }
-      reinterpret_cast<float4*>(a.subn + (uh * nsp + split) * WI_PART + 4)[lane] = sub;
-    }
-    if (lane == 0) {
-      if (ok && pk.opened) pk.close();
-      if (ok) ok = pk.open();  // the end marker: a stage with no rows
-      if (ok) pk.close();
-      if (!ok) {
-        flags[0] = 1;
-        const int issued = pk.stage_it;
-        for (int s = 0; s < kD3Stages && s < issued; ++s) {
-          const int last = ((issued - 1 - s) / kD3Stages) * kD3Stages + s;
-          mbar_wait(&full[s], (last / kD3Stages) & 1, a.err);
-        }
-      }
-      atomicAdd(a.rows_total, (unsigned long long)pk.rows_done);
+      finish();
     }
   } else {
     // ---- consumers
@@ -906,6 +978,37 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
     }
     float qr[4];
     load_bf16x4(a.q + uh * WI_D + 4 * lane, qr);
+    // value-sum terms sum_j w_j valsum_j of the retrieved clusters whose first row lies in this
+    // split (clusters [first, last) of the selection), one round trip while the first stage lands
+    float4 sub = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (split < a.NS) {
+      const int4 sa = a.splits[uh * nsp + split];
+      const int4 sb = a.splits[uh * nsp + split + 1];
+      const int kk = min(a.selcnt[uh], a.kmax);
+      const int first = max(sa.x, 0) + (sa.y > 0 ? 1 : 0);
+      const int last = min(sb.x + (sb.y > 0 ? 1 : 0), kk);
+      const int4* runs = a.runs + uh * a.kmax;
+      const float4* vsu = reinterpret_cast<const float4*>(a.valsum + (size_t)u * a.C * WI_D) + lane;
+      for (int c0 = first + warp; c0 < last; c0 += 4 * kD3Warps) {
+        float4 vv[4];
+        float ww[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const int c = c0 + x * kD3Warps;
+          const int4 rr = c < last ? runs[c] : make_int4(0, 0, 0, 0);
+          const int j = (rr.w >= 0 && rr.w < a.C) ? rr.w : 0;
+          ww[x] = c < last ? __int_as_float(rr.z) : 0.f;
+          vv[x] = __ldg(vsu + (size_t)j * (WI_D / 4));
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          sub.x = fmaf(ww[x], vv[x].x, sub.x);
+          sub.y = fmaf(ww[x], vv[x].y, sub.y);
+          sub.z = fmaf(ww[x], vv[x].z, sub.z);
+          sub.w = fmaf(ww[x], vv[x].w, sub.w);
+        }
+      }
+    }
     const int ri = lane >> 2;  // the row (of the warp's 8) whose logit this lane ends with
     for (int it = 0;; ++it) {
       const int s = it % kD3Stages, r = it / kD3Stages;
@@ -960,6 +1063,7 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
       red[warp * WI_PART + 1] = Z;
     }
     *reinterpret_cast<float4*>(&red[warp * WI_PART + 4 + 4 * lane]) = make_float4(N[0], N[1], N[2], N[3]);
+    *reinterpret_cast<float4*>(&vred[warp * WI_D + 4 * lane]) = sub;
   }
   __syncthreads();
   if (flags[0]) return;
@@ -982,6 +1086,10 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
       o3[1] = z;
     }
     o3[4 + tid] = acc;
+    float vs = 0.f;
+#pragma unroll
+    for (int w = 0; w < kD3Warps; ++w) vs += vred[w * WI_D + tid];
+    a.subn[(uh * nsp + split) * WI_PART + 4 + tid] = vs;
   }
   // Publish this CTA's partial and take a ticket: the barrier orders the CTA's writes before
   // thread 0's release; the acquire side makes every earlier CTA's partial visible to the last one.
@@ -990,65 +1098,113 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
   __syncthreads();
   if (!flags[1]) return;
   // ---- the last CTA of this head: estimate over all clusters - retrieved terms, plus exact, by LSE.
-  // One parallel gather of every partial row into shared memory (the K/V stages are free now),
-  // then each output dim sums its column there.  Rows: P estimation partials, nsp exact
-  // partials, nsp retrieved value-sum partials, then (m_sub, Z_sub).
+  // Rows: P estimation partials, nsp exact partials, nsp retrieved value-sum partials, then
+  // (m_sub, Z_sub).  Every warp fetches the headers (m, Z) of all rows and the value columns of
+  // its own rows in one round trip; the column sums meet in shared memory (the stages are free).
   const int kk = flags[2];
   const int nonempty = flags[3];
-  const int nrow = a.P + 2 * nsp + 1;
-  const float* p1 = a.part1 + uh * a.P * WI_PART;
+  constexpr int kMW = kD3Warps + 1;  // all warps of the CTA
+  constexpr int kMR = 4;             // rows per warp per round trip
+  const int P = a.P, rx = P, rs = P + nsp, rsub = P + 2 * nsp, nrow = rsub + 1;
+  const float* p1 = a.part1 + uh * P * WI_PART;
   const float* p3 = a.part3 + uh * nsp * WI_PART;
   const float* ps = a.subn + uh * nsp * WI_PART;
   const float* sp = a.subpart + uh * WI_PART;
   auto grow = [&](int r) -> const float* {
-    return r < a.P ? p1 + (size_t)r * WI_PART
-                   : (r < a.P + nsp ? p3 + (size_t)(r - a.P) * WI_PART
-                                    : (r < a.P + 2 * nsp ? ps + (size_t)(r - a.P - nsp) * WI_PART : sp));
+    return r < rx ? p1 + (size_t)r * WI_PART
+                  : (r < rs ? p3 + (size_t)(r - rx) * WI_PART
+                            : (r < rsub ? ps + (size_t)(r - rs) * WI_PART : sp));
   };
-  float* rows = reinterpret_cast<float*>(d3_raw);
-  const int maxrows = (int)(sizeof(D3Stage) * kD3Stages / (WI_PART * sizeof(float)));
-  const int nst = nrow < maxrows ? nrow : maxrows;
-  for (int i = tid; i < nst * (WI_PART / 4); i += kD3Threads) {
-    const int r = i / (WI_PART / 4), c4 = i % (WI_PART / 4);
-    reinterpret_cast<float4*>(rows)[i] = __ldcg(reinterpret_cast<const float4*>(grow(r)) + c4);
+  float* mz = reinterpret_cast<float*>(d3_raw);  // [nrow][2]
+  float* wred = mz + 2 * ((nrow + 31) & ~31);   // [kMW][3][WI_D]: estimate, exact, value-sum columns
+  float* zred = wred + kMW * 3 * WI_D;           // [kMW][2]
+  float4 colv[kMR];
+#pragma unroll
+  for (int i = 0; i < kMR; ++i) {
+    const int r = warp + i * kMW;
+    colv[i] = r < nrow ? __ldcg(reinterpret_cast<const float4*>(grow(r) + 4) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int r = tid; r < nrow; r += kD3Threads) {
+    const float2 h2 = __ldcg(reinterpret_cast<const float2*>(grow(r)));
+    mz[2 * r] = h2.x;
+    mz[2 * r + 1] = h2.y;
   }
   __syncthreads();
-  auto row = [&](int r) -> const float* { return r < nst ? rows + (size_t)r * WI_PART : grow(r); };
+  float Me = -INFINITY, Mx = -INFINITY;
+  for (int r = lane; r < rs; r += 32) {
+    if (r < rx) Me = fmaxf(Me, mz[2 * r]);
+    else Mx = fmaxf(Mx, mz[2 * r]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Me = fmaxf(Me, __shfl_xor_sync(0xffffffffu, Me, o));
+    Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+  }
+  const bool use_est = Me > -INFINITY && kk < nonempty;
+  float4 ce = make_float4(0.f, 0.f, 0.f, 0.f), cx = ce, cs = ce;
+  float ze = 0.f, zx = 0.f;
+  for (int r0 = warp; r0 < nrow; r0 += kMR * kMW) {
+    if (r0 != warp) {  // rows beyond the first round trip (more partials than warps * kMR)
+#pragma unroll
+      for (int i = 0; i < kMR; ++i) {
+        const int r = r0 + i * kMW;
+        colv[i] = r < nrow ? __ldcg(reinterpret_cast<const float4*>(grow(r) + 4) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kMR; ++i) {
+      const int r = r0 + i * kMW;
+      if (r >= rsub) continue;
+      const float mr = mz[2 * r], zr = mz[2 * r + 1];
+      if (r < rx) {
+        const float f = (use_est && mr > -INFINITY) ? __expf(mr - Me) : 0.f;
+        ze = fmaf(f, zr, ze);
+        ce.x = fmaf(f, colv[i].x, ce.x); ce.y = fmaf(f, colv[i].y, ce.y);
+        ce.z = fmaf(f, colv[i].z, ce.z); ce.w = fmaf(f, colv[i].w, ce.w);
+      } else if (r < rs) {
+        const float f = mr > -INFINITY ? __expf(mr - Mx) : 0.f;
+        zx = fmaf(f, zr, zx);
+        cx.x = fmaf(f, colv[i].x, cx.x); cx.y = fmaf(f, colv[i].y, cx.y);
+        cx.z = fmaf(f, colv[i].z, cx.z); cx.w = fmaf(f, colv[i].w, cx.w);
+      } else {
+        cs.x += colv[i].x; cs.y += colv[i].y; cs.z += colv[i].z; cs.w += colv[i].w;
+      }
+    }
+  }
+  reinterpret_cast<float4*>(wred + (warp * 3 + 0) * WI_D)[lane] = ce;
+  reinterpret_cast<float4*>(wred + (warp * 3 + 1) * WI_D)[lane] = cx;
+  reinterpret_cast<float4*>(wred + (warp * 3 + 2) * WI_D)[lane] = cs;
+  if (lane == 0) {
+    zred[2 * warp] = ze;
+    zred[2 * warp + 1] = zx;
+  }
+  __syncthreads();
   if (tid < WI_D) {
     const int d = tid;
-    float Me = -INFINITY, Mx = -INFINITY;
-    for (int c = 0; c < a.P; ++c) Me = fmaxf(Me, row(c)[0]);
-    for (int c = 0; c < nsp; ++c) Mx = fmaxf(Mx, row(a.P + c)[0]);
-    float Ze = 0.f, Ne = 0.f;
-    if (Me > -INFINITY && kk < nonempty) {
-      for (int c = 0; c < a.P; ++c) {
-        const float* r = row(c);
-        const float f = r[0] == -INFINITY ? 0.f : __expf(r[0] - Me);
-        Ze = fmaf(f, r[1], Ze);
-        Ne = fmaf(f, r[4 + d], Ne);
-      }
-      const float* r = row(a.P + 2 * nsp);
-      if (r[0] > -INFINITY) {
-        float nsub = 0.f;
-        for (int c = 0; c < nsp; ++c) nsub += row(a.P + nsp + c)[4 + d];
-        const float f = __expf(r[0] - Me);
-        Ze = fmaf(-f, r[1], Ze);
-        Ne = fmaf(-f, nsub, Ne);
+    float Ze = 0.f, Ne = 0.f, Zx = 0.f, Nx = 0.f, Ns = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMW; ++w) {
+      Ze += zred[2 * w];
+      Zx += zred[2 * w + 1];
+      Ne += wred[(w * 3 + 0) * WI_D + d];
+      Nx += wred[(w * 3 + 1) * WI_D + d];
+      Ns += wred[(w * 3 + 2) * WI_D + d];
+    }
+    if (use_est) {
+      const float msub = mz[2 * rsub];
+      if (msub > -INFINITY) {
+        const float f = __expf(msub - Me);
+        Ze = fmaf(-f, mz[2 * rsub + 1], Ze);
+        Ne = fmaf(-f, Ns, Ne);
       }
       Ze = fmaxf(Ze, 0.f);
-    }
-    float Zx = 0.f, Nx = 0.f;
-    if (Mx > -INFINITY) {
-      for (int c = 0; c < nsp; ++c) {
-        const float* r = row(a.P + c);
-        const float f = r[0] == -INFINITY ? 0.f : __expf(r[0] - Mx);
-        Zx = fmaf(f, r[1], Zx);
-        Nx = fmaf(f, r[4 + d], Nx);
-      }
+    } else {
+      Ze = 0.f;
+      Ne = 0.f;
     }
     const float M = fmaxf(Mx, Me);
     const float fx = Mx > -INFINITY ? __expf(Mx - M) : 0.f;
-    const float fe = (Me > -INFINITY && Ze > 0.f) ? __expf(Me - M) : 0.f;
+    const float fe = (use_est && Ze > 0.f) ? __expf(Me - M) : 0.f;
     a.out[uh * WI_D + d] = (Nx * fx + Ne * fe) / (Zx * fx + Ze * fe);
   }
   if (tid == 0) a.ticket[uh] = 0u;  // ready for the next step
@@ -1088,14 +1244,14 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-template <int G, int KPT>
+template <int G>
 cudaError_t launch_select(const WiGeom& g, const WiDecodeBufs& b, const TopkArgs& t, cudaStream_t st) {
-  const size_t sel = sizeof(SelSmem) + (size_t)(g.kmax + 1) * sizeof(int);
+  const size_t sel = sel_smem_bytes(g.C, g.kmax);
   const size_t smem = sel > kEsSmem ? sel : kEsSmem;
   static int smem_set = 0;
-  cudaError_t e = wi_ensure_smem(k_select_estimate<G, KPT>, smem, &smem_set);
+  cudaError_t e = wi_ensure_smem(k_select_estimate<G>, smem, &smem_set);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_select_estimate<G, KPT>, dim3(g.U * G + g.U * b.p_es), dim3(kSThreads), smem, st, t);
+  return launch_pdl(k_select_estimate<G>, dim3(g.U * G + g.U * b.p_es), dim3(kSThreads), smem, st, t);
 }
 
 template <int G>
@@ -1105,14 +1261,13 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   const float lam = 1.0f / sqrtf((float)WI_D);
   cudaError_t e = mark(ev, 0, st);
   if (e != cudaSuccess) return e;
-  // scores (+ first-digit histogram)
+  // scores
   static int smem_sc = 0;
   if ((e = wi_ensure_smem(k_scores<G>, ScCfg<G>::SMEM, &smem_sc)) != cudaSuccess) return e;
-  e = launch_pdl(k_scores<G>, dim3(b.p1, g.U), dim3(kScThreads), ScCfg<G>::SMEM, st, b.map_mu, q, b.cnt, b.scores,
-                 b.ghist, g.C, b.p1, b.err);
+  e = launch_pdl(k_scores<G>, dim3(b.p1, g.U), dim3(kScThreads), ScCfg<G>::SMEM, st, b.map_mu, q, b.scores, g.C,
+                 b.p1, b.err);
   if (e != cudaSuccess || (e = mark(ev, 1, st)) != cudaSuccess) return e;
   TopkArgs t;
-  t.ghist = b.ghist;
   t.scores = b.scores;
   t.cnt = b.cnt;
   t.off = b.off;
@@ -1133,11 +1288,7 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   t.PE = b.p_es;
   t.lam = lam;
   t.n_sink = g.n_sink;
-  const int kpt = (g.C + kSelThreads - 1) / kSelThreads;
-  if (kpt <= 16) e = launch_select<G, 16>(g, b, t, st);
-  else if (kpt <= 32) e = launch_select<G, 32>(g, b, t, st);
-  else if (kpt <= 64) e = launch_select<G, 64>(g, b, t, st);
-  else e = launch_select<G, 128>(g, b, t, st);
+  e = launch_select<G>(g, b, t, st);
   if (e != cudaSuccess || (e = mark(ev, 2, st)) != cudaSuccess) return e;
   ExactArgs a;
   a.q = q;

@@ -59,6 +59,8 @@ typedef struct wi_index wi_index; /* opaque, library-owned */
  * k-means (summary fr 2.A.2).  Retrieval budget (summary zh section 3):
  * k = budget_k if > 0, else ceil(budget_frac * C), C = all clusters of a unit;
  * capped at the unit's non-empty clusters at decode time.
+ * Limits of this build (WI_EUNSUPPORTED beyond them): n_q_heads / n_kv_heads
+ * <= 8, k <= 4096, seg_len <= 16384, C <= 65536.
  */
 typedef struct {
   int batch, layers, n_q_heads, n_kv_heads, head_dim; /* head_dim == 128 */

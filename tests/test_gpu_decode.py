@@ -23,8 +23,9 @@ def dev16(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(DEV)
 
 
-def run_case(wi, w, idx=None, steps=1, append=False, kv=None):
-    """Import the oracle index, decode `steps` steps (with append if asked), compare every step."""
+def run_case(wi, w, idx=None, steps=1, append=False, kv=None, strict_ids=False):
+    """Import the oracle index, decode `steps` steps (with append if asked), compare every step.
+    strict_ids: the selection must equal the oracle's exactly (ties included)."""
     k, v, q, K, V, Q = gen(w)
     if kv is not None:
         k, v = kv
@@ -64,6 +65,9 @@ def run_case(wi, w, idx=None, steps=1, append=False, kv=None):
             kk = oracle.budget_k(w.clusters, p)
             for h in range(w.group):
                 check_topk(ids[u, h], cnt[u, h], info[u][h]["scores"], ne, kk)
+                if strict_ids:
+                    ref_ids = np.sort(oracle.select_topk(info[u][h]["scores"], ne, kk))
+                    assert np.array_equal(ids[u, h][:cnt[u, h]], ref_ids), (u, h)
     ix.free()
     return worst
 
@@ -128,6 +132,34 @@ def test_decode_budget_above_nonempty(wi):
     idx = oracle.build_index(K, V, params_of(w))
     assert (idx[0]["counts"] > 0).sum() < 100
     assert run_case(wi, w, idx=idx, kv=(k, v)) < 1e-4
+
+
+def tied_index(w, pattern):
+    """Oracle index whose mean keys are overwritten so that scores tie: `pattern(j)` picks, per
+    cluster j, which of two fixed mean-key rows it gets (equal rows give bitwise-equal scores)."""
+    k, v, q, K, V, Q = gen(w)
+    idx = oracle.build_index(K, V, params_of(w))
+    for u in range(w.units):
+        mu = idx[u]["mu"]
+        rows = [mu[0].copy(), mu[1].copy()]
+        for j in range(mu.shape[0]):
+            mu[j] = rows[pattern(j)]
+    return idx
+
+
+def test_topk_all_scores_tied(wi):
+    # every score equal: more tied keys than top-k threads, the k lowest non-empty ids win
+    w = small(n_ctx=8192, seg_len=1024, clusters_per_seg=128, iters=1, n_q_heads=4, budget_k=100, seed=31)
+    idx = tied_index(w, lambda j: 0)
+    assert (idx[0]["counts"] > 0).sum() > 600
+    assert run_case(wi, w, idx=idx, strict_ids=True) < 1e-4
+
+
+def test_topk_half_tied(wi):
+    # two score levels, each shared by half the clusters: the threshold level holds ~512 ties
+    w = small(n_ctx=8192, seg_len=1024, clusters_per_seg=128, iters=1, n_q_heads=4, budget_k=100, seed=32)
+    idx = tied_index(w, lambda j: j & 1)
+    assert run_case(wi, w, idx=idx, strict_ids=True) < 1e-4
 
 
 @pytest.mark.parametrize("n_sink,window", [(0, 16), (8, 0), (4, 64)])
