@@ -41,14 +41,12 @@ constexpr int kSThreads = 32 * (kSWarps + 1);
 constexpr int kTopkBins = 2048;  // histogram bins of the top-k passes
 
 // G query heads per kv head, in blocks of 4 heads (HB blocks); GP = heads per
-// block rounded up to a power of two; NV = values per transpose-reduction
-// (8 clusters x GP heads); lane l ends with cluster l >> 2 and in-block head
-// (l & 3) >> SHIFT.
+// block rounded up to a power of two; lane l of a warp handles cluster l >> 2
+// and in-block head (l & 3) >> SHIFT.
 template <int G>
 struct HeadGeo {
   static constexpr int HB = G > 4 ? 2 : 1;
   static constexpr int GP = G > 2 ? 4 : (G > 1 ? 2 : 1);
-  static constexpr int NV = 8 * GP;
   static constexpr int SHIFT = GP == 4 ? 0 : (GP == 2 ? 1 : 2);
 };
 
@@ -280,21 +278,39 @@ __device__ void estimate_role(unsigned char* raw, const float* __restrict__ vals
   const bool rep = (lane & ((1 << HG::SHIFT) - 1)) == 0;
   if (warp == kSWarps) {
     if (lane == 0) {
-      int issued = 0;
-      for (int it = 0; it < ntile; ++it) {
-        const int s = it % kEsStages, r = it / kEsStages;
-        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, err)) { *s_abort = 1; break; }
+      // the value sums and counts (index data) of the first stages stream before the dependency
+      // wait; the scores come from the previous kernel
+      auto issue_index = [&](int it) {
+        const int s = it % kEsStages;
         const int j0 = c0 + it * kSTile, nj = min(kSTile, c1 - j0);
         mbar_arrive_expect_tx(&full[s], (uint32_t)nj * (WI_D * 4 + 4 + 4 * G));
         const size_t row = (size_t)u * C + j0;
         bulk_g2s(st[s].vs, valsum + row * WI_D, nj * WI_D * 4, &full[s]);
         bulk_g2s(st[s].cnt, cnt + row, nj * 4, &full[s]);
+      };
+      auto issue_scores = [&](int it) {
+        const int s = it % kEsStages;
+        const int j0 = c0 + it * kSTile, nj = min(kSTile, c1 - j0);
         for (int h = 0; h < G; ++h) bulk_g2s(st[s].sc[h], scores + ((size_t)u * G + h) * C + j0, nj * 4, &full[s]);
+      };
+      const int pre = min(ntile, kEsStages);
+      for (int it = 0; it < pre; ++it) issue_index(it);
+      pdl_wait();
+      for (int it = 0; it < pre; ++it) issue_scores(it);
+      int issued = pre;
+      for (int it = pre; it < ntile; ++it) {
+        const int s = it % kEsStages, r = it / kEsStages;
+        if (!mbar_wait(&empty[s], (r - 1) & 1, err)) { *s_abort = 1; break; }
+        issue_index(it);
+        issue_scores(it);
         issued = it + 1;
       }
       if (*s_abort) drain_stages<kEsStages>(full, issued, err);
+    } else {
+      pdl_wait();
     }
   } else {
+    pdl_wait();
     float* pb = pbuf + warp * 2 * 32;
     float* sb = sbuf + warp * 2 * 4;
     for (int it = 0; it < ntile; ++it) {
@@ -454,8 +470,6 @@ struct alignas(16) SelSmem {
   int s_wsum[32];
   uint32_t s_wmax[32];
   int s_bin, s_above, s_ncand, s_found;
-  uint32_t s_tkey;
-  int s_tid;
   int s_wt[32];
   float s_wf[32];
   uint32_t ckey[kSelThreads];
@@ -465,12 +479,12 @@ struct alignas(16) SelSmem {
 static_assert(sizeof(SelSmem) % 16 == 0, "the cached keys follow SelSmem 16-byte aligned");
 // Shared memory of the select role beyond SelSmem (a multiple of 16 bytes):
 // the keys (16-byte aligned, when cached), then per 32-id chunk the take bits
-// and their prefix, then the selected ids in position order and their first
-// rows among the selected rows.
+// and their prefix, then per selected position its id, rows, first row in the
+// index and first row among the selected rows.
 __host__ __device__ inline size_t sel_keys_bytes(int C) { return C <= kSelKeysMax ? (size_t)C * 4 : 0; }
 __host__ __device__ inline size_t sel_smem_bytes(int C, int kmax) {
   const size_t nch = ((size_t)C + 31) / 32;
-  return sizeof(SelSmem) + sel_keys_bytes(C) + nch * 8 + (size_t)kmax * 8;
+  return sizeof(SelSmem) + sel_keys_bytes(C) + nch * 8 + (size_t)kmax * 16;
 }
 
 // Block-wide search over 2048 ascending bins (thread t < 512 owns bins 4t..4t+3):
@@ -506,14 +520,15 @@ __device__ __forceinline__ bool find_bin(const int* hist, int target, SelSmem& s
   return true;
 }
 
-// Exclusive prefix, in place, of n ints in shared memory (each thread sums a
-// contiguous run); returns the total.  Ends with a barrier.
-__device__ __forceinline__ int block_excl_scan(int* v, int n, SelSmem& sm) {
+// Exclusive prefix over 32-id chunks of the number of set take bits:
+// pre[c] = sum of popc(tm[c']) for c' < c (each thread sums a contiguous run);
+// returns the total.  Ends with a barrier.
+__device__ __forceinline__ int block_popc_scan(const uint32_t* tm, int* pre, int n, SelSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (n + kSThreads - 1) / kSThreads;
   const int b0 = min(n, tid * per), b1 = min(n, b0 + per);
   int sum = 0;
-  for (int i = b0; i < b1; ++i) sum += v[i];
+  for (int i = b0; i < b1; ++i) sum += __popc(tm[i]);
   const int inc = warp_inclusive_scan(sum);
   if (lane == 31) sm.s_wt[warp] = inc;
   __syncthreads();
@@ -526,9 +541,8 @@ __device__ __forceinline__ int block_excl_scan(int* v, int n, SelSmem& sm) {
   }
   int run = before + inc - sum;
   for (int i = b0; i < b1; ++i) {
-    const int t = v[i];
-    v[i] = run;
-    run += t;
+    pre[i] = run;
+    run += __popc(tm[i]);
   }
   __syncthreads();
   return total;
@@ -544,41 +558,64 @@ struct KeySrc {
   }
 };
 
+constexpr int kSB = 8;  // keys per thread per batch: all loads of a batch are issued before any use
+
 __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& a, int u, int h) {
   SelSmem& sm = *reinterpret_cast<SelSmem*>(raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t uh = (size_t)u * a.G + h;
-  const int C = a.C, nch = (C + 31) / 32;
-  uint32_t* ks = reinterpret_cast<uint32_t*>(raw + sizeof(SelSmem));                 // [C] if cached
+  const int C = a.C, nch = (C + 31) / 32, kmax = a.kmax;
+  uint32_t* ks = reinterpret_cast<uint32_t*>(raw + sizeof(SelSmem));                        // [C] if cached
   uint32_t* tmask = reinterpret_cast<uint32_t*>(raw + sizeof(SelSmem) + sel_keys_bytes(C));  // [nch]
-  int* cpre = reinterpret_cast<int*>(tmask + nch);                                     // [nch]
-  int* sel_s = cpre + nch;                                                             // [kmax]
+  int* cpre = reinterpret_cast<int*>(tmask + nch);                                            // [nch]
+  int* sel_s = cpre + nch;                                                                    // [kmax] ids
+  int* nc_s = sel_s + kmax;                                                                   // [kmax] rows
+  int* of_s = nc_s + kmax;                                                                    // [kmax] first row
+  int* rp_s = of_s + kmax;  // [kmax] first row among the selected rows
   const float* s = a.scores + uh * C;
   const int* cn = a.cnt + (size_t)u * C;
-  int* out = a.sel + uh * a.kmax;
+  int* out = a.sel + uh * kmax;
   const bool cached = C <= kSelKeysMax;
   const KeySrc key_of{cached ? ks : nullptr, s, cn};
-  int kk = min(a.kmax, a.nonempty[u]);
+  int kk = min(kmax, a.nonempty[u]);
   for (int i = tid; i < 2 * kTopkBins; i += kSThreads) (&sm.hist[0][0])[i] = 0;
   if (tid == 0) { sm.s_ncand = 0; sm.s_found = 0; }
   // ---- keys (C is a multiple of 16) and their maximum
   uint32_t kmx = 0u;
   if (cached) {
-#pragma unroll 4
-    for (int i = tid; i < C / 4; i += kSThreads) {
-      const float4 f4 = __ldcg(reinterpret_cast<const float4*>(s) + i);
-      const int4 c4 = __ldg(reinterpret_cast<const int4*>(cn) + i);
-      uint4 k4;
-      k4.x = c4.x > 0 ? float_key(f4.x) : 0u;
-      k4.y = c4.y > 0 ? float_key(f4.y) : 0u;
-      k4.z = c4.z > 0 ? float_key(f4.z) : 0u;
-      k4.w = c4.w > 0 ? float_key(f4.w) : 0u;
-      reinterpret_cast<uint4*>(ks)[i] = k4;
-      kmx = max(kmx, max(max(k4.x, k4.y), max(k4.z, k4.w)));
+    const int n4 = C / 4;
+    for (int i0 = tid; i0 < n4; i0 += 4 * kSThreads) {
+      float4 f[4];
+      int4 c[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int i = i0 + r * kSThreads;
+        f[r] = i < n4 ? __ldcg(reinterpret_cast<const float4*>(s) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        c[r] = i < n4 ? __ldg(reinterpret_cast<const int4*>(cn) + i) : make_int4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int i = i0 + r * kSThreads;
+        uint4 k4;
+        k4.x = c[r].x > 0 ? float_key(f[r].x) : 0u;
+        k4.y = c[r].y > 0 ? float_key(f[r].y) : 0u;
+        k4.z = c[r].z > 0 ? float_key(f[r].z) : 0u;
+        k4.w = c[r].w > 0 ? float_key(f[r].w) : 0u;
+        if (i < n4) reinterpret_cast<uint4*>(ks)[i] = k4;
+        kmx = max(kmx, max(max(k4.x, k4.y), max(k4.z, k4.w)));
+      }
     }
   } else {
-#pragma unroll 4
-    for (int j = tid; j < C; j += kSThreads) kmx = max(kmx, key_of(j));
+    for (int j0 = tid; j0 < C; j0 += kSB * kSThreads) {
+      uint32_t kb[kSB];
+#pragma unroll
+      for (int r = 0; r < kSB; ++r) {
+        const int j = j0 + r * kSThreads;
+        kb[r] = j < C ? key_of(j) : 0u;
+      }
+#pragma unroll
+      for (int r = 0; r < kSB; ++r) kmx = max(kmx, kb[r]);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) kmx = max(kmx, __shfl_xor_sync(0xffffffffu, kmx, o));
@@ -591,45 +628,61 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   // ---- logarithmic histogram of d = K0 - key.  Keys at d >= 2^30 (in practice the negative
   // scores, often half of all keys) fall into a handful of bins where shared-memory atomics
   // would serialize; they are counted only if the nearer keys number fewer than k.
-  if (kk > 0) {
-#pragma unroll 4
-    for (int j = tid; j < C; j += kSThreads) {
-      const uint32_t k = key_of(j);
-      if (k != 0u && K0 - k < (1u << 30)) atomicAdd(&sm.hist[0][log_bin(K0 - k)], 1);
+  auto count_keys = [&](bool far) {
+    for (int j0 = tid; j0 < C; j0 += kSB * kSThreads) {
+      uint32_t kb[kSB];
+#pragma unroll
+      for (int r = 0; r < kSB; ++r) {
+        const int j = j0 + r * kSThreads;
+        kb[r] = j < C ? key_of(j) : 0u;
+      }
+#pragma unroll
+      for (int r = 0; r < kSB; ++r)
+        if (kb[r] != 0u && (K0 - kb[r] >= (1u << 30)) == far) atomicAdd(&sm.hist[0][log_bin(K0 - kb[r])], 1);
     }
-  }
+  };
+  if (kk > 0) count_keys(false);
   __syncthreads();
   bool found = kk == 0;
-  int bstar = -1, remaining = 0;
+  int bstar = -1, remaining = 0;  // -1: no bin, nothing is taken
   if (kk > 0) {
     int above = 0;
     found = find_bin(sm.hist[0], kk, sm, &bstar, &above);
     if (!found) {  // the k-th key is a far one: add the far keys and search again
-      for (int j = tid; j < C; j += kSThreads) {
-        const uint32_t k = key_of(j);
-        if (k != 0u && K0 - k >= (1u << 30)) atomicAdd(&sm.hist[0][log_bin(K0 - k)], 1);
-      }
+      count_keys(true);
       __syncthreads();
       found = find_bin(sm.hist[0], kk, sm, &bstar, &above);
     }
     remaining = kk - above;
+    if (!found) bstar = -1;
   }
-  uint32_t Tk = 0xffffffffu;
-  int Tid = -1;
-  if (kk > 0 && found) {
-    // ---- the keys of the threshold bin
-#pragma unroll 4
-    for (int j = tid; j < C; j += kSThreads) {
-      const uint32_t k = key_of(j);
-      if (k != 0u && log_bin(K0 - k) == bstar) {
+  // ---- one pass over 32-id chunks: keys in bins below the threshold bin are taken (ballot),
+  // keys in it are candidates
+  for (int c0 = warp; c0 < nch; c0 += kSB * kSNW) {
+    uint32_t kb[kSB];
+#pragma unroll
+    for (int r = 0; r < kSB; ++r) {
+      const int c = c0 + r * kSNW, j = c * 32 + lane;
+      kb[r] = (c < nch && j < C) ? key_of(j) : 0u;
+    }
+#pragma unroll
+    for (int r = 0; r < kSB; ++r) {
+      const int c = c0 + r * kSNW;
+      if (c >= nch) break;  // warp-uniform
+      const int b = (kk > 0 && kb[r] != 0u) ? log_bin(K0 - kb[r]) : kTopkBins;
+      const unsigned m = __ballot_sync(0xffffffffu, b < bstar);
+      if (lane == 0) tmask[c] = m;
+      if (b == bstar) {
         const int slot = atomicAdd(&sm.s_ncand, 1);
-        if (slot < kSelThreads) { sm.ckey[slot] = k; sm.cid[slot] = j; }
+        if (slot < kSelThreads) { sm.ckey[slot] = kb[r]; sm.cid[slot] = c * 32 + lane; }
       }
     }
-    __syncthreads();
-    const int ncand = sm.s_ncand;
+  }
+  __syncthreads();
+  const int ncand = sm.s_ncand;
+  if (kk > 0 && found) {
     if (ncand <= kSelThreads) {
-      // rank of candidate tid in (key descending, id ascending) order; rank remaining-1 is the k-th key
+      // rank of candidate tid in (key descending, id ascending) order: the first `remaining` are taken
       if (tid < ncand) {
         const uint32_t mk = sm.ckey[tid];
         const int mi = sm.cid[tid];
@@ -638,11 +691,12 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
           const uint32_t kj = sm.ckey[j];
           rank += (kj > mk || (kj == mk && sm.cid[j] < mi)) ? 1 : 0;
         }
-        if (rank == remaining - 1) { sm.s_tkey = mk; sm.s_tid = mi; sm.s_found = 1; }
+        if (rank < remaining) atomicOr(&tmask[mi >> 5], 1u << (mi & 31));
       }
     } else {
       // ---- many keys in one bin: radix select (11-bit digits, ascending) over the 48-bit
-      // composite (d << 16) | id of the bin's keys; ids are < 65536.
+      // composite (d << 16) | id of the bin's keys (ids are < 65536): the remaining-th one
+      // is the last taken
       unsigned long long cpfx = 0ull, cmask = 0ull;
       int rem = remaining;
       bool ok = true;
@@ -666,52 +720,49 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
         cpfx |= (unsigned long long)bin << sh;
         cmask |= dmask << sh;
       }
-      if (ok && tid == 0) {
-        sm.s_tkey = K0 - (uint32_t)(cpfx >> 16);
-        sm.s_tid = (int)(cpfx & 0xffffull);
-        sm.s_found = 1;
+      if (ok) {  // uniform
+        for (int j = tid; j < C; j += kSThreads) {
+          const uint32_t k = key_of(j);
+          if (k == 0u) continue;
+          const uint32_t d = K0 - k;
+          const unsigned long long comp = ((unsigned long long)d << 16) | (unsigned)j;
+          if (log_bin(d) == bstar && comp <= cpfx) atomicOr(&tmask[j >> 5], 1u << (j & 31));
+        }
       }
-    }
-    __syncthreads();
-    found = sm.s_found != 0;
-    Tk = sm.s_tkey;
-    Tid = sm.s_tid;
-  }
-  if (!found) {  // inconsistent counts: select nothing, report it
-    if (tid == 0) atomicOr(a.err, WI_DEVERR_TOPK);
-    kk = 0;
-  }
-  // ---- the selection in id order: cluster j is taken iff (key, -id) >= (Tk, -Tid)
-  for (int c = warp; c < nch; c += kSNW) {
-    const int j = c * 32 + lane;
-    const uint32_t k = j < C ? key_of(j) : 0u;
-    const bool take = kk > 0 && k != 0u && (k > Tk || (k == Tk && j <= Tid));
-    const unsigned m = __ballot_sync(0xffffffffu, take);
-    if (lane == 0) {
-      tmask[c] = m;
-      cpre[c] = __popc(m);
     }
   }
   __syncthreads();
-  const int total = block_excl_scan(cpre, nch, sm);
+  // ---- the selection in id order
+  const int total = block_popc_scan(tmask, cpre, nch, sm);
   if (total != kk) {  // uniform; cannot happen with consistent counts
     if (tid == 0) atomicOr(a.err, WI_DEVERR_TOPK);
     kk = min(kk, total);  // every position below kk gets an id
   }
-  for (int c = warp; c < nch; c += kSNW) {
-    const unsigned m = tmask[c];
-    if (m & (1u << lane)) {
-      const int pos = cpre[c] + __popc(m & ((1u << lane) - 1u));
-      if (pos < kk) sel_s[pos] = c * 32 + lane;
+  for (int c0 = warp; c0 < nch; c0 += kSB * kSNW) {
+    uint32_t mb[kSB];
+    int pb[kSB];
+#pragma unroll
+    for (int r = 0; r < kSB; ++r) {
+      const int c = c0 + r * kSNW;
+      mb[r] = c < nch ? tmask[c] : 0u;
+      pb[r] = c < nch ? cpre[c] : 0;
+    }
+#pragma unroll
+    for (int r = 0; r < kSB; ++r) {
+      if (mb[r] & (1u << lane)) {
+        const int pos = pb[r] + __popc(mb[r] & ((1u << lane) - 1u));
+        if (pos < kk) sel_s[pos] = (c0 + r * kSNW) * 32 + lane;
+      }
     }
   }
   __syncthreads();
   // ---- per selected cluster (position p = tid + rounds of kSThreads): rows and their prefix
-  int* rp_s = sel_s + a.kmax;  // [kmax] first row of position p among the selected rows
   int R = 0;
   for (int r0 = 0; r0 < kk; r0 += kSThreads) {  // uniform
     const int p = r0 + tid;
-    const int nc = p < kk ? __ldg(cn + sel_s[p]) : 0;
+    const int j = p < kk ? sel_s[p] : 0;
+    const int nc = p < kk ? __ldg(cn + j) : 0;
+    const int of = p < kk ? __ldg(a.off + (size_t)u * (C + 1) + j) : 0;
     const int inc = warp_inclusive_scan(nc);
     if (lane == 31) sm.s_wt[warp] = inc;
     __syncthreads();
@@ -722,25 +773,28 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
       b += __shfl_xor_sync(0xffffffffu, b, o);
       t += __shfl_xor_sync(0xffffffffu, t, o);
     }
-    if (p < kk) rp_s[p] = R + b + inc - nc;
+    if (p < kk) {
+      nc_s[p] = nc;
+      of_s[p] = of;
+      rp_s[p] = R + b + inc - nc;
+    }
     R += t;
-    __syncthreads();  // s_wt is reused by the next round
+    __syncthreads();  // s_wt is reused by the next round; the position arrays are complete
   }
   // ---- row run, weight and split starts per selected cluster
   const float m_sub = kk > 0 ? a.lam * key_float(K0) : -INFINITY;
   const int NS = a.NS;
-  int4* runs = a.runs + uh * a.kmax;
+  int4* runs = a.runs + uh * kmax;
   int4* splits = a.splits + uh * (NS + 1);
   float zpart = 0.f;
   // split b starts at row floor(R b / NS); the cluster holding that row records it
   const unsigned long long Rl = (unsigned long long)R;
   auto split_row = [&](int b) -> int { return (int)((Rl * (unsigned)b) / (unsigned)NS); };
   for (int p = tid; p < kk; p += kSThreads) {
-    const int j = sel_s[p], rp = rp_s[p];
-    const int nc = __ldg(cn + j), of = __ldg(a.off + (size_t)u * (C + 1) + j);
+    const int j = sel_s[p], nc = nc_s[p], rp = rp_s[p];
     const float w = __expf(a.lam * key_float(key_of(j)) - m_sub);
     out[p] = j;
-    runs[p] = make_int4(of, nc, __float_as_int(w), j);
+    runs[p] = make_int4(of_s[p], nc, __float_as_int(w), j);
     zpart = fmaf((float)nc, w, zpart);
     if (R == 0) continue;
     int b = (int)(((unsigned long long)rp * (unsigned)NS) / Rl);
@@ -751,7 +805,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
       splits[b] = make_int4(p, rb - rp, rb, 0);
     }
   }
-  for (int i = kk + tid; i < a.kmax; i += kSThreads) out[i] = -1;
+  for (int i = kk + tid; i < kmax; i += kSThreads) out[i] = -1;
   if (R == 0)  // nothing selected: every split is empty
     for (int b = tid; b < NS; b += kSThreads) splits[b] = make_int4(0, 0, 0, 0);
 #pragma unroll
@@ -774,9 +828,9 @@ template <int G>
 __global__ void __launch_bounds__(kSThreads, 1) k_select_estimate(TopkArgs a) {
   extern __shared__ __align__(128) unsigned char se_raw[];
   pdl_trigger();
-  pdl_wait();
   const int nsel = a.U * a.G;
   if ((int)blockIdx.x < nsel) {
+    pdl_wait();
     select_role(se_raw, a, blockIdx.x / a.G, blockIdx.x % a.G);
   } else {
     const int e = blockIdx.x - nsel;
