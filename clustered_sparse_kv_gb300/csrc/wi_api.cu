@@ -209,9 +209,11 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   A(b.subpart, U * G * WI_PART * 4);
   A(b.runs, U * G * (size_t)g.kmax * 16);
   A(b.splits, U * G * (size_t)(b.nsplit + 1) * 16);
+  A(b.sruns, U * G * (size_t)b.nsplit * 32 * 16);
   A(b.part3, U * G * (size_t)(b.nsplit + 1) * WI_PART * 4);
   A(b.subn, U * G * (size_t)(b.nsplit + 1) * WI_PART * 4);
   A(b.ticket, U * G * 4);
+  A(b.kmaxp, U * (size_t)b.p1 * G * 4);
   A(b.rows_total, 8);
   A(ix->q_dev, U * G * 128 * 2);
   A(ix->out_dev, U * G * 128 * 4);

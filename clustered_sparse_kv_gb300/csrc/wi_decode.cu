@@ -82,20 +82,24 @@ template <int G>
 struct ScCfg {
   static constexpr int STAGES = 6;
   static constexpr size_t A_OFF = kScQBytes;
-  static constexpr size_t BAR_OFF = A_OFF + (size_t)STAGES * kScATile;
+  static constexpr size_t CNT_OFF = A_OFF + (size_t)STAGES * kScATile;
+  static constexpr size_t WMAX_OFF = CNT_OFF + sizeof(int) * STAGES * kScTile;
+  static constexpr size_t BAR_OFF = WMAX_OFF + sizeof(uint32_t) * 32;
   static constexpr size_t SMEM = BAR_OFF + sizeof(uint64_t) * (2 * STAGES + 4) + 16;
 };
 
 template <int G>
 __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant__ CUtensorMap map_mu,
-                                                         const bf16* __restrict__ q,
-                                                         float* __restrict__ scores, int C,
-                                                         int P, int* err) {
+                                                         const bf16* __restrict__ q, const int* __restrict__ cnt,
+                                                         float* __restrict__ scores, unsigned* __restrict__ kmaxp,
+                                                         int C, int P, int* err) {
   using CF = ScCfg<G>;
   constexpr int STAGES = CF::STAGES;
   extern __shared__ __align__(1024) unsigned char sc_raw[];
   unsigned char* qB = sc_raw;                                              // [k half][16 rows][128 B]
   unsigned char* A = sc_raw + CF::A_OFF;                                   // [stage][k half][128 rows][128 B]
+  int* cnts = reinterpret_cast<int*>(sc_raw + CF::CNT_OFF);               // [stage][128]
+  uint32_t* wmax = reinterpret_cast<uint32_t*>(sc_raw + CF::WMAX_OFF);    // [epilogue warp][G]
   uint64_t* full = reinterpret_cast<uint64_t*>(sc_raw + CF::BAR_OFF);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
@@ -115,7 +119,7 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);  // the MMA commit: the tile has been read
+      mbar_init(&empty[s], 1 + kScEpiWarps);  // the MMA commit and every epilogue warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -137,9 +141,10 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
   auto issue = [&](int it) {
     const int s = it % STAGES;
     const int j0 = c0 + it * kScTile, nj = min(kScTile, c1 - j0);
-    mbar_arrive_expect_tx(&full[s], (uint32_t)kScATile);
+    mbar_arrive_expect_tx(&full[s], (uint32_t)(kScATile + nj * 4));
     tma_load_2d(A + (size_t)s * kScATile, &map_mu, 0, u * C + j0, &full[s]);
     tma_load_2d(A + (size_t)s * kScATile + kScATile / 2, &map_mu, 64, u * C + j0, &full[s]);
+    bulk_g2s(cnts + s * kScTile, cnt + (size_t)u * C + j0, nj * 4, &full[s]);
   };
   if (warp == 0 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_mu)) : "memory");
@@ -189,16 +194,20 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
       }
     }
   } else {
-    // epilogue: warp w reads TMEM lanes 32*(w%4).., i.e. clusters quarter*32 + lane of the tile
+    // epilogue: warp w reads TMEM lanes 32*(w%4).., i.e. clusters quarter*32 + lane of the tile;
+    // it also keeps the largest key of the non-empty clusters per head (for the top-k)
     const int quarter = warp & 3;
     bool ok = true;
+    uint32_t kmx[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) kmx[h] = 0u;
     for (int it = 0; it < ntile; ++it) {
-      const int b = it & 1;
+      const int s = it % STAGES, r = it / STAGES, b = it & 1;
       const int j0 = c0 + it * kScTile, nj = min(kScTile, c1 - j0);
       const int row = quarter * 32 + lane;
       uint32_t rr[16];
       if (ok) {
-        if (!mbar_wait(&tfull[b], (it >> 1) & 1, err)) {
+        if (!mbar_wait(&tfull[b], (it >> 1) & 1, err) || !mbar_wait(&full[s], r & 1, err)) {
           ok = false;
           *s_abort = 1;
         }
@@ -211,15 +220,35 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[b]);
+      const int cn = (ok && row < nj) ? cnts[s * kScTile + row] : 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
       const bool valid = ok && row < nj;
       if (valid) {
 #pragma unroll
-        for (int h = 0; h < G; ++h) scores[((size_t)u * G + h) * C + j0 + row] = __uint_as_float(rr[h]);
+        for (int h = 0; h < G; ++h) {
+          const float sc = __uint_as_float(rr[h]);
+          scores[((size_t)u * G + h) * C + j0 + row] = sc;
+          if (cn > 0) kmx[h] = max(kmx[h], float_key(sc));
+        }
       }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      uint32_t m = kmx[h];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) wmax[quarter * G + h] = m;
     }
   }
   tc_fence_before();
   __syncthreads();
+  if (tid < G) {  // this CTA's largest key per head: plain stores, the top-k takes the max over CTAs
+    uint32_t m = 0u;
+#pragma unroll
+    for (int q4 = 0; q4 < kScEpiWarps; ++q4) m = max(m, wmax[q4 * G + tid]);
+    kmaxp[((size_t)u * P + p) * G + tid] = m;
+  }
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"(tmem) : "memory");
@@ -423,9 +452,10 @@ __device__ void estimate_role(unsigned char* raw, const float* __restrict__ vals
 // summed where their rows are loaded (exact attention), and both are
 // subtracted from the estimate at the merge.
 //
-// Every loop runs over the clusters with the CTA's stride and is kept rolled:
-// the role runs once per CTA, from a cold instruction cache, so code size is
-// latency.  The keys are cached in shared memory when C <= kSelKeysMax, else
+// Every pass over the clusters is a short rolled loop with the CTA's stride:
+// the role runs once per CTA per step and its instructions mostly miss the
+// instruction cache, so the code executed once is kept small (the rare paths
+// are out of line).  The keys are cached in shared memory when C <= kSelKeysMax, else
 // recomputed from the (L2-resident) scores and counts at every pass.
 constexpr int kSelThreads = 512;  // ranking capacity: candidates in the threshold bin
 constexpr int kSelWarps = kSelThreads / 32;
@@ -440,12 +470,20 @@ __device__ __forceinline__ float key_float(uint32_t k) {
 
 // Logarithmic bin of a distance: 64 * (position of the leading one) + the next
 // six bits (d = 0 and 1 share bin 0).  Non-decreasing in d; within a bin of
-// leading position m >= 6 only the low m - 6 bits of d vary.
+// leading position m >= 6 only the low m - 6 bits of d vary.  Computed from
+// d converted to float with rounding toward zero: its exponent is m + 127 and
+// the top six bits of its mantissa are the six bits after the leading one, so
+// bits 30..17 of the float are 64 (m + 127) + those bits (branch-free).
 __device__ __forceinline__ int log_bin(uint32_t d) {
-  if (d == 0u) return 0;
-  const int m = 31 - __clz(d);
-  const uint32_t sub = m >= 6 ? (d >> (m - 6)) & 63u : (d << (6 - m)) & 63u;
-  return m * 64 + (int)sub;
+  return max((int)(__float_as_uint(__uint2float_rz(d)) >> 17) - 127 * 64, 0);
+}
+
+// Smallest d with log_bin(d) >= b (b in [0, 2047]): bin b > 0 starts at the
+// float 2^m (1 + sub / 64) (bits (b + 127 * 64) << 17), rounded up to an
+// integer; rounding toward zero maps d to a float >= that value exactly when
+// d >= it, since the value has 7 significant bits.
+__device__ __forceinline__ uint32_t log_bin_start(int b) {
+  return b == 0 ? 0u : __float2uint_ru(__uint_as_float((uint32_t)(b + 127 * 64) << 17));
 }
 
 struct TopkArgs {
@@ -459,17 +497,19 @@ struct TopkArgs {
   float* subpart;
   int4* runs;    // [U][G][kmax]  (first row, rows, weight bits e^{lam s - m_sub}, cluster id)
   int4* splits;  // [U][G][NS+1]  (position, row inside that cluster, split's first row, 0)
+  int4* sruns;   // [U][G][NS][32] runs of positions splits[b].x .. +31 (one read for the split's CTA)
   float* part1;  // estimation partials [U][G][PE]
+  const unsigned* kmaxp;  // [U][P1][G] largest key over the non-empty clusters of each k_scores CTA
   int* err;
-  int U, G, C, kmax, NS, PE, n_sink;
+  int U, G, C, kmax, NS, PE, n_sink, P1;
   float lam;
 };
 
 struct alignas(16) SelSmem {
   int hist[2][kTopkBins];
   int s_wsum[32];
-  uint32_t s_wmax[32];
-  int s_bin, s_above, s_ncand, s_found;
+  int s_bin, s_above, s_ncand, s_pad;
+  int s_spos[68];  // first position of each split
   int s_wt[32];
   float s_wf[32];
   uint32_t ckey[kSelThreads];
@@ -548,17 +588,61 @@ __device__ __forceinline__ int block_popc_scan(const uint32_t* tm, int* pre, int
   return total;
 }
 
+// Key of cluster j recomputed from the scores and counts (when the keys do not
+// fit in shared memory).  Out of line: it is the rare path.
+__device__ __noinline__ uint32_t key_global(const float* s, const int* cn, int j) {
+  return __ldg(cn + j) > 0 ? float_key(__ldcg(s + j)) : 0u;
+}
+
 struct KeySrc {
   const uint32_t* ks;  // cached keys, or null
   const float* s;
   const int* cn;
-  __device__ __forceinline__ uint32_t operator()(int j) const {
-    if (ks) return ks[j];
-    return __ldg(cn + j) > 0 ? float_key(__ldcg(s + j)) : 0u;
-  }
+  __device__ __forceinline__ uint32_t operator()(int j) const { return ks ? ks[j] : key_global(s, cn, j); }
 };
 
-constexpr int kSB = 8;  // keys per thread per batch: all loads of a batch are issued before any use
+// The threshold bin holds more keys than threads (large ties): radix select
+// (11-bit digits, ascending) over the 48-bit composite (d << 16) | id of the
+// bin's keys (ids < 65536); the remaining-th one is the last taken, and every
+// key of the bin up to it gets its take bit.  Out of line: the rare path.
+__device__ __noinline__ void take_in_bin_radix(const KeySrc key_of, int C, uint32_t K0, int bstar, int remaining,
+                                               uint32_t* tmask, SelSmem& sm) {
+  const int tid = threadIdx.x;
+  unsigned long long cpfx = 0ull, cmask = 0ull;
+  int rem = remaining;
+  bool ok = true;
+  for (int i = tid; i < kTopkBins; i += kSThreads) sm.hist[1][i] = 0;
+  __syncthreads();
+  for (int pass = 0; pass < 5 && ok; ++pass) {
+    const int sh = pass < 4 ? 37 - 11 * pass : 0;
+    const unsigned long long dmask = pass < 4 ? 2047ull : 15ull;
+    int* hc = sm.hist[(pass + 1) & 1];
+    int* hn = sm.hist[pass & 1];
+    for (int j = tid; j < C; j += kSThreads) {
+      const uint32_t k = key_of(j);
+      if (k == 0u) continue;
+      const uint32_t d = K0 - k;
+      const unsigned long long comp = ((unsigned long long)d << 16) | (unsigned)j;
+      if (log_bin(d) == bstar && (comp & cmask) == cpfx) atomicAdd(&hc[(comp >> sh) & dmask], 1);
+    }
+    __syncthreads();
+    for (int i = tid; i < kTopkBins; i += kSThreads) hn[i] = 0;
+    int bin = 0, above = 0;
+    ok = find_bin(hc, rem, sm, &bin, &above);
+    rem -= above;
+    cpfx |= (unsigned long long)bin << sh;
+    cmask |= dmask << sh;
+  }
+  if (ok) {  // uniform
+    for (int j = tid; j < C; j += kSThreads) {
+      const uint32_t k = key_of(j);
+      if (k == 0u) continue;
+      const uint32_t d = K0 - k;
+      const unsigned long long comp = ((unsigned long long)d << 16) | (unsigned)j;
+      if (log_bin(d) == bstar && comp <= cpfx) atomicOr(&tmask[j >> 5], 1u << (j & 31));
+    }
+  }
+}
 
 __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& a, int u, int h) {
   SelSmem& sm = *reinterpret_cast<SelSmem*>(raw);
@@ -578,21 +662,39 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   const bool cached = C <= kSelKeysMax;
   const KeySrc key_of{cached ? ks : nullptr, s, cn};
   int kk = min(kmax, a.nonempty[u]);
-  for (int i = tid; i < 2 * kTopkBins; i += kSThreads) (&sm.hist[0][0])[i] = 0;
-  if (tid == 0) { sm.s_ncand = 0; sm.s_found = 0; }
-  // ---- keys (C is a multiple of 16) and their maximum
-  uint32_t kmx = 0u;
+  // K0 = the largest key of a non-empty cluster, from k_scores' per-CTA maxima of the same
+  // scores (every warp reduces them itself: no barrier)
+  uint32_t K0 = 0u;
+  for (int i = lane; i < a.P1; i += 32) K0 = max(K0, __ldcg(a.kmaxp + ((size_t)u * a.P1 + i) * a.G + h));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) K0 = max(K0, __shfl_xor_sync(0xffffffffu, K0, o));
+  for (int i = tid; i < kTopkBins; i += kSThreads) sm.hist[0][i] = 0;
+  for (int i = tid; i < nch; i += kSThreads) tmask[i] = 0u;
+  if (tid == 0) sm.s_ncand = 0;
+  if (K0 == 0u) kk = 0;  // no non-empty cluster at all
+  // ---- keys (C is a multiple of 16) and the logarithmic histogram of d = K0 - key.  Keys at
+  // d >= 2^30 (in practice the negative scores, often half of all keys) fall into a handful of
+  // bins where shared-memory atomics would serialize; they are counted (second round) only if
+  // the nearer keys number fewer than k.
+  auto count_key = [&](uint32_t k, bool far) {
+    if (k != 0u && (K0 - k >= (1u << 30)) == far) atomicAdd(&sm.hist[0][log_bin(K0 - k)], 1);
+  };
   if (cached) {
     const int n4 = C / 4;
-    for (int i0 = tid; i0 < n4; i0 += 4 * kSThreads) {
-      float4 f[4];
-      int4 c[4];
+    float4 f[4];
+    int4 c[4];
+    auto load4 = [&](int i0) {
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int i = i0 + r * kSThreads;
         f[r] = i < n4 ? __ldcg(reinterpret_cast<const float4*>(s) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
         c[r] = i < n4 ? __ldg(reinterpret_cast<const int4*>(cn) + i) : make_int4(0, 0, 0, 0);
       }
+    };
+    load4(tid);       // in flight across the barrier
+    __syncthreads();  // the histogram and the masks are zero
+    for (int i0 = tid; i0 < n4; i0 += 4 * kSThreads) {
+      if (i0 != tid) load4(i0);
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int i = i0 + r * kSThreads;
@@ -601,80 +703,53 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
         k4.y = c[r].y > 0 ? float_key(f[r].y) : 0u;
         k4.z = c[r].z > 0 ? float_key(f[r].z) : 0u;
         k4.w = c[r].w > 0 ? float_key(f[r].w) : 0u;
-        if (i < n4) reinterpret_cast<uint4*>(ks)[i] = k4;
-        kmx = max(kmx, max(max(k4.x, k4.y), max(k4.z, k4.w)));
+        if (i < n4) {
+          reinterpret_cast<uint4*>(ks)[i] = k4;
+          if (kk > 0) {
+            count_key(k4.x, false);
+            count_key(k4.y, false);
+            count_key(k4.z, false);
+            count_key(k4.w, false);
+          }
+        }
       }
     }
   } else {
-    for (int j0 = tid; j0 < C; j0 += kSB * kSThreads) {
-      uint32_t kb[kSB];
-#pragma unroll
-      for (int r = 0; r < kSB; ++r) {
-        const int j = j0 + r * kSThreads;
-        kb[r] = j < C ? key_of(j) : 0u;
-      }
-#pragma unroll
-      for (int r = 0; r < kSB; ++r) kmx = max(kmx, kb[r]);
-    }
+    __syncthreads();
+    if (kk > 0)
+      for (int j = tid; j < C; j += kSThreads) count_key(key_of(j), false);
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) kmx = max(kmx, __shfl_xor_sync(0xffffffffu, kmx, o));
-  if (lane == 0) sm.s_wmax[warp] = kmx;
-  __syncthreads();
-  uint32_t K0 = lane < kSNW ? sm.s_wmax[lane] : 0u;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) K0 = max(K0, __shfl_xor_sync(0xffffffffu, K0, o));
-  if (K0 == 0u) kk = 0;  // no non-empty cluster at all
-  // ---- logarithmic histogram of d = K0 - key.  Keys at d >= 2^30 (in practice the negative
-  // scores, often half of all keys) fall into a handful of bins where shared-memory atomics
-  // would serialize; they are counted only if the nearer keys number fewer than k.
-  auto count_keys = [&](bool far) {
-    for (int j0 = tid; j0 < C; j0 += kSB * kSThreads) {
-      uint32_t kb[kSB];
-#pragma unroll
-      for (int r = 0; r < kSB; ++r) {
-        const int j = j0 + r * kSThreads;
-        kb[r] = j < C ? key_of(j) : 0u;
-      }
-#pragma unroll
-      for (int r = 0; r < kSB; ++r)
-        if (kb[r] != 0u && (K0 - kb[r] >= (1u << 30)) == far) atomicAdd(&sm.hist[0][log_bin(K0 - kb[r])], 1);
-    }
-  };
-  if (kk > 0) count_keys(false);
   __syncthreads();
   bool found = kk == 0;
-  int bstar = -1, remaining = 0;  // -1: no bin, nothing is taken
+  int bstar = -1, remaining = 0;  // bstar -1: no bin, nothing is taken
   if (kk > 0) {
     int above = 0;
     found = find_bin(sm.hist[0], kk, sm, &bstar, &above);
-    if (!found) {  // the k-th key is a far one: add the far keys and search again
-      count_keys(true);
+    if (!found) {  // uniform: the k-th key is a far one; add the far keys and search again
+      for (int j = tid; j < C; j += kSThreads) count_key(key_of(j), true);
       __syncthreads();
       found = find_bin(sm.hist[0], kk, sm, &bstar, &above);
     }
     remaining = kk - above;
     if (!found) bstar = -1;
   }
-  // ---- one pass over 32-id chunks: keys in bins below the threshold bin are taken (ballot),
-  // keys in it are candidates
-  for (int c0 = warp; c0 < nch; c0 += kSB * kSNW) {
-    uint32_t kb[kSB];
-#pragma unroll
-    for (int r = 0; r < kSB; ++r) {
-      const int c = c0 + r * kSNW, j = c * 32 + lane;
-      kb[r] = (c < nch && j < C) ? key_of(j) : 0u;
-    }
-#pragma unroll
-    for (int r = 0; r < kSB; ++r) {
-      const int c = c0 + r * kSNW;
-      if (c >= nch) break;  // warp-uniform
-      const int b = (kk > 0 && kb[r] != 0u) ? log_bin(K0 - kb[r]) : kTopkBins;
-      const unsigned m = __ballot_sync(0xffffffffu, b < bstar);
-      if (lane == 0) tmask[c] = m;
-      if (b == bstar) {
+  // ---- one pass: keys in bins below the threshold bin are taken (their bit set in the chunk
+  // masks, about k of them), keys in it are candidates; bins are ranges of d, the threshold
+  // bin is [dlo, dhi)
+  const uint32_t dlo = bstar >= 0 ? log_bin_start(bstar) : 0u;
+  const uint32_t dhi = bstar >= 0 && bstar < kTopkBins - 1 ? log_bin_start(bstar + 1) : 0xffffffffu;
+  const bool top_open = bstar == kTopkBins - 1;  // the last bin also holds d = 2^32 - 1
+  if (bstar >= 0) {
+#pragma unroll 2
+    for (int j = tid; j < C; j += kSThreads) {
+      const uint32_t k = key_of(j);
+      const uint32_t d = K0 - k;
+      if (k == 0u || d >= dhi && !top_open) continue;
+      if (d < dlo) {
+        atomicOr(&tmask[j >> 5], 1u << (j & 31));
+      } else {
         const int slot = atomicAdd(&sm.s_ncand, 1);
-        if (slot < kSelThreads) { sm.ckey[slot] = kb[r]; sm.cid[slot] = c * 32 + lane; }
+        if (slot < kSelThreads) { sm.ckey[slot] = k; sm.cid[slot] = j; }
       }
     }
   }
@@ -687,48 +762,14 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
         const uint32_t mk = sm.ckey[tid];
         const int mi = sm.cid[tid];
         int rank = 0;
-        for (int j = 0; j < ncand; ++j) {
-          const uint32_t kj = sm.ckey[j];
-          rank += (kj > mk || (kj == mk && sm.cid[j] < mi)) ? 1 : 0;
+        for (int i = 0; i < ncand; ++i) {
+          const uint32_t ki = sm.ckey[i];
+          rank += (ki > mk || (ki == mk && sm.cid[i] < mi)) ? 1 : 0;
         }
         if (rank < remaining) atomicOr(&tmask[mi >> 5], 1u << (mi & 31));
       }
     } else {
-      // ---- many keys in one bin: radix select (11-bit digits, ascending) over the 48-bit
-      // composite (d << 16) | id of the bin's keys (ids are < 65536): the remaining-th one
-      // is the last taken
-      unsigned long long cpfx = 0ull, cmask = 0ull;
-      int rem = remaining;
-      bool ok = true;
-      for (int pass = 0; pass < 5 && ok; ++pass) {
-        const int sh = pass < 4 ? 37 - 11 * pass : 0;
-        const unsigned long long dmask = pass < 4 ? 2047ull : 15ull;
-        int* hc = sm.hist[(pass + 1) & 1];
-        int* hn = sm.hist[pass & 1];
-        for (int j = tid; j < C; j += kSThreads) {
-          const uint32_t k = key_of(j);
-          if (k == 0u) continue;
-          const uint32_t d = K0 - k;
-          const unsigned long long comp = ((unsigned long long)d << 16) | (unsigned)j;
-          if (log_bin(d) == bstar && (comp & cmask) == cpfx) atomicAdd(&hc[(comp >> sh) & dmask], 1);
-        }
-        __syncthreads();
-        for (int i = tid; i < kTopkBins; i += kSThreads) hn[i] = 0;
-        int bin = 0, above = 0;
-        ok = find_bin(hc, rem, sm, &bin, &above);
-        rem -= above;
-        cpfx |= (unsigned long long)bin << sh;
-        cmask |= dmask << sh;
-      }
-      if (ok) {  // uniform
-        for (int j = tid; j < C; j += kSThreads) {
-          const uint32_t k = key_of(j);
-          if (k == 0u) continue;
-          const uint32_t d = K0 - k;
-          const unsigned long long comp = ((unsigned long long)d << 16) | (unsigned)j;
-          if (log_bin(d) == bstar && comp <= cpfx) atomicOr(&tmask[j >> 5], 1u << (j & 31));
-        }
-      }
+      take_in_bin_radix(key_of, C, K0, bstar, remaining, tmask, sm);
     }
   }
   __syncthreads();
@@ -738,21 +779,11 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
     if (tid == 0) atomicOr(a.err, WI_DEVERR_TOPK);
     kk = min(kk, total);  // every position below kk gets an id
   }
-  for (int c0 = warp; c0 < nch; c0 += kSB * kSNW) {
-    uint32_t mb[kSB];
-    int pb[kSB];
-#pragma unroll
-    for (int r = 0; r < kSB; ++r) {
-      const int c = c0 + r * kSNW;
-      mb[r] = c < nch ? tmask[c] : 0u;
-      pb[r] = c < nch ? cpre[c] : 0;
-    }
-#pragma unroll
-    for (int r = 0; r < kSB; ++r) {
-      if (mb[r] & (1u << lane)) {
-        const int pos = pb[r] + __popc(mb[r] & ((1u << lane) - 1u));
-        if (pos < kk) sel_s[pos] = (c0 + r * kSNW) * 32 + lane;
-      }
+  for (int c = warp; c < nch; c += kSNW) {
+    const unsigned m = tmask[c];
+    if (m & (1u << lane)) {
+      const int pos = cpre[c] + __popc(m & ((1u << lane) - 1u));
+      if (pos < kk) sel_s[pos] = c * 32 + lane;
     }
   }
   __syncthreads();
@@ -781,33 +812,44 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
     R += t;
     __syncthreads();  // s_wt is reused by the next round; the position arrays are complete
   }
-  // ---- row run, weight and split starts per selected cluster
+  // ---- split b (< NS) starts at row floor(R b / NS): (position of the cluster holding that
+  // row, row inside it, the row); split NS is the end
   const float m_sub = kk > 0 ? a.lam * key_float(K0) : -INFINITY;
   const int NS = a.NS;
   int4* runs = a.runs + uh * kmax;
   int4* splits = a.splits + uh * (NS + 1);
-  float zpart = 0.f;
-  // split b starts at row floor(R b / NS); the cluster holding that row records it
-  const unsigned long long Rl = (unsigned long long)R;
-  auto split_row = [&](int b) -> int { return (int)((Rl * (unsigned)b) / (unsigned)NS); };
-  for (int p = tid; p < kk; p += kSThreads) {
-    const int j = sel_s[p], nc = nc_s[p], rp = rp_s[p];
-    const float w = __expf(a.lam * key_float(key_of(j)) - m_sub);
-    out[p] = j;
-    runs[p] = make_int4(of_s[p], nc, __float_as_int(w), j);
-    zpart = fmaf((float)nc, w, zpart);
-    if (R == 0) continue;
-    int b = (int)(((unsigned long long)rp * (unsigned)NS) / Rl);
-    while (b < NS && split_row(b) < rp) ++b;
-    for (; b < NS; ++b) {
-      const int rb = split_row(b);
-      if (rb >= rp + nc) break;
-      splits[b] = make_int4(p, rb - rp, rb, 0);
+  int4* sruns = a.sruns + uh * NS * 32;
+  if (tid < NS) {
+    int4 sp = make_int4(0, 0, 0, 0);
+    if (R > 0) {
+      const int rb = (int)(((unsigned long long)R * (unsigned)tid) / (unsigned)NS);
+      int lo = 0, hi = kk - 1;  // largest position whose first row is <= rb
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (rp_s[mid] <= rb) lo = mid; else hi = mid - 1;
+      }
+      sp = make_int4(lo, rb - rp_s[lo], rb, 0);
     }
+    splits[tid] = sp;
+    sm.s_spos[tid] = sp.x;
+  }
+  __syncthreads();
+  // ---- row run and weight per selected cluster; copies into the run windows of the splits
+  float zpart = 0.f;
+  for (int p = tid; p < kk; p += kSThreads) {
+    const int j = sel_s[p], nc = nc_s[p];
+    const float w = __expf(a.lam * key_float(key_of(j)) - m_sub);
+    const int4 run = make_int4(of_s[p], nc, __float_as_int(w), j);
+    out[p] = j;
+    runs[p] = run;
+    for (int b = 0; b < NS; ++b) {
+      const int p0 = sm.s_spos[b];
+      if (p0 > p) break;
+      if (p < p0 + 32) sruns[b * 32 + (p - p0)] = run;
+    }
+    zpart = fmaf((float)nc, w, zpart);
   }
   for (int i = kk + tid; i < kmax; i += kSThreads) out[i] = -1;
-  if (R == 0)  // nothing selected: every split is empty
-    for (int b = tid; b < NS; b += kSThreads) splits[b] = make_int4(0, 0, 0, 0);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) zpart += __shfl_xor_sync(0xffffffffu, zpart, o);
   if (lane == 0) sm.s_wf[warp] = zpart;
@@ -869,6 +911,7 @@ struct ExactArgs {
   const int* selcnt;
   const int4* runs;
   const int4* splits;
+  const int4* sruns;
   const float* valsum;
   const int* nonempty;
   const float* part1;    // [U][G][P]
@@ -993,15 +1036,17 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
     } else {
       // ---- selected clusters: rows [b_s, b_{s+1}) of the head's row-balanced split
       pdl_wait();
+      // one round trip: the split bounds and the copies of its first 32 runs
       const int4 sa = a.splits[uh * nsp + split];
       const int4 sb = a.splits[uh * nsp + split + 1];
       const int kk = min(a.selcnt[uh], a.kmax);
+      const int4 r0 = a.sruns[(uh * a.NS + split) * 32 + lane];
       int rows_left = sb.z - sa.z;
       int pos = max(sa.x, 0), in = sa.y;
       const int4* runs = a.runs + uh * a.kmax;
       while (rows_left > 0 && pos < kk) {
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-        const int4 rr = (pos + lane < kk) ? runs[pos + lane] : make_int4(0, 0, 0, 0);
+        const int4 rr = (pos + lane < kk) ? (pos == sa.x ? r0 : runs[pos + lane]) : make_int4(0, 0, 0, 0);
         const int nb = min(32, kk - pos);
         for (int i = 0; i < nb && rows_left > 0; ++i) {
           const int o = __shfl_sync(0xffffffffu, rr.x, i);
@@ -1036,14 +1081,49 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
     // split (clusters [first, last) of the selection), one round trip while the first stage lands
     float4 sub = make_float4(0.f, 0.f, 0.f, 0.f);
     if (split < a.NS) {
+      // the copies of the split's first 32 runs are read with the split bounds: window index
+      // o + warp + 8x, o = 1 if the split starts inside a cluster (both offsets are fetched)
+      const int4* sr = a.sruns + (uh * a.NS + split) * 32;
+      int4 e0[4], e1[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int i = warp + 8 * x;
+        e0[x] = sr[i];
+        e1[x] = i + 1 < 32 ? sr[i + 1] : make_int4(0, 0, 0, 0);
+      }
       const int4 sa = a.splits[uh * nsp + split];
       const int4 sb = a.splits[uh * nsp + split + 1];
       const int kk = min(a.selcnt[uh], a.kmax);
-      const int first = max(sa.x, 0) + (sa.y > 0 ? 1 : 0);
+      const int o = sa.y > 0 ? 1 : 0;
+      const int first = max(sa.x, 0) + o;
       const int last = min(sb.x + (sb.y > 0 ? 1 : 0), kk);
       const int4* runs = a.runs + uh * a.kmax;
       const float4* vsu = reinterpret_cast<const float4*>(a.valsum + (size_t)u * a.C * WI_D) + lane;
-      for (int c0 = first + warp; c0 < last; c0 += 4 * kD3Warps) {
+      auto add_terms = [&](const float (&ww)[4], const float4 (&vv)[4]) {
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          sub.x = fmaf(ww[x], vv[x].x, sub.x);
+          sub.y = fmaf(ww[x], vv[x].y, sub.y);
+          sub.z = fmaf(ww[x], vv[x].z, sub.z);
+          sub.w = fmaf(ww[x], vv[x].w, sub.w);
+        }
+      };
+      {
+        float4 vv[4];
+        float ww[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const int c = first + warp + 8 * x;
+          const int4 rr = o ? e1[x] : e0[x];
+          const bool v = c < last && o + warp + 8 * x < 32;
+          const int j = (v && rr.w >= 0 && rr.w < a.C) ? rr.w : 0;
+          ww[x] = v ? __int_as_float(rr.z) : 0.f;
+          vv[x] = __ldg(vsu + (size_t)j * (WI_D / 4));
+        }
+        add_terms(ww, vv);
+      }
+      // clusters beyond the window
+      for (int c0 = max(sa.x, 0) + 32 + warp; c0 < last; c0 += 4 * kD3Warps) {
         float4 vv[4];
         float ww[4];
 #pragma unroll
@@ -1054,13 +1134,7 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
           ww[x] = c < last ? __int_as_float(rr.z) : 0.f;
           vv[x] = __ldg(vsu + (size_t)j * (WI_D / 4));
         }
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          sub.x = fmaf(ww[x], vv[x].x, sub.x);
-          sub.y = fmaf(ww[x], vv[x].y, sub.y);
-          sub.z = fmaf(ww[x], vv[x].z, sub.z);
-          sub.w = fmaf(ww[x], vv[x].w, sub.w);
-        }
+        add_terms(ww, vv);
       }
     }
     const int ri = lane >> 2;  // the row (of the warp's 8) whose logit this lane ends with
@@ -1318,7 +1392,7 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   // scores
   static int smem_sc = 0;
   if ((e = wi_ensure_smem(k_scores<G>, ScCfg<G>::SMEM, &smem_sc)) != cudaSuccess) return e;
-  e = launch_pdl(k_scores<G>, dim3(b.p1, g.U), dim3(kScThreads), ScCfg<G>::SMEM, st, b.map_mu, q, b.scores, g.C,
+  e = launch_pdl(k_scores<G>, dim3(b.p1, g.U), dim3(kScThreads), ScCfg<G>::SMEM, st, b.map_mu, q, b.cnt, b.scores, b.kmaxp, g.C,
                  b.p1, b.err);
   if (e != cudaSuccess || (e = mark(ev, 1, st)) != cudaSuccess) return e;
   TopkArgs t;
@@ -1332,6 +1406,9 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   t.subpart = b.subpart;
   t.runs = b.runs;
   t.splits = b.splits;
+  t.kmaxp = b.kmaxp;
+  t.P1 = b.p1;
+  t.sruns = b.sruns;
   t.part1 = b.part1;
   t.err = b.err;
   t.U = g.U;
@@ -1354,6 +1431,7 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   a.selcnt = b.selcnt;
   a.runs = b.runs;
   a.splits = b.splits;
+  a.sruns = b.sruns;
   a.valsum = b.valsum;
   a.subn = b.subn;
   a.C = g.C;

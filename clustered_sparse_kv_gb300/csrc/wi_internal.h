@@ -68,9 +68,11 @@ struct WiDecodeBufs {
   float* subpart;         // [U][G][WI_PART]      estimation terms of the selected clusters
   int4* runs;             // [U][G][kmax]  (first row, rows, weight bits, id) of each selected cluster
   int4* splits;           // [U][G][nsplit+1]  row-balanced split starts over the selected rows
+  int4* sruns;            // [U][G][nsplit][32] the first 32 runs of each split (copies)
   float* part3;           // [U][G][nsplit+1][WI_PART]  exact partials (the last split: steady rows)
   float* subn;            // [U][G][nsplit+1][WI_PART]  retrieved clusters' value-sum terms per split
   unsigned int* ticket;   // [U][G]  CTAs of exact_merge finished, per head
+  unsigned int* kmaxp;    // [U][p1][G] largest score key over the non-empty clusters of each k_scores CTA
   unsigned long long* rows_total;  // running sum of exact rows loaded over all steps
   int* err;
   int p1;                 // k_scores CTAs per unit
