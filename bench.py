@@ -207,6 +207,20 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def profile_run(wi, torch, w, dev, steps):
+    """One index of the workload and `steps` decode steps, nothing timed."""
+    k, v = kvsynth.kv_cache(w)
+    kd = torch.from_numpy(k.view(np.int16)).to(dev)
+    vd = torch.from_numpy(v.view(np.int16)).to(dev)
+    ix = wi.WaveIndex.build(wi.config_from_workload(w), kd, vd)
+    for s in range(steps):
+        ix.decode(torch.from_numpy(kvsynth.queries(w, step=s).view(np.int16)).to(dev))
+    torch.cuda.synchronize()
+    ix.check()
+    ix.free()
+    print(json.dumps({"profile_steps": steps, "workload": w.name}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -221,6 +235,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-kernel-events", action="store_true",
                     help="do not record per-kernel events inside the timed region (value only)")
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="profiling run: build one index of the workload, run this many decode steps, "
+                         "print nothing else (a small case for ncu captures)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -248,6 +265,9 @@ def main():
         torch.cuda.synchronize()
 
     seed = w.seed + 1000 * rank
+    if args.profile_steps > 0:
+        profile_run(wi, torch, w, dev, args.profile_steps)
+        return
     k, v = kvsynth.kv_cache(w, seed=seed)
     k_dev = torch.from_numpy(k.view(np.int16)).to(dev)
     v_dev = torch.from_numpy(v.view(np.int16)).to(dev)

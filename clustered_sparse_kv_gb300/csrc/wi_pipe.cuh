@@ -58,12 +58,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-// Bulk prefetch global -> L2 (no completion tracking).  src and bytes must be
-// multiples of 16.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // Transpose-reduction across a warp: every lane holds NV partial values
 // (NV = 8, 16 or 32) of NV different sums.  Afterwards lane l holds the full
 // sum of index (l >> (5 - log2 NV)) in v[0].  Halving exchanges first (each
