@@ -1,0 +1,129 @@
+"""Full-size decode parity for the batch-16 workload (Llama-3-8B shape, 122880
+tokens, 128 units) and the grouped-query append workload (Qwen2.5-7B shape,
+batch 8, 262144 tokens, 7 query heads per kv head, 64 decode steps that each
+append a token), in the launch configuration of the default build.
+
+The oracle cannot cluster these sizes, so the library builds its own index
+(ten rounds); the index is checked by its invariants, and the oracle decodes
+sampled (unit, step) pairs with the exported index (same counts, members,
+mean keys and value sums), which pins every decode step (scores, top-k,
+estimation, exact attention, merge, append) at full size."""
+import numpy as np
+import pytest
+import torch
+
+import kvsynth
+import oracle
+from helpers import OUT_REL_L2, assignment_from_index, check_topk, params_of, rel_l2
+from test_gpu_build import dev16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def wi():
+    import clustered_sparse_kv_gb300 as m
+    return m
+
+
+def build_and_export(wi, w):
+    k, v = kvsynth.kv_cache(w)
+    cfg = wi.config_from_workload(w)
+    kt, vt = dev16(k), dev16(v)
+    ix = wi.WaveIndex.build(cfg, kt, vt)
+    exp = {name: t.cpu().numpy() for name, t in ix.export().items()}
+    torch.cuda.synchronize()
+    ix.check()
+    return k, v, kt, vt, ix, exp
+
+
+def check_invariants(w, k, kt, exp, units):
+    p = params_of(w)
+    I = oracle.indexed_positions(w.n_ctx, p)
+    kp = kt.reshape(w.units, w.n_ctx, 128)
+    kf = k.reshape(w.units, w.n_ctx, 128)
+    for u in units:
+        counts, perm = exp["counts"][u], exp["perm"][u]
+        assert counts.sum() == I.size
+        np.testing.assert_array_equal(np.sort(perm), I)
+        owner = np.repeat(np.arange(w.clusters), counts) // w.clusters_per_seg
+        assert np.all(perm // w.seg_len == owner)  # every cluster inside its segment
+        rows = kp[u, w.n_sink:w.n_ctx - w.local_window].cpu().numpy().view(np.uint16)
+        np.testing.assert_array_equal(rows, kf[u][perm])  # the permuted rows are the members' keys
+        np.testing.assert_array_equal(exp["offsets"][u][:-1], w.n_sink + np.concatenate([[0], np.cumsum(counts)[:-1]]))
+
+
+def oracle_index(w, exp, u):
+    p = params_of(w)
+    return {
+        "counts": exp["counts"][u].astype(np.int64),
+        "mu": oracle.bf16_from_bits(exp["mu"][u].view(np.uint16)).reshape(w.clusters, 128),
+        "valsum": exp["valsum"][u].astype(np.float64),
+        "assignment": assignment_from_index(exp["counts"][u], exp["perm"][u], w.n_ctx, p.n_sink),
+    }
+
+
+def check_step(w, u_list, k, v, exp, qb, got, ids, cnt, k_app=None, v_app=None):
+    p = params_of(w)
+    kk = oracle.budget_k(w.clusters, p)
+    Q = oracle.bf16_from_bits(qb).reshape(w.units, w.group, 128)
+    kf = k.reshape(w.units, w.n_ctx, 128)
+    vf = v.reshape(w.units, w.n_ctx, 128)
+    for u in u_list:
+        idx = oracle_index(w, exp, u)
+        K = oracle.bf16_from_bits(kf[u]).reshape(w.n_ctx, 128)
+        V = oracle.bf16_from_bits(vf[u]).reshape(w.n_ctx, 128)
+        ka = None if k_app is None else k_app[u]
+        va = None if v_app is None else v_app[u]
+        ref, info = oracle.decode_unit(Q[u], K, V, idx, p, ka, va, details=True)
+        err = rel_l2(got[u], ref)
+        assert err.max() <= OUT_REL_L2, (u, err.max())
+        ne = idx["counts"] > 0
+        for h in range(w.group):
+            check_topk(ids[u, h], cnt[u, h], info[h]["scores"], ne, kk)
+
+
+def test_batch16_120k(wi):
+    w = kvsynth.get_workload("llama3-8b-b16-120k")
+    assert (w.units, w.clusters, oracle.budget_k(w.clusters, params_of(w))) == (128, 7680, 139)
+    k, v, kt, vt, ix, exp = build_and_export(wi, w)
+    sample = [0, 77, 127]
+    check_invariants(w, k, kt, exp, sample)
+    qb = kvsynth.queries(w, step=0)
+    out = ix.decode(dev16(qb))
+    ids, cnt = ix.selection()
+    torch.cuda.synchronize()
+    ix.check()
+    got = out.cpu().numpy().reshape(w.units, w.group, 128).astype(np.float64)
+    assert np.isfinite(got).all()
+    check_step(w, sample, k, v, exp, qb, got, ids.cpu().numpy(), cnt.cpu().numpy())
+    ix.free()
+
+
+def test_gqa7_262k_append_64_steps(wi):
+    w = kvsynth.get_workload("qwen2.5-7b-b8-262k")
+    assert (w.units, w.group, w.clusters, oracle.budget_k(w.clusters, params_of(w))) == (32, 7, 16384, 295)
+    k, v, kt, vt, ix, exp = build_and_export(wi, w)
+    sample = [0, 13, 31]
+    check_invariants(w, k, kt, exp, sample)
+    T = w.decode_steps
+    ka, va = kvsynth.kv_cache(w, p0=w.n_ctx, p1=w.n_ctx + T)
+    KA = oracle.bf16_from_bits(ka).reshape(w.units, T, 128)
+    VA = oracle.bf16_from_bits(va).reshape(w.units, T, 128)
+    checked = 0
+    for t in range(T):
+        qb = kvsynth.queries(w, step=t)
+        out = ix.decode(dev16(qb), dev16(ka[:, :, :, t]), dev16(va[:, :, :, t]))
+        if t in (0, 1, 31, T - 1):
+            ids, cnt = ix.selection()
+            torch.cuda.synchronize()
+            ix.check()
+            got = out.cpu().numpy().reshape(w.units, w.group, 128).astype(np.float64)
+            assert np.isfinite(got).all()
+            check_step(w, sample, k, v, exp, qb, got, ids.cpu().numpy(), cnt.cpu().numpy(),
+                       KA[:, :t], VA[:, :t])
+            checked += 1
+    torch.cuda.synchronize()
+    ix.check()
+    assert checked == 4
+    ix.free()

@@ -162,6 +162,12 @@ def test_topk_half_tied(wi):
     assert run_case(wi, w, idx=idx, strict_ids=True) < 1e-4
 
 
+def test_decode_large_budget(wi):
+    # k above the top-k's list capacity (512): the selection goes through per-chunk bit masks
+    w = small(n_ctx=16384, seg_len=1024, clusters_per_seg=128, iters=2, n_q_heads=4, budget_k=700, seed=33)
+    assert run_case(wi, w, strict_ids=False) < 1e-4
+
+
 @pytest.mark.parametrize("n_sink,window", [(0, 16), (8, 0), (4, 64)])
 def test_decode_steady_zone_shapes(wi, n_sink, window):
     w = small(n_ctx=2048, seg_len=512, clusters_per_seg=32, iters=2, n_q_heads=4, n_sink=n_sink,
