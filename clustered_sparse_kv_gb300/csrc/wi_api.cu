@@ -208,8 +208,8 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   A(b.selcnt, U * G * 4);
   A(b.subpart, U * G * WI_PART * 4);
   A(b.runs, U * G * (size_t)g.kmax * 16);
-  A(b.splits, U * G * (size_t)(b.nsplit + 1) * 16);
-  A(b.sruns, U * G * (size_t)b.nsplit * 32 * 16);
+  A(b.splits, U * G * (size_t)(b.nsplit + 2) * 16);
+  A(b.sruns, U * G * (size_t)(b.nsplit + 1) * 32 * 16);
   A(b.part3, U * G * (size_t)(b.nsplit + 1) * WI_PART * 4);
   A(b.subn, U * G * (size_t)(b.nsplit + 1) * WI_PART * 4);
   A(b.ticket, U * G * 4);

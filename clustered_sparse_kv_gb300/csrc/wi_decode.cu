@@ -8,18 +8,20 @@
 //                    exp(q.mu_j/sqrt(d)) * valsum_j to the numerator
 //                    (a Jensen lower bound, zh 2.A);
 //   the zones merge into one softmax by log-sum-exp.
-// Three kernels per step, each over the whole batch:
-//   score_estimate  streams every cluster's mu / valsum / count through shared
-//                   memory (bulk copies, mbarrier pipeline) once: the scores
-//                   s_hj = q_h . mu_j of the G heads of the group, and the
-//                   estimation partial (m, Z, N) over ALL non-empty clusters;
-//   topk_sub        per head: radix select of the k best non-empty clusters
-//                   (ties to the lowest id, ids ascending) and the estimation
-//                   terms of exactly those clusters, to be taken back out;
-//   exact_merge     per head and row split: flash-decode over the steady rows
-//                   and the retrieved clusters' contiguous rows (bulk copies
-//                   into shared memory); the last CTA of a head merges
-//                   estimate - retrieved terms + exact partials by LSE.
+// Three kernels per step, each over the whole batch, chained by programmatic
+// dependent launch:
+//   k_scores          s_hj = q_h . mu_j for every cluster on the tensor cores
+//                     (tcgen05, TMA-fed), and each CTA's largest score key;
+//   k_select_estimate one launch, two roles: per head, the top-k clusters
+//                     (ties to the lowest id, ids ascending), their row runs and
+//                     the row-balanced splits of the exact rows; per range of
+//                     clusters, the estimation partial (m, Z, N) over ALL
+//                     non-empty clusters (streamed value sums);
+//   k_exact_merge     per head and row split: flash-decode over the steady rows
+//                     and the retrieved clusters' contiguous rows (bulk copies
+//                     into shared memory), plus the retrieved clusters' value-sum
+//                     terms; the last CTA of a head merges estimate - retrieved
+//                     terms + exact partials by LSE.
 #include <cuda_runtime.h>
 
 #include "wi_common.cuh"
@@ -496,12 +498,13 @@ struct TopkArgs {
   int* selcnt;
   float* subpart;
   int4* runs;    // [U][G][kmax]  (first row, rows, weight bits e^{lam s - m_sub}, cluster id)
-  int4* splits;  // [U][G][NS+1]  (position, row inside that cluster, split's first row, 0)
-  int4* sruns;   // [U][G][NS][32] runs of positions splits[b].x .. +31 (one read for the split's CTA)
+  int4* splits;  // [U][G][NS+2]  (position, row inside that cluster, split's first selected row, 0)
+  int4* sruns;   // [U][G][NS+1][32] runs of positions splits[b].x .. +31 (one read for the split's CTA)
+  const int* app_count;
   float* part1;  // estimation partials [U][G][PE]
   const unsigned* kmaxp;  // [U][P1][G] largest key over the non-empty clusters of each k_scores CTA
   int* err;
-  int U, G, C, kmax, NS, PE, n_sink, P1;
+  int U, G, C, kmax, NS, PE, n_sink, W, P1;
   float lam;
 };
 
@@ -812,23 +815,28 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
     R += t;
     __syncthreads();  // s_wt is reused by the next round; the position arrays are complete
   }
-  // ---- split b (< NS) starts at row floor(R b / NS): (position of the cluster holding that
-  // row, row inside it, the row); split NS is the end
+  // ---- NSP = NS + 1 row-balanced splits of the head's exact rows [steady rows | selected rows]
+  // (T = S + R rows): split b starts at row floor(T b / NSP), i.e. at selected row
+  // max(0, floor(T b / NSP) - S): (position of the cluster holding that row, row inside it, the
+  // selected row); entry NSP is the end.  Split 0 also takes the S steady rows.
   const float m_sub = kk > 0 ? a.lam * key_float(K0) : -INFINITY;
-  const int NS = a.NS;
+  const int NSP = a.NS + 1;
   int4* runs = a.runs + uh * kmax;
-  int4* splits = a.splits + uh * (NS + 1);
-  int4* sruns = a.sruns + uh * NS * 32;
-  if (tid < NS) {
+  int4* splits = a.splits + uh * (NSP + 1);
+  int4* sruns = a.sruns + uh * NSP * 32;
+  if (tid < NSP) {
     int4 sp = make_int4(0, 0, 0, 0);
-    if (R > 0) {
-      const int rb = (int)(((unsigned long long)R * (unsigned)tid) / (unsigned)NS);
+    const long long S = (long long)a.n_sink + a.W + max(*a.app_count, 0), T = S + R;
+    const int rb = (int)max(0LL, (T * tid) / NSP - S);
+    if (R > 0 && rb < R) {
       int lo = 0, hi = kk - 1;  // largest position whose first row is <= rb
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (rp_s[mid] <= rb) lo = mid; else hi = mid - 1;
       }
       sp = make_int4(lo, rb - rp_s[lo], rb, 0);
+    } else {
+      sp = make_int4(kk, 0, R, 0);
     }
     splits[tid] = sp;
     sm.s_spos[tid] = sp.x;
@@ -842,7 +850,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
     const int4 run = make_int4(of_s[p], nc, __float_as_int(w), j);
     out[p] = j;
     runs[p] = run;
-    for (int b = 0; b < NS; ++b) {
+    for (int b = 0; b < NSP; ++b) {
       const int p0 = sm.s_spos[b];
       if (p0 > p) break;
       if (p < p0 + 32) sruns[b * 32 + (p - p0)] = run;
@@ -857,7 +865,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   // the retrieved clusters' value-sum terms are summed by the exact-attention CTAs that load them
   if (tid == 0) {
     a.selcnt[uh] = kk;
-    splits[NS] = make_int4(kk, 0, R, 0);
+    splits[NSP] = make_int4(kk, 0, R, 0);
     float zz = 0.f;
     for (int w = 0; w < kSNW; ++w) zz += sm.s_wf[w];
     float* sp = a.subpart + uh * WI_PART;
@@ -881,14 +889,15 @@ __global__ void __launch_bounds__(kSThreads, 1) k_select_estimate(TopkArgs a) {
 }
 
 // ---------------------------------------------------------- exact_merge ----
-// CTA = (split, head, unit).  Splits 0..NS-1 take row-balanced shares of the
-// head's selected clusters (the split starts come from topk_sub); split NS
-// takes the steady rows (sinks and local window, which it starts copying
-// before the previous kernel has finished, then the appended tokens).  A
-// producer lane packs the row runs into 64-row stages (K and V rows
-// bulk-copied into shared memory; a stage with no rows ends the stream); 8
-// consumer warps take 8 rows each per stage, flash-decode style.  The last
-// CTA of the head (ticket counter) merges all partials into the output row.
+// CTA = (split, head, unit).  The head's exact rows -- the steady rows (sinks,
+// local window, appended tokens) followed by its selected clusters' rows in
+// position order -- are cut into NS+1 row-balanced splits by the top-k; split
+// 0 starts with the steady rows (sinks and window copied before the
+// dependency wait).  A producer lane packs the row runs into 64-row stages
+// (K and V rows bulk-copied into shared memory; a stage with no rows ends the
+// stream); 8 consumer warps take 8 rows each per stage, flash-decode style.
+// The last CTA of the head (ticket counter) merges all partials into the
+// output row.
 constexpr int kD3Rows = 64;
 constexpr int kD3Stages = 3;
 constexpr int kD3Warps = 8;
@@ -1021,26 +1030,24 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
       }
       atomicAdd(a.rows_total, (unsigned long long)pk.rows_done);
     };
-    if (split == a.NS) {
-      // ---- steady rows: sinks and local window are fixed since the build; appended rows after the wait
-      if (lane == 0) {
+    {
+      if (split == 0 && lane == 0) {
+        // ---- steady rows first: sinks and local window are fixed since the build (copied before
+        // the wait), appended rows after it
         ok = ok && pk.push(Ku, Vu, a.n_sink);
         ok = ok && pk.push(Ku + (size_t)(a.n - a.W) * WI_D, Vu + (size_t)(a.n - a.W) * WI_D, a.W);
       }
       pdl_wait();
-      if (lane == 0) {
+      if (split == 0 && lane == 0) {
         const int amax = a.max_append > 0 ? a.max_append : 1;
         ok = ok && pk.push(a.appK + (size_t)u * amax * WI_D, a.appV + (size_t)u * amax * WI_D, *a.app_count);
       }
-      finish();
-    } else {
       // ---- selected clusters: rows [b_s, b_{s+1}) of the head's row-balanced split
-      pdl_wait();
       // one round trip: the split bounds and the copies of its first 32 runs
-      const int4 sa = a.splits[uh * nsp + split];
-      const int4 sb = a.splits[uh * nsp + split + 1];
+      const int4 sa = a.splits[uh * (nsp + 1) + split];
+      const int4 sb = a.splits[uh * (nsp + 1) + split + 1];
       const int kk = min(a.selcnt[uh], a.kmax);
-      const int4 r0 = a.sruns[(uh * a.NS + split) * 32 + lane];
+      const int4 r0 = a.sruns[(uh * nsp + split) * 32 + lane];
       int rows_left = sb.z - sa.z;
       int pos = max(sa.x, 0), in = sa.y;
       const int4* runs = a.runs + uh * a.kmax;
@@ -1080,10 +1087,10 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
     // value-sum terms sum_j w_j valsum_j of the retrieved clusters whose first row lies in this
     // split (clusters [first, last) of the selection), one round trip while the first stage lands
     float4 sub = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (split < a.NS) {
+    {
       // the copies of the split's first 32 runs are read with the split bounds: window index
       // o + warp + 8x, o = 1 if the split starts inside a cluster (both offsets are fetched)
-      const int4* sr = a.sruns + (uh * a.NS + split) * 32;
+      const int4* sr = a.sruns + (uh * nsp + split) * 32;
       int4 e0[4], e1[4];
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
@@ -1091,8 +1098,8 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
         e0[x] = sr[i];
         e1[x] = i + 1 < 32 ? sr[i + 1] : make_int4(0, 0, 0, 0);
       }
-      const int4 sa = a.splits[uh * nsp + split];
-      const int4 sb = a.splits[uh * nsp + split + 1];
+      const int4 sa = a.splits[uh * (nsp + 1) + split];
+      const int4 sb = a.splits[uh * (nsp + 1) + split + 1];
       const int kk = min(a.selcnt[uh], a.kmax);
       const int o = sa.y > 0 ? 1 : 0;
       const int first = max(sa.x, 0) + o;
@@ -1407,6 +1414,8 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   t.runs = b.runs;
   t.splits = b.splits;
   t.kmaxp = b.kmaxp;
+  t.app_count = b.app_count;
+  t.W = g.W;
   t.P1 = b.p1;
   t.sruns = b.sruns;
   t.part1 = b.part1;

@@ -67,8 +67,8 @@ struct WiDecodeBufs {
   int* selcnt;            // [U][G]
   float* subpart;         // [U][G][WI_PART]      estimation terms of the selected clusters
   int4* runs;             // [U][G][kmax]  (first row, rows, weight bits, id) of each selected cluster
-  int4* splits;           // [U][G][nsplit+1]  row-balanced split starts over the selected rows
-  int4* sruns;            // [U][G][nsplit][32] the first 32 runs of each split (copies)
+  int4* splits;           // [U][G][nsplit+2]  starts of the nsplit+1 row-balanced splits (steady + selected rows)
+  int4* sruns;            // [U][G][nsplit+1][32] the first 32 runs of each split (copies)
   float* part3;           // [U][G][nsplit+1][WI_PART]  exact partials (the last split: steady rows)
   float* subn;            // [U][G][nsplit+1][WI_PART]  retrieved clusters' value-sum terms per split
   unsigned int* ticket;   // [U][G]  CTAs of exact_merge finished, per head
