@@ -69,12 +69,14 @@ __device__ void drain_stages(uint64_t* full, int issued, int* err) {
 // ---- k_scores: s_hj = q_h . mu_j for every cluster on the tensor cores.
 // Per 128-cluster tile: TMA loads the mean keys (A, 128 x 128 bf16, K-major,
 // 128-byte swizzle); one thread issues eight tcgen05.mma (M = 128 clusters,
-// N = 16 heads (G used, the rest zero), K = 16) into one of two 16-column TMEM
+// N = 16 heads (G used, the rest zero), K = 16) into one of four 16-column TMEM
 // accumulators; four epilogue warps read one cluster row each per lane
 // (tcgen05.ld 32x32b.x16) and store the G scores.  Warp 0: TMA producer;
-// warp 1: TMEM allocation + MMA; warps 2..5: epilogue.
+// warp 1: TMEM allocation + MMA; warps 2..5 and 6..9: two epilogue groups
+// that take alternate tiles (four accumulators, so both can be busy).
 constexpr int kScTile = 128;
-constexpr int kScEpiWarps = 4;
+constexpr int kScEpiWarps = 8;  // two groups of 4 (one TMEM lane quarter each), alternate tiles
+constexpr int kScAcc = 4;       // TMEM accumulators (16 columns each): tile it uses it % 4
 constexpr int kScThreads = 32 * (2 + kScEpiWarps);
 constexpr int kScATile = kScTile * WI_D * 2;  // 32 KB: two 16 KB halves of 64 columns
 constexpr int kScN = 16;                        // MMA N: heads padded to 16
@@ -86,8 +88,8 @@ struct ScCfg {
   static constexpr size_t A_OFF = kScQBytes;
   static constexpr size_t CNT_OFF = A_OFF + (size_t)STAGES * kScATile;
   static constexpr size_t WMAX_OFF = CNT_OFF + sizeof(int) * STAGES * kScTile;
-  static constexpr size_t BAR_OFF = WMAX_OFF + sizeof(uint32_t) * 32;
-  static constexpr size_t SMEM = BAR_OFF + sizeof(uint64_t) * (2 * STAGES + 4) + 16;
+  static constexpr size_t BAR_OFF = WMAX_OFF + sizeof(uint32_t) * kScEpiWarps * 8;
+  static constexpr size_t SMEM = BAR_OFF + sizeof(uint64_t) * (2 * STAGES + 2 * kScAcc) + 16;
 };
 
 template <int G>
@@ -105,8 +107,8 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
   uint64_t* full = reinterpret_cast<uint64_t*>(sc_raw + CF::BAR_OFF);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint32_t* tbase = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* tempty = tfull + kScAcc;
+  uint32_t* tbase = reinterpret_cast<uint32_t*>(tempty + kScAcc);
   int* s_abort = reinterpret_cast<int*>(tbase + 1);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (smem_addr(sc_raw) & 1023u) {  // the swizzled tiles need 1024-byte alignment; never run misaligned
@@ -121,17 +123,18 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + kScEpiWarps);  // the MMA commit and every epilogue warp
+      mbar_init(&empty[s], 1 + kScEpiWarps / 2);  // the MMA commit and the 4 warps of the tile's group
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kScAcc; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], kScEpiWarps);
+      mbar_init(&tempty[b], kScEpiWarps / 2);
     }
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;" ::"r"(smem_addr(tbase))
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tbase)),
+                 "n"(kScAcc * kScN)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -180,9 +183,9 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
       const uint32_t idesc = make_idesc(kScTile, kScN);
       const uint32_t q0 = smem_addr(qB);
       for (int it = 0; it < ntile; ++it) {
-        const int s = it % STAGES, r = it / STAGES, b = it & 1;
+        const int s = it % STAGES, r = it / STAGES, b = it % kScAcc;
         if (!mbar_wait(&full[s], r & 1, err)) { *s_abort = 1; break; }
-        if (it >= 2 && !mbar_wait(&tempty[b], ((it >> 1) - 1) & 1, err)) { *s_abort = 1; break; }
+        if (it >= kScAcc && !mbar_wait(&tempty[b], (it / kScAcc - 1) & 1, err)) { *s_abort = 1; break; }
         tc_fence_after();
         const uint32_t a0 = smem_addr(A + (size_t)s * kScATile);
 #pragma unroll
@@ -196,20 +199,21 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
       }
     }
   } else {
-    // epilogue: warp w reads TMEM lanes 32*(w%4).., i.e. clusters quarter*32 + lane of the tile;
-    // it also keeps the largest key of the non-empty clusters per head (for the top-k)
-    const int quarter = warp & 3;
+    // epilogue: group grp = (warp - 2) / 4 takes the tiles it = grp (mod 2); warp w reads TMEM
+    // lanes 32*(w%4).., i.e. clusters quarter*32 + lane of the tile; it also keeps the largest
+    // key of the non-empty clusters per head (for the top-k)
+    const int quarter = warp & 3, grp = (warp - 2) >> 2;
     bool ok = true;
     uint32_t kmx[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) kmx[h] = 0u;
-    for (int it = 0; it < ntile; ++it) {
-      const int s = it % STAGES, r = it / STAGES, b = it & 1;
+    for (int it = grp; it < ntile; it += 2) {
+      const int s = it % STAGES, r = it / STAGES, b = it % kScAcc;
       const int j0 = c0 + it * kScTile, nj = min(kScTile, c1 - j0);
       const int row = quarter * 32 + lane;
       uint32_t rr[16];
       if (ok) {
-        if (!mbar_wait(&tfull[b], (it >> 1) & 1, err) || !mbar_wait(&full[s], r & 1, err)) {
+        if (!mbar_wait(&tfull[b], (it / kScAcc) & 1, err) || !mbar_wait(&full[s], r & 1, err)) {
           ok = false;
           *s_abort = 1;
         }
@@ -240,7 +244,7 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
       uint32_t m = kmx[h];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) wmax[quarter * G + h] = m;
+      if (lane == 0) wmax[(warp - 2) * G + h] = m;
     }
   }
   tc_fence_before();
@@ -248,12 +252,12 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
   if (tid < G) {  // this CTA's largest key per head: plain stores, the top-k takes the max over CTAs
     uint32_t m = 0u;
 #pragma unroll
-    for (int q4 = 0; q4 < kScEpiWarps; ++q4) m = max(m, wmax[q4 * G + tid]);
+    for (int w8 = 0; w8 < kScEpiWarps; ++w8) m = max(m, wmax[w8 * G + tid]);
     kmaxp[((size_t)u * P + p) * G + tid] = m;
   }
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"(tmem) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kScAcc * kScN) : "memory");
   }
 }
 
