@@ -207,6 +207,26 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def rank_seed(w, rank):
+    """Each rank decodes its own independent replicas (weak scaling): seeds differ per rank."""
+    return w.seed + 1000 * rank
+
+
+def max_over_ranks(x, dist, device):
+    """The job's time is the slowest rank's: max over ranks (identity on one rank)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, steps, batch, layers, seconds):
+    """Whole-job throughput: every rank runs `steps` steps of batch x layers in `seconds` (max over ranks)."""
+    return world * steps * batch * layers / seconds
+
+
 def profile_run(wi, torch, w, dev, steps):
     """One index of the workload and `steps` decode steps, nothing timed."""
     k, v = kvsynth.kv_cache(w)
@@ -264,7 +284,7 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    seed = w.seed + 1000 * rank
+    seed = rank_seed(w, rank)
     if args.profile_steps > 0:
         profile_run(wi, torch, w, dev, args.profile_steps)
         return
@@ -354,10 +374,7 @@ def main():
     with ClockSampler(local) as clocks:
         ms = run_region(g_full, g_rest)
     barrier()
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     for ix in replicas:
         ix.check()
     ms_events = None
@@ -400,7 +417,7 @@ def main():
     achieved = cand[dom] / (mean_us[dom] * 1e-6) / 1e9 if mean_us[dom] > 0 else 0.0
     step_bytes = bytes_d1 + bytes_d3 + w.units * w.group * 128 * (2 + 4)
     ms_per_step = ms / K
-    value = world * K * w.batch * w.layers / (ms / 1e3)
+    value = job_value(world, K, w.batch, w.layers, ms / 1e3)
 
     # e2e: host buffers through the C ABI, copies inside the timed region
     for ix in replicas:
@@ -416,7 +433,9 @@ def main():
     for s in range(E):
         wi.wi_decode_step_host(replicas[s % R].handle, qh[s % 8], oh, stream=stream)
     e2e_s = time.perf_counter() - t0
-    e2e_val = world * E * w.batch * w.layers / e2e_s
+    barrier()
+    e2e_s = max_over_ranks(e2e_s, dist, dev)
+    e2e_val = job_value(world, E, w.batch, w.layers, e2e_s)
     for ix in replicas:
         ix.check()
 
