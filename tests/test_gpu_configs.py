@@ -1,7 +1,9 @@
 """Full-size decode parity for the batch-16 workload (Llama-3-8B shape, 122880
-tokens, 128 units) and the grouped-query append workload (Qwen2.5-7B shape,
+tokens, 128 units), the grouped-query append workload (Qwen2.5-7B shape,
 batch 8, 262144 tokens, 7 query heads per kv head, 64 decode steps that each
-append a token), in the launch configuration of the default build.
+append a token) and one kv head of the million-token workload (C = 65536
+clusters, k = 1180: the top-k without a shared-memory key cache and above its
+list capacity), in the launch configuration of the default build.
 
 The oracle cannot cluster these sizes, so the library builds its own index
 (ten rounds); the index is checked by its invariants, and the oracle decodes
@@ -126,4 +128,20 @@ def test_gqa7_262k_append_64_steps(wi):
     torch.cuda.synchronize()
     ix.check()
     assert checked == 4
+    ix.free()
+
+
+def test_one_million_tokens_one_kv_head(wi):
+    w = kvsynth.get_workload("llama3-8b-1m-32l").with_(layers=1, n_kv_heads=1, n_q_heads=4)
+    assert (w.units, w.clusters, oracle.budget_k(w.clusters, params_of(w))) == (1, 65536, 1180)
+    k, v, kt, vt, ix, exp = build_and_export(wi, w)
+    check_invariants(w, k, kt, exp, [0])
+    for step in range(2):
+        qb = kvsynth.queries(w, step=step)
+        out = ix.decode(dev16(qb))
+        ids, cnt = ix.selection()
+        torch.cuda.synchronize()
+        ix.check()
+        got = out.cpu().numpy().reshape(w.units, w.group, 128).astype(np.float64)
+        check_step(w, [0], k, v, exp, qb, got, ids.cpu().numpy(), cnt.cpu().numpy())
     ix.free()
