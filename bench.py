@@ -207,6 +207,16 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of the
+# current kernels on this workload (profiles/decode_kernels_llama3-8b-131k.md); to be retaken whenever
+# a kernel changes.
+NCU_TRAFFIC = {
+    ("llama3-8b-131k", "exact_merge"): 38.795776e6 + 28.672e3,
+    ("llama3-8b-131k", "select_estimate"): 35.144192e6,
+    ("llama3-8b-131k", "scores"): 17.07264e6,
+}
+
+
 def rank_seed(w, rank):
     """Each rank decodes its own independent replicas (weak scaling): seeds differ per rank."""
     return w.seed + 1000 * rank
@@ -458,7 +468,7 @@ def main():
                        "timing": f"CUDA graphs of {L} steps replayed; events on the launching stream"},
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_kind": peak_kind,
-                         "bytes_per_launch": cand[dom], "traffic": None},
+                         "bytes_per_launch": cand[dom], "traffic": NCU_TRAFFIC.get((w.name, dom))},
             "step_hbm_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
             "step_bytes": step_bytes,
             "exact_rows_per_step": rows_per_step,
