@@ -52,6 +52,11 @@ struct HeadGeo {
   static constexpr int SHIFT = GP == 4 ? 0 : (GP == 2 ? 1 : 2);
 };
 
+// Inverse of float_key for finite scores.
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 __device__ __forceinline__ void cluster_range(int C, int p, int P, int* c0, int* c1) {
   *c0 = (int)(((long long)C * p / P) & ~15LL);
   *c1 = p + 1 == P ? C : (int)(((long long)C * (p + 1) / P) & ~15LL);
@@ -95,7 +100,7 @@ struct ScCfg {
 template <int G>
 __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant__ CUtensorMap map_mu,
                                                          const bf16* __restrict__ q, const int* __restrict__ cnt,
-                                                         float* __restrict__ scores, unsigned* __restrict__ kmaxp,
+                                                         uint32_t* __restrict__ keys, unsigned* __restrict__ kmaxp,
                                                          int C, int P, int* err) {
   using CF = ScCfg<G>;
   constexpr int STAGES = CF::STAGES;
@@ -233,9 +238,9 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
       if (valid) {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float sc = __uint_as_float(rr[h]);
-          scores[((size_t)u * G + h) * C + j0 + row] = sc;
-          if (cn > 0) kmx[h] = max(kmx[h], float_key(sc));
+          const uint32_t key = cn > 0 ? float_key(__uint_as_float(rr[h])) : 0u;
+          keys[((size_t)u * G + h) * C + j0 + row] = key;
+          kmx[h] = max(kmx[h], key);
         }
       }
     }
@@ -275,14 +280,14 @@ constexpr int kEsStages = 3;
 struct EsStage {
   float vs[kSTile * WI_D];
   int cnt[kSTile];
-  float sc[8][kSTile];  // scores of up to 8 heads
+  uint32_t sc[8][kSTile];  // score keys of up to 8 heads (0: empty cluster)
 };
 constexpr size_t kEsSmem = sizeof(EsStage) * kEsStages + 2 * kEsStages * sizeof(uint64_t) +
                            sizeof(float) * kSWarps * 2 * 32 + sizeof(float) * kSWarps * 2 * 4 + 16;
 
 template <int G>
 __device__ void estimate_role(unsigned char* raw, const float* __restrict__ valsum, const int* __restrict__ cnt,
-                              const float* __restrict__ scores, float* __restrict__ part, int C, int u, int p,
+                              const uint32_t* __restrict__ scores, float* __restrict__ part, int C, int u, int p,
                               int P, float lam, int* err) {
   using HG = HeadGeo<G>;
   EsStage* st = reinterpret_cast<EsStage*>(raw);
@@ -361,7 +366,8 @@ __device__ void estimate_role(unsigned char* raw, const float* __restrict__ vals
         for (int b = 0; b < HG::HB; ++b) {
           const int head = b * 4 + hl;
           const bool valid = valid_c && head < G;
-          const float se = (valid && cn > 0) ? lam * T.sc[head < G ? head : 0][i0 + ci] : -INFINITY;
+          const uint32_t key = T.sc[head < G ? head : 0][i0 + ci];
+          const float se = (valid && cn > 0 && key != 0u) ? lam * key_float(key) : -INFINITY;
           float mx = fmaxf(se, __shfl_xor_sync(0xffffffffu, se, 4));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -469,10 +475,6 @@ constexpr int kBinsPerLane = kTopkBins / kSelThreads;  // 4
 constexpr int kSelKeysMax = 32768;
 constexpr int kSNW = kSThreads / 32;  // warps of the CTA
 
-// Inverse of float_key for finite scores.
-__device__ __forceinline__ float key_float(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
 
 // Logarithmic bin of a distance: 64 * (position of the leading one) + the next
 // six bits (d = 0 and 1 share bin 0).  Non-decreasing in d; within a bin of
@@ -493,7 +495,7 @@ __device__ __forceinline__ uint32_t log_bin_start(int b) {
 }
 
 struct TopkArgs {
-  const float* scores;
+  const uint32_t* scores;  // [U][G][C] score keys (order-preserving bits; 0 = empty cluster)
   const int* cnt;
   const int* off;
   const int* nonempty;
@@ -597,15 +599,12 @@ __device__ __forceinline__ int block_popc_scan(const uint32_t* tm, int* pre, int
 
 // Key of cluster j recomputed from the scores and counts (when the keys do not
 // fit in shared memory).  Out of line: it is the rare path.
-__device__ __noinline__ uint32_t key_global(const float* s, const int* cn, int j) {
-  return __ldg(cn + j) > 0 ? float_key(__ldcg(s + j)) : 0u;
-}
+__device__ __noinline__ uint32_t key_global(const uint32_t* s, int j) { return __ldcg(s + j); }
 
 struct KeySrc {
   const uint32_t* ks;  // cached keys, or null
-  const float* s;
-  const int* cn;
-  __device__ __forceinline__ uint32_t operator()(int j) const { return ks ? ks[j] : key_global(s, cn, j); }
+  const uint32_t* s;
+  __device__ __forceinline__ uint32_t operator()(int j) const { return ks ? ks[j] : key_global(s, j); }
 };
 
 // The threshold bin holds more keys than threads (large ties): radix select
@@ -663,11 +662,11 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   int* nc_s = sel_s + kmax;                                                                   // [kmax] rows
   int* of_s = nc_s + kmax;                                                                    // [kmax] first row
   int* rp_s = of_s + kmax;  // [kmax] first row among the selected rows
-  const float* s = a.scores + uh * C;
+  const uint32_t* s = a.scores + uh * C;
   const int* cn = a.cnt + (size_t)u * C;
   int* out = a.sel + uh * kmax;
   const bool cached = C <= kSelKeysMax;
-  const KeySrc key_of{cached ? ks : nullptr, s, cn};
+  const KeySrc key_of{cached ? ks : nullptr, s};
   int kk = min(kmax, a.nonempty[u]);
   // K0 = the largest key of a non-empty cluster, from k_scores' per-CTA maxima of the same
   // scores (every warp reduces them itself: no barrier)
@@ -688,14 +687,12 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   };
   if (cached) {
     const int n4 = C / 4;
-    float4 f[4];
-    int4 c[4];
+    uint4 f[4];
     auto load4 = [&](int i0) {
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int i = i0 + r * kSThreads;
-        f[r] = i < n4 ? __ldcg(reinterpret_cast<const float4*>(s) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        c[r] = i < n4 ? __ldg(reinterpret_cast<const int4*>(cn) + i) : make_int4(0, 0, 0, 0);
+        f[r] = i < n4 ? __ldcg(reinterpret_cast<const uint4*>(s) + i) : make_uint4(0u, 0u, 0u, 0u);
       }
     };
     load4(tid);       // in flight across the barrier
@@ -705,11 +702,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int i = i0 + r * kSThreads;
-        uint4 k4;
-        k4.x = c[r].x > 0 ? float_key(f[r].x) : 0u;
-        k4.y = c[r].y > 0 ? float_key(f[r].y) : 0u;
-        k4.z = c[r].z > 0 ? float_key(f[r].z) : 0u;
-        k4.w = c[r].w > 0 ? float_key(f[r].w) : 0u;
+        const uint4 k4 = f[r];
         if (i < n4) {
           reinterpret_cast<uint4*>(ks)[i] = k4;
           if (kk > 0) {
@@ -1403,11 +1396,12 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   // scores
   static int smem_sc = 0;
   if ((e = wi_ensure_smem(k_scores<G>, ScCfg<G>::SMEM, &smem_sc)) != cudaSuccess) return e;
-  e = launch_pdl(k_scores<G>, dim3(b.p1, g.U), dim3(kScThreads), ScCfg<G>::SMEM, st, b.map_mu, q, b.cnt, b.scores, b.kmaxp, g.C,
+  e = launch_pdl(k_scores<G>, dim3(b.p1, g.U), dim3(kScThreads), ScCfg<G>::SMEM, st, b.map_mu, q, b.cnt,
+                 reinterpret_cast<uint32_t*>(b.scores), b.kmaxp, g.C,
                  b.p1, b.err);
   if (e != cudaSuccess || (e = mark(ev, 1, st)) != cudaSuccess) return e;
   TopkArgs t;
-  t.scores = b.scores;
+  t.scores = reinterpret_cast<const uint32_t*>(b.scores);
   t.cnt = b.cnt;
   t.off = b.off;
   t.nonempty = b.nonempty;
