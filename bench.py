@@ -212,8 +212,6 @@ def run_reference(args, w, rank, world):
 # a kernel changes.
 NCU_TRAFFIC = {
     ("llama3-8b-131k", "exact_merge"): 38.795776e6 + 28.672e3,
-    ("llama3-8b-131k", "select_estimate"): 35.144192e6,
-    ("llama3-8b-131k", "scores"): 17.07264e6,
 }
 
 
