@@ -933,51 +933,88 @@ struct ExactArgs {
   float lam;
 };
 
-// Producer state of exact_merge (lane 0 of the producer warp only).
-struct RunPacker {
+// Producer of exact_merge: the whole producer warp.  The CTA's rows form one
+// stream cut into 64-row stages; a batch of up to 32 runs (one per lane) is
+// placed by a prefix sum of their lengths, then for every stage the batch
+// touches, lane 0 opens the stage (waits until the consumers freed it) and
+// announces its bytes, and each lane bulk-copies the part of its own run that
+// falls in the stage (the copy engine takes ~60-100 cycles per copy, so the
+// copies of a stage are issued by several lanes at once); a stage is closed
+// once its 64 rows are placed.
+struct StagePacker {
   D3Stage* st;
   uint64_t* full;
   uint64_t* empty;
   int* nrows;
   int* err;
-  int stage_it = 0, fill = 0;
-  bool opened = false;
-  long long rows_done = 0;
+  int fpos = 0;     // rows placed so far (uniform in the warp)
+  int opened = -1;  // last stage opened
+  bool ok = true;   // uniform
 
-  __device__ bool open() {
-    const int s = stage_it % kD3Stages, r = stage_it / kD3Stages;
-    if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, err)) return false;
-    fill = 0;
-    opened = true;
-    return true;
-  }
-  __device__ void close() {
-    const int s = stage_it % kD3Stages;
-    nrows[s] = fill;
-    mbar_arrive(&full[s]);  // completes the stage once its announced bytes have landed
-    ++stage_it;
-    opened = false;
-  }
-  // rows [0, len) of the runs starting at kb / vb
-  __device__ bool push(const bf16* kb, const bf16* vb, int len) {
-    while (len > 0) {
-      if (!opened && !open()) return false;
-      const int s = stage_it % kD3Stages;
-      const int take = min(len, kD3Rows - fill);
-      const uint32_t bytes = (uint32_t)take * WI_D * 2;
-      asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&full[s])),
-                   "r"(2 * bytes)
-                   : "memory");
-      bulk_g2s(&st[s].k[fill * WI_D], kb, bytes, &full[s]);
-      bulk_g2s(&st[s].v[fill * WI_D], vb, bytes, &full[s]);
-      fill += take;
-      rows_done += take;
-      kb += (size_t)take * WI_D;
-      vb += (size_t)take * WI_D;
-      len -= take;
-      if (fill == kD3Rows) close();
+  // this lane's run: rows [0, len) at kb / vb (len 0: no run)
+  __device__ void push(const bf16* kb, const bf16* vb, int len) {
+    const int lane = threadIdx.x & 31;
+    const int incl = warp_inclusive_scan(len);
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    const int my0 = fpos + incl - len, my1 = my0 + len;
+    const int A = fpos, B = fpos + total;
+    for (int t = A / kD3Rows; ok && t * kD3Rows < B; ++t) {
+      const int s = t % kD3Stages, r = t / kD3Stages;
+      const int lo = max(A, t * kD3Rows), hi = min(B, (t + 1) * kD3Rows);
+      if (lane == 0) {
+        if (t > opened && r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, err)) ok = false;
+        if (ok)
+          asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&full[s])),
+                       "r"((uint32_t)(hi - lo) * WI_D * 4)
+                       : "memory");
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      opened = max(opened, t);
+      if (!ok) break;
+      const int p0 = max(my0, lo), p1 = min(my1, hi);
+      if (p1 > p0) {
+        const uint32_t bytes = (uint32_t)(p1 - p0) * WI_D * 2;
+        const int d = p0 - t * kD3Rows;
+        bulk_g2s(&st[s].k[d * WI_D], kb + (size_t)(p0 - my0) * WI_D, bytes, &full[s]);
+        bulk_g2s(&st[s].v[d * WI_D], vb + (size_t)(p0 - my0) * WI_D, bytes, &full[s]);
+      }
+      if (hi == (t + 1) * kD3Rows && lane == 0) {  // the stage is full: hand it over
+        nrows[s] = kD3Rows;
+        mbar_arrive(&full[s]);
+      }
     }
-    return true;
+    if (ok) fpos = B;
+  }
+  // Close the partial last stage and send the end marker (a stage with no rows); on failure,
+  // close what is open and wait for the copies in flight, so that none lands after the CTA left.
+  __device__ void finish(int* abort_flag) {
+    const int lane = threadIdx.x & 31;
+    if (lane != 0) return;
+    int t = fpos / kD3Rows;
+    if (ok && fpos % kD3Rows != 0) {  // opened stage with rows: close it
+      const int s = t % kD3Stages;
+      nrows[s] = fpos % kD3Rows;
+      mbar_arrive(&full[s]);
+      ++t;
+    }
+    if (ok) {  // the end marker
+      const int s = t % kD3Stages, r = t / kD3Stages;
+      if (t > opened && r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, err)) ok = false;
+      if (ok) {
+        nrows[s] = 0;
+        mbar_arrive(&full[s]);
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      if (fpos % kD3Rows != 0) {  // the stage being filled has rows in flight: let it complete
+        const int s = (fpos / kD3Rows) % kD3Stages;
+        nrows[s] = fpos % kD3Rows;
+        mbar_arrive(&full[s]);
+      }
+      for (int tt = max(0, opened - kD3Stages + 1); tt <= opened; ++tt)  // bounded waits
+        mbar_wait(&full[tt % kD3Stages], (tt / kD3Stages) & 1, err);
+    }
   }
 };
 
@@ -1008,70 +1045,49 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
   if (warp == kD3Warps) {
     const bf16* Ku = a.K + (size_t)u * a.n * WI_D;
     const bf16* Vu = a.V + (size_t)u * a.n * WI_D;
-    RunPacker pk{st, full, empty, nrows, a.err};
-    bool ok = true;
-    // Close the open stage and send the end marker (a stage with no rows); on failure, wait for
-    // the copies already in flight so that none lands after the CTA has left.
-    auto finish = [&]() {
-      if (lane != 0) return;
-      if (ok && pk.opened) pk.close();
-      if (ok) ok = pk.open();
-      if (ok) pk.close();
-      if (!ok) {
-        flags[0] = 1;
-        const int issued = pk.stage_it;
-        for (int s = 0; s < kD3Stages && s < issued; ++s) {
-          const int last = ((issued - 1 - s) / kD3Stages) * kD3Stages + s;
-          mbar_wait(&full[s], (last / kD3Stages) & 1, a.err);
-        }
-      }
-      atomicAdd(a.rows_total, (unsigned long long)pk.rows_done);
-    };
-    {
-      if (split == 0 && lane == 0) {
-        // ---- steady rows first: sinks and local window are fixed since the build (copied before
-        // the wait), appended rows after it
-        ok = ok && pk.push(Ku, Vu, a.n_sink);
-        ok = ok && pk.push(Ku + (size_t)(a.n - a.W) * WI_D, Vu + (size_t)(a.n - a.W) * WI_D, a.W);
-      }
-      pdl_wait();
-      if (split == 0 && lane == 0) {
-        const int amax = a.max_append > 0 ? a.max_append : 1;
-        ok = ok && pk.push(a.appK + (size_t)u * amax * WI_D, a.appV + (size_t)u * amax * WI_D, *a.app_count);
-      }
-      // ---- selected clusters: rows [b_s, b_{s+1}) of the head's row-balanced split
-      // one round trip: the split bounds and the copies of its first 32 runs
-      const int4 sa = a.splits[uh * (nsp + 1) + split];
-      const int4 sb = a.splits[uh * (nsp + 1) + split + 1];
-      const int kk = min(a.selcnt[uh], a.kmax);
-      const int4 r0 = a.sruns[(uh * nsp + split) * 32 + lane];
-      int rows_left = sb.z - sa.z;
-      int pos = max(sa.x, 0), in = sa.y;
-      const int4* runs = a.runs + uh * a.kmax;
-      while (rows_left > 0 && pos < kk) {
-        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-        const int4 rr = (pos + lane < kk) ? (pos == sa.x ? r0 : runs[pos + lane]) : make_int4(0, 0, 0, 0);
-        const int nb = min(32, kk - pos);
-        for (int i = 0; i < nb && rows_left > 0; ++i) {
-          const int o = __shfl_sync(0xffffffffu, rr.x, i);
-          const int z = __shfl_sync(0xffffffffu, rr.y, i);
-          const int take = min(z - in, rows_left);
-          // a run must lie inside the clustered rows; anything else is reported, never copied
-          const bool sane = in >= 0 && in <= z && o >= a.n_sink && (long long)o + z <= a.n - a.W;
-          if (!sane) {
-            if (lane == 0) atomicOr(a.err, WI_DEVERR_BAD_ROW);
-            rows_left = 0;
-            break;
-          }
-          if (lane == 0 && ok && take > 0)
-            ok = pk.push(Ku + (size_t)(o + in) * WI_D, Vu + (size_t)(o + in) * WI_D, take);
-          rows_left -= take;
-          in = 0;
-        }
-        pos += nb;
-      }
-      finish();
+    StagePacker pk{st, full, empty, nrows, a.err};
+    const int amax = a.max_append > 0 ? a.max_append : 1;
+    if (split == 0) {
+      // ---- steady rows first: sinks and local window are fixed since the build (copied before
+      // the wait), appended rows after it
+      const size_t w0 = (size_t)(a.n - a.W) * WI_D;
+      pk.push(lane == 0 ? Ku : Ku + w0, lane == 0 ? Vu : Vu + w0, lane == 0 ? a.n_sink : (lane == 1 ? a.W : 0));
     }
+    pdl_wait();
+    if (split == 0) {
+      const int na = *a.app_count;
+      pk.push(a.appK + (size_t)u * amax * WI_D, a.appV + (size_t)u * amax * WI_D, lane == 0 ? na : 0);
+    }
+    // ---- selected clusters: rows [b_s, b_{s+1}) of the head's row-balanced split, 32 runs per
+    // batch; one round trip gives the split bounds and the copies of its first 32 runs
+    const int4 sa = a.splits[uh * (nsp + 1) + split];
+    const int4 sb = a.splits[uh * (nsp + 1) + split + 1];
+    const int kk = min(a.selcnt[uh], a.kmax);
+    const int4 r0 = a.sruns[(uh * nsp + split) * 32 + lane];
+    int rows_left = sb.z - sa.z;
+    int pos = max(sa.x, 0), in = sa.y;
+    const int4* runs = a.runs + uh * a.kmax;
+    while (rows_left > 0 && pos < kk && pk.ok) {
+      const int4 rr = (pos + lane < kk) ? (pos == sa.x ? r0 : runs[pos + lane]) : make_int4(0, 0, 0, 0);
+      const int i_in = lane == 0 ? in : 0;
+      const bool valid = pos + lane < kk;
+      // a run must lie inside the clustered rows; anything else is reported, never copied
+      const bool sane = !valid || (i_in >= 0 && i_in <= rr.y && rr.x >= a.n_sink && (long long)rr.x + rr.y <= a.n - a.W);
+      if (__any_sync(0xffffffffu, !sane)) {
+        if (lane == 0) atomicOr(a.err, WI_DEVERR_BAD_ROW);
+        break;
+      }
+      const int len = valid ? rr.y - i_in : 0;
+      const int before = warp_inclusive_scan(len) - len;
+      const int take = max(0, min(len, rows_left - before));
+      const size_t r = (size_t)(rr.x + i_in) * WI_D;
+      pk.push(Ku + r, Vu + r, take);
+      rows_left -= __shfl_sync(0xffffffffu, warp_inclusive_scan(take), 31);
+      in = 0;
+      pos += 32;
+    }
+    pk.finish(&flags[0]);
+    if (lane == 0) atomicAdd(a.rows_total, (unsigned long long)pk.fpos);
   } else {
     // ---- consumers
     pdl_wait();
