@@ -530,10 +530,23 @@ static_assert(sizeof(SelSmem) % 16 == 0, "the cached keys follow SelSmem 16-byte
 // the keys (16-byte aligned, when cached), then per 32-id chunk the take bits
 // and their prefix, then per selected position its id, rows, first row in the
 // index and first row among the selected rows.
-__host__ __device__ inline size_t sel_keys_bytes(int C) { return C <= kSelKeysMax ? (size_t)C * 4 : 0; }
+__host__ __device__ inline size_t sel_base_bytes(int C, int kmax) {
+  return sizeof(SelSmem) + ((size_t)C + 31) / 32 * 8 + (size_t)kmax * 16;
+}
+// Row counts and first rows of the selected clusters land, while the top-k runs, in per-cluster
+// slots next to the keys (asynchronous 4-byte copies) when that fits.
+__host__ __device__ inline bool sel_rows_async(int C, int kmax) {
+  return C <= kSelKeysMax && sel_base_bytes(C, kmax) + (size_t)C * 12 <= 200 * 1024;
+}
+__host__ __device__ inline size_t sel_keys_bytes(int C, int kmax) {
+  return C <= kSelKeysMax ? (size_t)C * (sel_rows_async(C, kmax) ? 12 : 4) : 0;
+}
 __host__ __device__ inline size_t sel_smem_bytes(int C, int kmax) {
-  const size_t nch = ((size_t)C + 31) / 32;
-  return sizeof(SelSmem) + sel_keys_bytes(C) + nch * 8 + (size_t)kmax * 16;
+  return sel_base_bytes(C, kmax) + sel_keys_bytes(C, kmax);
+}
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
 // Block-wide search over 2048 ascending bins (thread t < 512 owns bins 4t..4t+3):
@@ -656,7 +669,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   const size_t uh = (size_t)u * a.G + h;
   const int C = a.C, nch = (C + 31) / 32, kmax = a.kmax;
   uint32_t* ks = reinterpret_cast<uint32_t*>(raw + sizeof(SelSmem));                        // [C] if cached
-  uint32_t* tmask = reinterpret_cast<uint32_t*>(raw + sizeof(SelSmem) + sel_keys_bytes(C));  // [nch]
+  uint32_t* tmask = reinterpret_cast<uint32_t*>(raw + sizeof(SelSmem) + sel_keys_bytes(C, kmax));  // [nch]
   int* cpre = reinterpret_cast<int*>(tmask + nch);                                            // [nch]
   int* sel_s = cpre + nch;                                                                    // [kmax] ids
   int* nc_s = sel_s + kmax;                                                                   // [kmax] rows
@@ -666,6 +679,16 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   const int* cn = a.cnt + (size_t)u * C;
   int* out = a.sel + uh * kmax;
   const bool cached = C <= kSelKeysMax;
+  bool rows_async = sel_rows_async(C, kmax);                  // uniform
+  int* nc_a = reinterpret_cast<int*>(ks + C);                 // [C] counts of taken clusters, if rows_async
+  int* of_a = nc_a + C;                                       // [C] their first rows
+  const int* offu = a.off + (size_t)u * (C + 1);
+  auto fetch_rows = [&](int j) {  // start the copies of cluster j's count and first row
+    if (rows_async) {
+      cp_async4(nc_a + j, cn + j);
+      cp_async4(of_a + j, offu + j);
+    }
+  };
   const KeySrc key_of{cached ? ks : nullptr, s};
   int kk = min(kmax, a.nonempty[u]);
   // K0 = the largest key of a non-empty cluster, from k_scores' per-CTA maxima of the same
@@ -747,6 +770,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
       if (k == 0u || d >= dhi && !top_open) continue;
       if (d < dlo) {
         atomicOr(&tmask[j >> 5], 1u << (j & 31));
+        fetch_rows(j);
       } else {
         const int slot = atomicAdd(&sm.s_ncand, 1);
         if (slot < kSelThreads) { sm.ckey[slot] = k; sm.cid[slot] = j; }
@@ -766,10 +790,14 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
           const uint32_t ki = sm.ckey[i];
           rank += (ki > mk || (ki == mk && sm.cid[i] < mi)) ? 1 : 0;
         }
-        if (rank < remaining) atomicOr(&tmask[mi >> 5], 1u << (mi & 31));
+        if (rank < remaining) {
+          atomicOr(&tmask[mi >> 5], 1u << (mi & 31));
+          fetch_rows(mi);
+        }
       }
     } else {
       take_in_bin_radix(key_of, C, K0, bstar, remaining, tmask, sm);
+      rows_async = false;  // uniform: that path sets take bits only
     }
   }
   __syncthreads();
@@ -786,14 +814,15 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
       if (pos < kk) sel_s[pos] = c * 32 + lane;
     }
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");  // this thread's row copies have landed
   __syncthreads();
   // ---- per selected cluster (position p = tid + rounds of kSThreads): rows and their prefix
   int R = 0;
   for (int r0 = 0; r0 < kk; r0 += kSThreads) {  // uniform
     const int p = r0 + tid;
     const int j = p < kk ? sel_s[p] : 0;
-    const int nc = p < kk ? __ldg(cn + j) : 0;
-    const int of = p < kk ? __ldg(a.off + (size_t)u * (C + 1) + j) : 0;
+    const int nc = p < kk ? (rows_async ? nc_a[j] : __ldg(cn + j)) : 0;
+    const int of = p < kk ? (rows_async ? of_a[j] : __ldg(offu + j)) : 0;
     const int inc = warp_inclusive_scan(nc);
     if (lane == 31) sm.s_wt[warp] = inc;
     __syncthreads();
