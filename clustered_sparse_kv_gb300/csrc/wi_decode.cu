@@ -691,6 +691,17 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   };
   const KeySrc key_of{cached ? ks : nullptr, s};
   int kk = min(kmax, a.nonempty[u]);
+  // the first keys' loads are in flight across the K0 reduction and the barrier below
+  const int n4 = C / 4;
+  uint4 f[4];
+  auto load4 = [&](int i0) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = i0 + r * kSThreads;
+      f[r] = i < n4 ? __ldcg(reinterpret_cast<const uint4*>(s) + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  if (cached) load4(tid);
   // K0 = the largest key of a non-empty cluster, from k_scores' per-CTA maxima of the same
   // scores (every warp reduces them itself: no barrier)
   uint32_t K0 = 0u;
@@ -709,16 +720,6 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
     if (k != 0u && (K0 - k >= (1u << 30)) == far) atomicAdd(&sm.hist[0][log_bin(K0 - k)], 1);
   };
   if (cached) {
-    const int n4 = C / 4;
-    uint4 f[4];
-    auto load4 = [&](int i0) {
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int i = i0 + r * kSThreads;
-        f[r] = i < n4 ? __ldcg(reinterpret_cast<const uint4*>(s) + i) : make_uint4(0u, 0u, 0u, 0u);
-      }
-    };
-    load4(tid);       // in flight across the barrier
     __syncthreads();  // the histogram and the masks are zero
     for (int i0 = tid; i0 < n4; i0 += 4 * kSThreads) {
       if (i0 != tid) load4(i0);
