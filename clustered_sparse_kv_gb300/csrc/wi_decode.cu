@@ -527,11 +527,11 @@ struct alignas(16) SelSmem {
 
 static_assert(sizeof(SelSmem) % 16 == 0, "the cached keys follow SelSmem 16-byte aligned");
 // Shared memory of the select role beyond SelSmem (a multiple of 16 bytes):
-// the keys (16-byte aligned, when cached), then per 32-id chunk the take bits
-// and their prefix, then per selected position its id, rows, first row in the
-// index and first row among the selected rows.
+// the keys (16-byte aligned, when cached), then per 32-id chunk the take bits,
+// then per selected position its id, rows, first row in the index and first
+// row among the selected rows.
 __host__ __device__ inline size_t sel_base_bytes(int C, int kmax) {
-  return sizeof(SelSmem) + ((size_t)C + 31) / 32 * 8 + (size_t)kmax * 16;
+  return sizeof(SelSmem) + ((size_t)C + 31) / 32 * 4 + (size_t)kmax * 16;
 }
 // Row counts and first rows of the selected clusters land, while the top-k runs, in per-cluster
 // slots next to the keys (asynchronous 4-byte copies) when that fits.
@@ -582,10 +582,11 @@ __device__ __forceinline__ bool find_bin(const int* hist, int target, SelSmem& s
   return true;
 }
 
-// Exclusive prefix over 32-id chunks of the number of set take bits:
-// pre[c] = sum of popc(tm[c']) for c' < c (each thread sums a contiguous run);
-// returns the total.  Ends with a barrier.
-__device__ __forceinline__ int block_popc_scan(const uint32_t* tm, int* pre, int n, SelSmem& sm) {
+// The ids of the set take bits in ascending order: each thread owns a contiguous
+// run of 32-id chunks, an exclusive prefix of their popcounts gives the position
+// of its first id, and it writes its ids to sel[pos] for pos < min(limit, total).
+// Returns the total number of set bits.
+__device__ __forceinline__ int block_list_taken(const uint32_t* tm, int n, int* sel, int limit, SelSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (n + kSThreads - 1) / kSThreads;
   const int b0 = min(n, tid * per), b1 = min(n, b0 + per);
@@ -601,12 +602,12 @@ __device__ __forceinline__ int block_popc_scan(const uint32_t* tm, int* pre, int
     before += __shfl_xor_sync(0xffffffffu, before, o);
     total += __shfl_xor_sync(0xffffffffu, total, o);
   }
-  int run = before + inc - sum;
+  const int lim = min(limit, total);
+  int pos = before + inc - sum;
   for (int i = b0; i < b1; ++i) {
-    pre[i] = run;
-    run += __popc(tm[i]);
+    for (uint32_t m = tm[i]; m != 0u; m &= m - 1u, ++pos)
+      if (pos < lim) sel[pos] = i * 32 + __ffs(m) - 1;
   }
-  __syncthreads();
   return total;
 }
 
@@ -670,8 +671,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   const int C = a.C, nch = (C + 31) / 32, kmax = a.kmax;
   uint32_t* ks = reinterpret_cast<uint32_t*>(raw + sizeof(SelSmem));                        // [C] if cached
   uint32_t* tmask = reinterpret_cast<uint32_t*>(raw + sizeof(SelSmem) + sel_keys_bytes(C, kmax));  // [nch]
-  int* cpre = reinterpret_cast<int*>(tmask + nch);                                            // [nch]
-  int* sel_s = cpre + nch;                                                                    // [kmax] ids
+  int* sel_s = reinterpret_cast<int*>(tmask + nch);                                           // [kmax] ids
   int* nc_s = sel_s + kmax;                                                                   // [kmax] rows
   int* of_s = nc_s + kmax;                                                                    // [kmax] first row
   int* rp_s = of_s + kmax;  // [kmax] first row among the selected rows
@@ -803,17 +803,10 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   }
   __syncthreads();
   // ---- the selection in id order
-  const int total = block_popc_scan(tmask, cpre, nch, sm);
+  const int total = block_list_taken(tmask, nch, sel_s, kk, sm);
   if (total != kk) {  // uniform; cannot happen with consistent counts
     if (tid == 0) atomicOr(a.err, WI_DEVERR_TOPK);
-    kk = min(kk, total);  // every position below kk gets an id
-  }
-  for (int c = warp; c < nch; c += kSNW) {
-    const unsigned m = tmask[c];
-    if (m & (1u << lane)) {
-      const int pos = cpre[c] + __popc(m & ((1u << lane) - 1u));
-      if (pos < kk) sel_s[pos] = c * 32 + lane;
-    }
+    kk = min(kk, total);  // every position below kk got an id
   }
   asm volatile("cp.async.wait_all;" ::: "memory");  // this thread's row copies have landed
   __syncthreads();
