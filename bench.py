@@ -461,7 +461,8 @@ def main():
                        "k": replicas[0].k_max, "steady": w.n_sink + w.local_window,
                        "l2": f"inputs larger than L2: {R} rotating index+KV replicas "
                              f"({R * (w.units * w.n_ctx * 512 + bytes_d1) / 1e9:.1f} GB)",
-                       "timing": f"CUDA graphs of {L} steps replayed; events on the launching stream"},
+                       "timing": f"CUDA graphs of {L} steps replayed; events on the launching stream",
+                       "decode_layout": wi.wi_decode_layout(replicas[0].handle)},
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_kind": peak_kind,
                          "bytes_per_launch": cand[dom], "traffic": NCU_TRAFFIC.get((w.name, dom))},

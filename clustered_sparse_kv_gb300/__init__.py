@@ -56,6 +56,7 @@ _SIGS = {
     "wi_decode_step_host": [_vp, _vp, _vp, _vp, _vp, _vp],
     "wi_last_selection": [_vp, _vp, _vp, _vp],
     "wi_index_shape": [_vp, _ip, _ip, _ip, _ip, _ip],
+    "wi_decode_layout": [_vp, _ip, _ip, _ip],
     "wi_kmeans_step": [_cfgp, _vp, _vp, _vp, _vp, _vp],
     "wi_kmeans_step_noalloc": [_cfgp, _vp, _vp, _vp, _vp, _vp],
     "wi_check_device": [_vp],
@@ -157,6 +158,12 @@ def wi_index_shape(ix: int) -> dict:
     vals = [ctypes.c_int() for _ in range(5)]
     _check(lib.wi_index_shape(ix, *[ctypes.byref(x) for x in vals]))
     return dict(zip(["units", "clusters", "k_max", "group", "appended"], [x.value for x in vals]))
+
+
+def wi_decode_layout(ix: int) -> dict:
+    vals = [ctypes.c_int() for _ in range(3)]
+    _check(lib.wi_decode_layout(ix, *[ctypes.byref(x) for x in vals]))
+    return dict(zip(["score_ctas", "estimate_ctas", "exact_splits"], [x.value for x in vals]))
 
 
 def wi_kmeans_step(cfg: wi_config, k, centroids, assign, new_centroids, stream=None):

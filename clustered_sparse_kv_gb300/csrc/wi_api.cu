@@ -202,7 +202,6 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   if (ns < 1) ns = 1;
   b.nsplit = ns;
   A(b.scores, U * G * C * 4);
-  A(b.ghist, U * G * 2048 * 4);
   A(b.part1, U * G * (size_t)b.p_es * WI_PART * 4);
   A(b.sel, U * G * (size_t)g.kmax * 4);
   A(b.selcnt, U * G * 4);
@@ -237,7 +236,6 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   WI_CUDA(cudaMemsetAsync(ix->err, 0, 4, st));
   WI_CUDA(cudaMemsetAsync(b.selcnt, 0, U * G * 4, st));
   WI_CUDA(cudaMemsetAsync(b.ticket, 0, U * G * 4, st));
-  WI_CUDA(cudaMemsetAsync(b.ghist, 0, U * G * 2048 * 4, st));
 
   WI_CUDA(cudaMemsetAsync(b.rows_total, 0, 8, st));
   return WI_OK;
@@ -533,6 +531,15 @@ int wi_index_shape(const wi_index* ix, int* units, int* clusters, int* k_max, in
   if (k_max) *k_max = ix->g.kmax;
   if (group) *group = ix->g.G;
   if (appended) *appended = ix->appended;
+  return WI_OK;
+}
+
+int wi_decode_layout(const wi_index* ix, int* score_ctas, int* estimate_ctas, int* exact_splits) {
+  g_err[0] = 0;
+  if (!ix) return fail(WI_EINVAL, "index is NULL");
+  if (score_ctas) *score_ctas = ix->b.p1;
+  if (estimate_ctas) *estimate_ctas = ix->b.p_es;
+  if (exact_splits) *exact_splits = ix->b.nsplit;
   return WI_OK;
 }
 

@@ -61,7 +61,6 @@ struct WiDecodeBufs {
   void* appV;
   int* app_count;
   float* scores;          // [U][G][C] order-preserving score keys (uint32; 0 = empty cluster)
-  int* ghist;             // [U][G][2048] first radix digit of the score keys (built by k_scores)
   float* part1;           // [U][G][p_es][WI_PART]  estimation partials
   int* sel;               // [U][G][kmax]
   int* selcnt;            // [U][G]

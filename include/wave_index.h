@@ -147,6 +147,17 @@ int wi_last_selection(const wi_index* ix, int32_t* ids, int32_t* counts, void* s
 int wi_index_shape(const wi_index* ix, int* units, int* clusters, int* k_max, int* group, int* appended);
 
 /*
+ * Launch layout of this index's decode kernels, fixed when the index is made
+ * from the device's SM count: scores CTAs per unit, estimation CTAs per unit,
+ * and exact-attention splits per head over the selected rows (one more CTA
+ * takes the steady rows).  The environment variables WI_D1_CTAS_PER_UNIT,
+ * WI_ESTIMATE_CTAS_PER_UNIT and WI_D3_SPLITS (positive integers), read when
+ * the index is made, override the defaults.  Results do not depend on the
+ * layout beyond float rounding order.  Any output pointer may be NULL.
+ */
+int wi_decode_layout(const wi_index* ix, int* score_ctas, int* estimate_ctas, int* exact_splits);
+
+/*
  * One spherical k-means round on every segment, for per-round checking:
  * assignment of each clustered token against `centroids` (device bf16
  * [units][n_segments][clusters_per_seg][128]) written to assign (device int32

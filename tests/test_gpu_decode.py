@@ -235,3 +235,27 @@ def test_graph_replay_matches_direct(wi):
         torch.cuda.synchronize()
         assert torch.equal(got, direct)
     ix.free()
+
+
+
+@pytest.mark.parametrize("splits", [1, 5, 12])
+def test_exact_split_counts(wi, monkeypatch, splits):
+    """The exact-attention rows cut into 1, 5 or 12 row-balanced splits per head (plus the steady
+    CTA) give the oracle's output; the layout query reports the count in use."""
+    w = small(batch=2, n_q_heads=8, n_kv_heads=2, n_ctx=4096, seg_len=1024, clusters_per_seg=64, iters=2,
+              budget_k=12, seed=5)
+    k, v, q, K, V, Q = gen(w)
+    p = params_of(w)
+    idx = oracle.build_index(K, V, p)
+    monkeypatch.setenv("WI_D3_SPLITS", str(splits))
+    ix = wi.WaveIndex.adopt(wi.config_from_workload(w), dev16(k), dev16(v), *index_arrays(idx))
+    assert wi.wi_decode_layout(ix.handle)["exact_splits"] == splits
+    for t in range(2):
+        qb = kvsynth.queries(w, step=t)
+        out = ix.decode(dev16(qb)).cpu().numpy()
+        ix.check()
+        Qt = oracle.bf16_from_bits(qb).reshape(w.units, w.group, 128)
+        ref = oracle.decode(Qt, K, V, idx, p, w.group)
+        err = rel_l2(out.reshape(w.units, w.group, 128).astype(np.float64), ref)
+        assert err.max() <= OUT_REL_L2, (t, err.max())
+    ix.free()
