@@ -18,6 +18,10 @@ Parity status per function (what pins it is in ``tests/test_oracle_pins.py``):
                               singleton clusters exact; Jensen bound; cosh
                               closed form; explicit per-token loop)
   lse_merge           pinned (associativity against the single sum)
+  full_attention      pinned (equals decode_unit with every cluster
+                              retrieved; one row gives its value row;
+                              identical keys give the mean value row;
+                              row-order invariance)
 Approximation quality against full attention on synthetic data: parity
 unpinned (the summaries claim accuracy only on RULER / Needle-in-a-Haystack
 with trained models).
@@ -39,4 +43,5 @@ from .wave_index import (  # noqa: F401
     lse_merge,
     decode_unit,
     decode,
+    full_attention,
 )

@@ -292,3 +292,28 @@ def decode(Q: np.ndarray, K: np.ndarray, V: np.ndarray, indexes: list, p: IndexP
             outs.append(r)
     o = np.stack(outs)
     return (o, infos) if details else o
+
+
+# ------------------------------------------------------ full attention ----
+
+def full_attention(Q: np.ndarray, K: np.ndarray, V: np.ndarray, k_app=None, v_app=None) -> np.ndarray:
+    """Full (dense) attention, the baseline the summaries measure the wave index against
+    (de/fr/zh 2.A: the tripartite approximation stands in for attention over every cached
+    token; zh section 3 reports the speed-up over it).
+
+    For every unit u and query head h: softmax(q K^T / sqrt(d)) V over all n context rows of
+    the unit followed by its appended rows, in float64.  Q [units][g][d]; K, V [units][n][d];
+    appended rows [units][t][d] or None.  Returns [units][g][d]."""
+    U, n, d = K.shape
+    scale = 1.0 / math.sqrt(d)
+    out = np.zeros((U, Q.shape[1], d))
+    for u in range(U):
+        Ku, Vu = K[u], V[u]
+        if k_app is not None and k_app.shape[1] > 0:
+            Ku = np.concatenate([Ku, k_app[u]])
+            Vu = np.concatenate([Vu, v_app[u]])
+        for h in range(Q.shape[1]):
+            logits = (Ku @ Q[u, h]) * scale
+            w = np.exp(logits - logits.max())
+            out[u, h] = (w @ Vu) / w.sum()
+    return out

@@ -363,3 +363,37 @@ def test_steady_zone_partition():
     assert s.size == 68 and i.size == n - 68
     assert np.intersect1d(s, i).size == 0
     np.testing.assert_array_equal(np.sort(np.concatenate([s, i])), np.arange(n))
+
+
+# ------------------------------------------------- full-attention oracle ----
+
+def test_full_attention_equals_wave_index_with_every_cluster_retrieved():
+    """The comparator's oracle against the (separately pinned) tripartite decode with a budget
+    above the cluster count, appended tokens included: two different computations of one value."""
+    w = tiny_workload(n=512, S=128, Cs=8, g=4, budget_k=10 ** 6)
+    K, V, Q = gen_unit(w)
+    ka, va = kvsynth.kv_cache(w, p0=512, p1=515)
+    KA = oracle.bf16_from_bits(ka).reshape(1, 3, D)
+    VA = oracle.bf16_from_bits(va).reshape(1, 3, D)
+    p = params_of(w)
+    idx = oracle.build_index(K, V, p)
+    wave = oracle.decode(Q, K, V, idx, p, 4, k_app=KA, v_app=VA)
+    np.testing.assert_allclose(oracle.full_attention(Q, K, V, KA, VA), wave, rtol=0, atol=1e-12)
+
+
+def test_full_attention_closed_forms():
+    rng = np.random.default_rng(3)
+    V = rng.standard_normal((1, 40, D))
+    Q = rng.standard_normal((1, 2, D))
+    # one row: the weights are {1}, the output is that value row
+    np.testing.assert_allclose(oracle.full_attention(Q, rng.standard_normal((1, 1, D)), V[:, :1]),
+                               np.repeat(V[:, :1], 2, axis=1), rtol=0, atol=1e-15)
+    # identical keys: uniform weights, the output is the mean value row
+    Kc = np.repeat(rng.standard_normal((1, 1, D)), 40, axis=1)
+    np.testing.assert_allclose(oracle.full_attention(Q, Kc, V), np.repeat(V.mean(axis=1, keepdims=True), 2, axis=1),
+                               rtol=0, atol=1e-13)
+    # attention is a set function of the (key, value) rows: any row order gives the same output
+    K = rng.standard_normal((1, 40, D))
+    perm = rng.permutation(40)
+    np.testing.assert_allclose(oracle.full_attention(Q, K[:, perm], V[:, perm]), oracle.full_attention(Q, K, V),
+                               rtol=0, atol=1e-13)
