@@ -233,14 +233,18 @@ def job_value(world, steps, batch, layers, seconds):
     return world * steps * batch * layers / seconds
 
 
-def profile_run(wi, torch, w, dev, steps):
-    """One index of the workload and `steps` decode steps, nothing timed."""
+def profile_run(wi, torch, w, dev, steps, dense=False):
+    """One index of the workload and `steps` decode steps (each followed by a dense comparator step
+    if asked), nothing timed."""
     k, v = kvsynth.kv_cache(w)
     kd = torch.from_numpy(k.view(np.int16)).to(dev)
     vd = torch.from_numpy(v.view(np.int16)).to(dev)
     ix = wi.WaveIndex.build(wi.config_from_workload(w), kd, vd)
     for s in range(steps):
-        ix.decode(torch.from_numpy(kvsynth.queries(w, step=s).view(np.int16)).to(dev))
+        q = torch.from_numpy(kvsynth.queries(w, step=s).view(np.int16)).to(dev)
+        ix.decode(q)
+        if dense:
+            ix.dense_decode(q)
     torch.cuda.synchronize()
     ix.check()
     ix.free()
@@ -264,6 +268,10 @@ def main():
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="profiling run: build one index of the workload, run this many decode steps, "
                          "print nothing else (a small case for ncu captures)")
+    ap.add_argument("--profile-dense", action="store_true",
+                    help="with --profile-steps: also run the dense comparator after every decode step")
+    ap.add_argument("--dense-steps", type=int, default=640,
+                    help="dense comparator steps timed after the wave-index region (0: skip)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -292,7 +300,7 @@ def main():
 
     seed = rank_seed(w, rank)
     if args.profile_steps > 0:
-        profile_run(wi, torch, w, dev, args.profile_steps)
+        profile_run(wi, torch, w, dev, args.profile_steps, dense=args.profile_dense)
         return
     k, v = kvsynth.kv_cache(w, seed=seed)
     k_dev = torch.from_numpy(k.view(np.int16)).to(dev)
@@ -445,6 +453,35 @@ def main():
     for ix in replicas:
         ix.check()
 
+    # the dense comparator (full attention over every cached token) on the same replicas and queries:
+    # graphs of L steps, CUDA events on the launching stream, after the wave-index regions
+    dense = None
+    if args.dense_steps > 0:
+        with torch.cuda.stream(stream):
+            for s in range(3):
+                replicas[s % R].dense_decode(qs[s % L], out=outs[s % R], stream=stream)
+            stream.synchronize()
+            gd = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gd, stream=stream):
+                for s in range(L):
+                    replicas[s % R].dense_decode(qs[s], out=outs[s % R], stream=stream)
+            nd = max(1, args.dense_steps // L)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(nd):
+                gd.replay()
+            e1.record(stream)
+        stream.synchronize()
+        for ix in replicas:
+            ix.check()
+        d_ms = max_over_ranks(e0.elapsed_time(e1) / (nd * L), dist, dev)
+        d_bytes = w.units * w.n_ctx * ROW_BYTES + w.units * w.group * 128 * (2 + 4)
+        d_gbs = d_bytes / (d_ms * 1e-3) / 1e9
+        dense = {"kernel": "k_dense_decode", "steps": nd * L, "ms_per_step": d_ms,
+                 "value": job_value(world, 1, w.batch, w.layers, d_ms / 1e3), "unit": UNIT,
+                 "bytes_per_step": d_bytes, "hbm_gbs": d_gbs, "peak": hbm, "frac": d_gbs / hbm,
+                 "peak_kind": peak_kind, "wave_index_speedup": d_ms / ms_per_step}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, k, v)
@@ -480,6 +517,8 @@ def main():
         }
         if build is not None:
             line["build"] = build
+        if dense is not None:
+            line["dense_comparator"] = dense
         print(json.dumps(line), flush=True)
     for ix in replicas:
         ix.free()

@@ -54,6 +54,7 @@ _SIGS = {
     "wi_index_export": [_vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "wi_decode_step": [_vp, _vp, _vp, _vp, _vp, _vp],
     "wi_decode_step_host": [_vp, _vp, _vp, _vp, _vp, _vp],
+    "wi_dense_decode": [_vp, _vp, _vp, _vp],
     "wi_last_selection": [_vp, _vp, _vp, _vp],
     "wi_index_shape": [_vp, _ip, _ip, _ip, _ip, _ip],
     "wi_decode_layout": [_vp, _ip, _ip, _ip],
@@ -145,6 +146,10 @@ def wi_decode_step(ix: int, q, out, k_new=None, v_new=None, stream=None):
     _check(lib.wi_decode_step(ix, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out), _stream(stream)))
 
 
+def wi_dense_decode(ix: int, q, out, stream=None):
+    _check(lib.wi_dense_decode(ix, _ptr(q), _ptr(out), _stream(stream)))
+
+
 def wi_decode_step_host(ix: int, q_host, out_host, k_new_host=None, v_new_host=None, stream=None):
     _check(lib.wi_decode_step_host(ix, _ptr(q_host), _ptr(k_new_host), _ptr(v_new_host), _ptr(out_host),
                                    _stream(stream)))
@@ -232,6 +237,14 @@ class WaveIndex:
             out = torch.empty((self.cfg.batch, self.cfg.layers, self.cfg.n_q_heads, 128), dtype=torch.float32,
                               device=q.device)
         wi_decode_step(self.handle, q, out, k_new, v_new, stream)
+        return out
+
+    def dense_decode(self, q: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+        """Full attention over every cached and appended token (the comparator)."""
+        if out is None:
+            out = torch.empty((self.cfg.batch, self.cfg.layers, self.cfg.n_q_heads, 128), dtype=torch.float32,
+                              device=q.device)
+        wi_dense_decode(self.handle, q, out, stream)
         return out
 
     def export(self, stream=None) -> dict:

@@ -201,6 +201,13 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   if (ns > 64) ns = 64;
   if (ns < 1) ns = 1;
   b.nsplit = ns;
+  // dense comparator: row ranges per unit so that all CTAs fill the SMs once
+  int ds = (int)((wi_dense_ctas_per_sm(G) * (size_t)sms + U - 1) / U);
+  if (ds > 256) ds = 256;
+  if (ds < 1) ds = 1;
+  b.dsplits = ds;
+  A(b.dpart, U * G * (size_t)ds * WI_PART * 4);
+  A(b.dticket, U * 4);
   A(b.scores, U * G * C * 4);
   A(b.part1, U * G * (size_t)b.p_es * WI_PART * 4);
   A(b.sel, U * G * (size_t)g.kmax * 4);
@@ -236,6 +243,7 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   WI_CUDA(cudaMemsetAsync(ix->err, 0, 4, st));
   WI_CUDA(cudaMemsetAsync(b.selcnt, 0, U * G * 4, st));
   WI_CUDA(cudaMemsetAsync(b.ticket, 0, U * G * 4, st));
+  WI_CUDA(cudaMemsetAsync(b.dticket, 0, U * 4, st));
 
   WI_CUDA(cudaMemsetAsync(b.rows_total, 0, 8, st));
   return WI_OK;
@@ -488,6 +496,17 @@ int wi_decode_step(wi_index* ix, const void* q, const void* k_new, const void* v
     if (e != cudaSuccess) return fail(WI_ECUDA, "append launch: %s", cudaGetErrorString(e));
     ix->appended++;
   }
+  return WI_OK;
+}
+
+int wi_dense_decode(wi_index* ix, const void* q, float* out, void* stream) {
+  g_err[0] = 0;
+  if (!ix || !q || !out) return fail(WI_EINVAL, "index, q and out must be non-NULL");
+  if (reinterpret_cast<uintptr_t>(q) & 15) return fail(WI_EINVAL, "q must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ix->last_stream = st;
+  cudaError_t e = wi_launch_dense(ix->g, ix->b, q, out, st);
+  if (e != cudaSuccess) return fail(WI_ECUDA, "dense decode launch: %s", cudaGetErrorString(e));
   return WI_OK;
 }
 

@@ -77,11 +77,18 @@ struct WiDecodeBufs {
   int p1;                 // k_scores CTAs per unit
   int p_es;               // estimation CTAs per unit (= estimation partials per head)
   int nsplit;             // exact_merge CTAs per head over the selected rows (plus one for steady rows)
+  // dense comparator (full attention)
+  float* dpart;           // [U][G][dsplits][WI_PART]  row-range partials
+  unsigned int* dticket;  // [U]
+  int dsplits;            // row ranges (CTAs) per unit
 };
 #define WI_PART 132  // floats per zone partial: m, Z, 2 pad, N[128]
 
 #define WI_DECODE_KERNELS 3  // scores, select_estimate (top-k + estimation CTAs), exact_merge
 #define WI_DECODE_EVENTS 4   // per profiled step: before the first kernel, then after each kernel
+// Full attention over every cached and appended token (the dense comparator).
+cudaError_t wi_launch_dense(const WiGeom& g, const WiDecodeBufs& b, const void* q, float* out, cudaStream_t st);
+int wi_dense_ctas_per_sm(int G);
 cudaError_t wi_launch_decode(const WiGeom& g, const WiDecodeBufs& b, const void* q, float* out, cudaStream_t st,
                              const cudaEvent_t* ev);
 cudaError_t wi_launch_append(const WiGeom& g, const WiDecodeBufs& b, const void* k_new, const void* v_new, int t,

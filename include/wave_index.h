@@ -142,6 +142,20 @@ int wi_decode_step_host(wi_index* ix, const void* q_host, const void* k_new_host
  */
 int wi_last_selection(const wi_index* ix, int32_t* ids, int32_t* counts, void* stream);
 
+/*
+ * Full attention over every token the index holds: the dense comparator that
+ * the wave index approximates (RetroInfer summaries de/fr/zh section 2.A; the
+ * speed-up over it in zh section 3).  For every unit and query head,
+ * out = softmax(q K^T / sqrt(128)) V over the unit's n_ctx context rows and
+ * the tokens appended so far, with no index involved (the context rows are
+ * read in the index's cluster-contiguous order; attention does not depend on
+ * the order).  q: device bf16 [batch][layers][n_q_heads][128]; out: device
+ * fp32, same layout (both caller-owned, q 16-byte aligned).  Uses the index's
+ * own scratch: calls on one index must be ordered (one stream).  Stream-
+ * ordered, asynchronous, no allocation, graph-capturable.  Fp32 accumulation.
+ */
+int wi_dense_decode(wi_index* ix, const void* q, float* out, void* stream);
+
 /* Sizes of an index: units, clusters per unit, k_max (the budget), group g,
  * tokens appended so far (host-side count).  Any output pointer may be NULL. */
 int wi_index_shape(const wi_index* ix, int* units, int* clusters, int* k_max, int* group, int* appended);
