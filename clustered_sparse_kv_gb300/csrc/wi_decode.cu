@@ -763,18 +763,30 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   const uint32_t dlo = bstar >= 0 ? log_bin_start(bstar) : 0u;
   const uint32_t dhi = bstar >= 0 && bstar < kTopkBins - 1 ? log_bin_start(bstar + 1) : 0xffffffffu;
   const bool top_open = bstar == kTopkBins - 1;  // the last bin also holds d = 2^32 - 1
+  auto classify = [&](uint32_t k, int j) -> uint32_t {  // the take bit of j within its chunk, or 0
+    const uint32_t d = K0 - k;
+    if (k == 0u || d >= dhi && !top_open) return 0u;
+    if (d < dlo) {
+      fetch_rows(j);
+      return 1u << (j & 31);
+    }
+    const int slot = atomicAdd(&sm.s_ncand, 1);
+    if (slot < kSelThreads) { sm.ckey[slot] = k; sm.cid[slot] = j; }
+    return 0u;
+  };
   if (bstar >= 0) {
-#pragma unroll 2
-    for (int j = tid; j < C; j += kSThreads) {
-      const uint32_t k = key_of(j);
-      const uint32_t d = K0 - k;
-      if (k == 0u || d >= dhi && !top_open) continue;
-      if (d < dlo) {
-        atomicOr(&tmask[j >> 5], 1u << (j & 31));
-        fetch_rows(j);
-      } else {
-        const int slot = atomicAdd(&sm.s_ncand, 1);
-        if (slot < kSelThreads) { sm.ckey[slot] = k; sm.cid[slot] = j; }
+    if (cached) {  // four cached keys per load; their take bits share one chunk word
+      for (int i = tid; i < C / 4; i += kSThreads) {
+        const uint4 k4 = reinterpret_cast<const uint4*>(ks)[i];
+        const int j = 4 * i;
+        const uint32_t bits = classify(k4.x, j) | classify(k4.y, j + 1) | classify(k4.z, j + 2) |
+                              classify(k4.w, j + 3);
+        if (bits) atomicOr(&tmask[j >> 5], bits);
+      }
+    } else {
+      for (int j = tid; j < C; j += kSThreads) {
+        const uint32_t bits = classify(key_of(j), j);
+        if (bits) atomicOr(&tmask[j >> 5], bits);
       }
     }
   }
