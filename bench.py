@@ -439,7 +439,7 @@ def main():
     qh = [torch.from_numpy(kvsynth.queries(w, step=L + s, seed=seed).view(np.int16)).pin_memory()
           for s in range(8)]
     oh = torch.empty((w.batch, w.layers, w.n_q_heads, 128), dtype=torch.float32).pin_memory()
-    for s in range(3):
+    for s in range(max(3, R)):  # every replica once: its first host-buffer call captures its graph
         wi.wi_decode_step_host(replicas[s % R].handle, qh[s % 8], oh, stream=stream)
     E = max(1, min(args.e2e_steps, K))
     barrier()

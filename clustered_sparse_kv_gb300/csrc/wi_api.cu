@@ -67,6 +67,14 @@ struct wi_index {
   void* kn_dev = nullptr;
   void* vn_dev = nullptr;
   float* out_dev = nullptr;
+  // ... and, for steps without append from pinned host buffers, the copy-in, the decode chain and
+  // the copy-out as one CUDA graph (captured on first use; the copies' host addresses are set at
+  // every launch)
+  cudaStream_t cap_stream = nullptr;
+  cudaGraph_t host_graph = nullptr;
+  cudaGraphExec_t host_exec = nullptr;
+  cudaGraphNode_t host_in = nullptr, host_out = nullptr;
+  bool host_graph_off = false;  // capture failed once: direct launches from then on
   cudaStream_t last_stream = nullptr;
   std::vector<void*> allocs;
   // build timing: events around the whole build and around every assignment launch
@@ -154,6 +162,9 @@ int alloc(wi_index* ix, void** p, size_t bytes) {
 
 void destroy(wi_index* ix) {
   if (!ix) return;
+  if (ix->host_exec) cudaGraphExecDestroy(ix->host_exec);
+  if (ix->host_graph) cudaGraphDestroy(ix->host_graph);
+  if (ix->cap_stream) cudaStreamDestroy(ix->cap_stream);
   for (cudaEvent_t e : ix->prof_ev) cudaEventDestroy(e);
   for (cudaEvent_t e : ix->build_ev) cudaEventDestroy(e);
   for (void* p : ix->allocs) cudaFree(p);
@@ -510,6 +521,55 @@ int wi_dense_decode(wi_index* ix, const void* q, float* out, void* stream) {
   return WI_OK;
 }
 
+static bool is_pinned(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost;
+}
+
+// Capture the host-buffer step (copy-in, decode chain, copy-out) as a graph; false if the
+// runtime refuses (the caller then launches directly).
+static bool capture_host_graph(wi_index* ix, const void* q_host, float* out_host, size_t qb, size_t ob) {
+  if (!ix->cap_stream && cudaStreamCreateWithFlags(&ix->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
+    return false;
+  cudaStream_t cs = ix->cap_stream;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) return false;
+  bool ok = cudaMemcpyAsync(ix->q_dev, q_host, qb, cudaMemcpyHostToDevice, cs) == cudaSuccess &&
+            wi_launch_decode(ix->g, ix->b, ix->q_dev, ix->out_dev, cs, nullptr) == cudaSuccess &&
+            cudaMemcpyAsync(out_host, ix->out_dev, ob, cudaMemcpyDeviceToHost, cs) == cudaSuccess;
+  cudaGraph_t graph = nullptr;
+  ok = cudaStreamEndCapture(cs, &graph) == cudaSuccess && ok && graph;
+  if (!ok) {
+    if (graph) cudaGraphDestroy(graph);
+    return false;
+  }
+  // the two copy nodes: the one into the query staging buffer and the one out of the output staging
+  size_t n = 0;
+  cudaGraphGetNodes(graph, nullptr, &n);
+  std::vector<cudaGraphNode_t> nodes(n);
+  cudaGraphGetNodes(graph, nodes.data(), &n);
+  for (cudaGraphNode_t nd : nodes) {
+    cudaGraphNodeType ty;
+    if (cudaGraphNodeGetType(nd, &ty) != cudaSuccess || ty != cudaGraphNodeTypeMemcpy) continue;
+    cudaMemcpy3DParms pm{};
+    if (cudaGraphMemcpyNodeGetParams(nd, &pm) != cudaSuccess) continue;
+    if (pm.dstPtr.ptr == ix->q_dev) ix->host_in = nd;
+    if (pm.srcPtr.ptr == ix->out_dev) ix->host_out = nd;
+  }
+  cudaGraphExec_t exec = nullptr;
+  if (!ix->host_in || !ix->host_out || cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    ix->host_in = ix->host_out = nullptr;
+    return false;
+  }
+  ix->host_graph = graph;
+  ix->host_exec = exec;
+  return true;
+}
+
 int wi_decode_step_host(wi_index* ix, const void* q_host, const void* k_new_host, const void* v_new_host,
                         float* out_host, void* stream) {
   g_err[0] = 0;
@@ -519,6 +579,22 @@ int wi_decode_step_host(wi_index* ix, const void* q_host, const void* k_new_host
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const WiGeom& g = ix->g;
   const size_t qb = (size_t)g.U * g.G * 128 * 2, kb = (size_t)g.U * 128 * 2, ob = (size_t)g.U * g.G * 128 * 4;
+  if (!k_new_host && ix->prof_slots == 0 && !ix->host_graph_off && is_pinned(q_host) && is_pinned(out_host)) {
+    if (!ix->host_exec && !capture_host_graph(ix, q_host, out_host, qb, ob)) {
+      cudaGetLastError();
+      ix->host_graph_off = true;
+    }
+    if (ix->host_exec) {
+      ix->last_stream = st;
+      WI_CUDA(cudaGraphExecMemcpyNodeSetParams1D(ix->host_exec, ix->host_in, ix->q_dev, q_host, qb,
+                                                 cudaMemcpyHostToDevice));
+      WI_CUDA(cudaGraphExecMemcpyNodeSetParams1D(ix->host_exec, ix->host_out, out_host, ix->out_dev, ob,
+                                                 cudaMemcpyDeviceToHost));
+      WI_CUDA(cudaGraphLaunch(ix->host_exec, st));
+      WI_CUDA(cudaStreamSynchronize(st));
+      return WI_OK;
+    }
+  }
   WI_CUDA(cudaMemcpyAsync(ix->q_dev, q_host, qb, cudaMemcpyHostToDevice, st));
   if (k_new_host) {
     WI_CUDA(cudaMemcpyAsync(ix->kn_dev, k_new_host, kb, cudaMemcpyHostToDevice, st));

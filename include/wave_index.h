@@ -130,7 +130,12 @@ int wi_decode_step(wi_index* ix, const void* q, const void* k_new, const void* v
  * wi_decode_step with HOST q / k_new / v_new / out: copies the inputs to the
  * device, runs the step, copies the output back and synchronises `stream`
  * before returning (out is valid on return).  Pinned host memory makes the
- * copies asynchronous DMA; pageable memory works but is slower.
+ * copies asynchronous DMA; pageable memory works but is slower.  A step with
+ * pinned q and out, no append and decode profiling off runs as one CUDA graph
+ * (copy-in, the decode kernels, copy-out) that the index captures on its
+ * first such call (the index then owns a stream and the graph until
+ * wi_free) and relaunches with the call's host addresses; other steps are
+ * launched directly.  Results are identical either way.
  */
 int wi_decode_step_host(wi_index* ix, const void* q_host, const void* k_new_host, const void* v_new_host,
                         float* out_host, void* stream);

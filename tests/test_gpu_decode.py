@@ -204,8 +204,20 @@ def test_host_buffer_variant_matches(wi):
     ref = ix.decode(dev16(q)).cpu()
     qh = torch.from_numpy(q.view(np.int16)).pin_memory()
     oh = torch.empty((1, 1, 4, 128), dtype=torch.float32).pin_memory()
-    wi.wi_decode_step_host(ix.handle, qh, oh)
+    wi.wi_decode_step_host(ix.handle, qh, oh)  # pinned buffers: the captured graph
     assert torch.equal(oh, ref)
+    # other pinned buffers and other queries through the same graph (its copy addresses are reset
+    # at every call), and pageable buffers (direct launches)
+    for t in (1, 2):
+        qt = kvsynth.queries(w, step=t)
+        want = ix.decode(dev16(qt)).cpu()
+        qh2 = torch.from_numpy(qt.view(np.int16).copy()).pin_memory()
+        oh2 = torch.full((1, 1, 4, 128), float("nan"), dtype=torch.float32).pin_memory()
+        wi.wi_decode_step_host(ix.handle, qh2, oh2)
+        assert torch.equal(oh2, want)
+        oh3 = torch.full((1, 1, 4, 128), float("nan"), dtype=torch.float32)
+        wi.wi_decode_step_host(ix.handle, torch.from_numpy(qt.view(np.int16).copy()), oh3)
+        assert torch.equal(oh3, want)
     ix.free()
 
 
