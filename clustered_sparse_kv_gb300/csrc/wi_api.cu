@@ -68,13 +68,14 @@ struct wi_index {
   void* vn_dev = nullptr;
   float* out_dev = nullptr;
   // ... and, for steps without append from pinned host buffers, the copy-in, the decode chain and
-  // the copy-out as one CUDA graph (captured on first use; the copies' host addresses are set at
-  // every launch)
+  // the copy-out as one CUDA graph (captured on first use with those buffers)
   cudaStream_t cap_stream = nullptr;
   cudaGraph_t host_graph = nullptr;
   cudaGraphExec_t host_exec = nullptr;
-  cudaGraphNode_t host_in = nullptr, host_out = nullptr;
-  bool host_graph_off = false;  // capture failed once: direct launches from then on
+  const void* host_q = nullptr;  // the mapped host buffers the graph reads and writes
+  void* host_o = nullptr;
+  int host_recaptures = 0;
+  bool host_graph_off = false;  // capture failed, or the buffers keep changing: direct launches
   cudaStream_t last_stream = nullptr;
   std::vector<void*> allocs;
   // build timing: events around the whole build and around every assignment launch
@@ -151,6 +152,11 @@ namespace {
 
 int alloc(wi_index* ix, void** p, size_t bytes) {
   if (bytes == 0) bytes = 16;
+  // fault injection for the error path: WI_FAIL_ALLOC_AT=n makes the n-th device allocation of every
+  // index report out-of-memory (nothing is allocated)
+  const int fail_at = env_int("WI_FAIL_ALLOC_AT", 0);
+  if (fail_at > 0 && ix->allocs.size() + 1 == (size_t)fail_at)
+    return fail(WI_ENOMEM, "device allocation %d refused (WI_FAIL_ALLOC_AT)", fail_at);
   cudaError_t e = cudaMalloc(p, bytes);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -521,52 +527,45 @@ int wi_dense_decode(wi_index* ix, const void* q, float* out, void* stream) {
   return WI_OK;
 }
 
-static bool is_pinned(const void* p) {
+// The device address of page-locked host memory mapped into the device's address space, or null.
+static void* mapped_host(const void* p) {
   cudaPointerAttributes at{};
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
     cudaGetLastError();
-    return false;
+    return nullptr;
   }
-  return at.type == cudaMemoryTypeHost;
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
 }
 
-// Capture the host-buffer step (copy-in, decode chain, copy-out) as a graph; false if the
-// runtime refuses (the caller then launches directly).
-static bool capture_host_graph(wi_index* ix, const void* q_host, float* out_host, size_t qb, size_t ob) {
+static void drop_host_graph(wi_index* ix) {
+  if (ix->host_exec) cudaGraphExecDestroy(ix->host_exec);
+  if (ix->host_graph) cudaGraphDestroy(ix->host_graph);
+  ix->host_exec = nullptr;
+  ix->host_graph = nullptr;
+}
+
+// Capture the host-buffer step as a graph: a copy kernel reads the query from mapped host memory,
+// the decode chain runs, a copy kernel writes the output to mapped host memory (no DMA setup per
+// step).  False if the runtime refuses (the caller then launches directly).
+static bool capture_host_graph(wi_index* ix, const void* qd, void* od, size_t qb, size_t ob) {
   if (!ix->cap_stream && cudaStreamCreateWithFlags(&ix->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
     return false;
   cudaStream_t cs = ix->cap_stream;
   if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) return false;
-  bool ok = cudaMemcpyAsync(ix->q_dev, q_host, qb, cudaMemcpyHostToDevice, cs) == cudaSuccess &&
+  bool ok = wi_launch_copy16(qd, ix->q_dev, qb, cs) == cudaSuccess &&
             wi_launch_decode(ix->g, ix->b, ix->q_dev, ix->out_dev, cs, nullptr) == cudaSuccess &&
-            cudaMemcpyAsync(out_host, ix->out_dev, ob, cudaMemcpyDeviceToHost, cs) == cudaSuccess;
+            wi_launch_copy16(ix->out_dev, od, ob, cs) == cudaSuccess;
   cudaGraph_t graph = nullptr;
   ok = cudaStreamEndCapture(cs, &graph) == cudaSuccess && ok && graph;
-  if (!ok) {
-    if (graph) cudaGraphDestroy(graph);
-    return false;
-  }
-  // the two copy nodes: the one into the query staging buffer and the one out of the output staging
-  size_t n = 0;
-  cudaGraphGetNodes(graph, nullptr, &n);
-  std::vector<cudaGraphNode_t> nodes(n);
-  cudaGraphGetNodes(graph, nodes.data(), &n);
-  for (cudaGraphNode_t nd : nodes) {
-    cudaGraphNodeType ty;
-    if (cudaGraphNodeGetType(nd, &ty) != cudaSuccess || ty != cudaGraphNodeTypeMemcpy) continue;
-    cudaMemcpy3DParms pm{};
-    if (cudaGraphMemcpyNodeGetParams(nd, &pm) != cudaSuccess) continue;
-    if (pm.dstPtr.ptr == ix->q_dev) ix->host_in = nd;
-    if (pm.srcPtr.ptr == ix->out_dev) ix->host_out = nd;
-  }
   cudaGraphExec_t exec = nullptr;
-  if (!ix->host_in || !ix->host_out || cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
-    cudaGraphDestroy(graph);
-    ix->host_in = ix->host_out = nullptr;
+  if (!ok || cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
     return false;
   }
   ix->host_graph = graph;
   ix->host_exec = exec;
+  ix->host_q = qd;
+  ix->host_o = od;
   return true;
 }
 
@@ -579,17 +578,20 @@ int wi_decode_step_host(wi_index* ix, const void* q_host, const void* k_new_host
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const WiGeom& g = ix->g;
   const size_t qb = (size_t)g.U * g.G * 128 * 2, kb = (size_t)g.U * 128 * 2, ob = (size_t)g.U * g.G * 128 * 4;
-  if (!k_new_host && ix->prof_slots == 0 && !ix->host_graph_off && is_pinned(q_host) && is_pinned(out_host)) {
-    if (!ix->host_exec && !capture_host_graph(ix, q_host, out_host, qb, ob)) {
+  void* qd = nullptr;
+  void* od = nullptr;
+  if (!k_new_host && ix->prof_slots == 0 && !ix->host_graph_off && (qd = mapped_host(q_host)) &&
+      (od = mapped_host(out_host)) && ((reinterpret_cast<uintptr_t>(qd) | reinterpret_cast<uintptr_t>(od)) & 15) == 0) {
+    if (ix->host_exec && (ix->host_q != qd || ix->host_o != od)) {  // other buffers: capture again
+      drop_host_graph(ix);
+      if (++ix->host_recaptures > 4) ix->host_graph_off = true;  // buffers keep changing: stop capturing
+    }
+    if (!ix->host_graph_off && !ix->host_exec && !capture_host_graph(ix, qd, od, qb, ob)) {
       cudaGetLastError();
       ix->host_graph_off = true;
     }
-    if (ix->host_exec) {
+    if (ix->host_exec && !ix->host_graph_off) {
       ix->last_stream = st;
-      WI_CUDA(cudaGraphExecMemcpyNodeSetParams1D(ix->host_exec, ix->host_in, ix->q_dev, q_host, qb,
-                                                 cudaMemcpyHostToDevice));
-      WI_CUDA(cudaGraphExecMemcpyNodeSetParams1D(ix->host_exec, ix->host_out, out_host, ix->out_dev, ob,
-                                                 cudaMemcpyDeviceToHost));
       WI_CUDA(cudaGraphLaunch(ix->host_exec, st));
       WI_CUDA(cudaStreamSynchronize(st));
       return WI_OK;

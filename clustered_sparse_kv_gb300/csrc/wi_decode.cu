@@ -1393,6 +1393,13 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
   if (tid == 0) a.ticket[uh] = 0u;  // ready for the next step
 }
 
+// ------------------------------------------------------------- host copy ----
+// 16-byte words from src to dst, either side possibly host memory mapped into the device's
+// address space (the host-buffer step reads its query and writes its output this way).
+__global__ void k_copy16(const uint4* __restrict__ src, uint4* __restrict__ dst, int n16) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += gridDim.x * blockDim.x) dst[i] = src[i];
+}
+
 // ---------------------------------------------------------------- append ----
 __global__ void k_append(const bf16* __restrict__ k_new, const bf16* __restrict__ v_new, bf16* __restrict__ appK,
                          bf16* __restrict__ appV, int* __restrict__ app_count, int t, int max_append) {
@@ -1532,6 +1539,13 @@ cudaError_t wi_launch_decode(const WiGeom& g, const WiDecodeBufs& b, const void*
     case 8: return launch_g<8>(g, b, q, out, st, ev);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t wi_launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t st) {
+  const int n16 = (int)(bytes / 16);
+  const int blocks = (n16 + 255) / 256 < 64 ? (n16 + 255) / 256 : 64;
+  k_copy16<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16);
+  return cudaGetLastError();
 }
 
 cudaError_t wi_launch_append(const WiGeom& g, const WiDecodeBufs& b, const void* k_new, const void* v_new, int t,

@@ -131,11 +131,13 @@ int wi_decode_step(wi_index* ix, const void* q, const void* k_new, const void* v
  * device, runs the step, copies the output back and synchronises `stream`
  * before returning (out is valid on return).  Pinned host memory makes the
  * copies asynchronous DMA; pageable memory works but is slower.  A step with
- * pinned q and out, no append and decode profiling off runs as one CUDA graph
- * (copy-in, the decode kernels, copy-out) that the index captures on its
- * first such call (the index then owns a stream and the graph until
- * wi_free) and relaunches with the call's host addresses; other steps are
- * launched directly.  Results are identical either way.
+ * pinned (device-mapped, 16-byte aligned) q and out, no append and decode
+ * profiling off runs as one CUDA graph that the index captures for that pair
+ * of buffers: a copy kernel reads q from host memory, the decode kernels run,
+ * a copy kernel writes out to host memory.  The index owns a stream and the
+ * graph until wi_free; a call with other buffers captures again, and after a
+ * few such changes the index launches directly, as it does for every other
+ * step.  Results are identical either way.
  */
 int wi_decode_step_host(wi_index* ix, const void* q_host, const void* k_new_host, const void* v_new_host,
                         float* out_host, void* stream);
@@ -238,6 +240,10 @@ int wi_index_build_stats(wi_index* ix, double* build_ms, double* assign_ms, int*
 /* Synchronise the index's last stream and report a device-side invariant
  * violation recorded by any kernel since the last call (WI_EDEVICE). */
 int wi_check_device(wi_index* ix);
+
+/* Error-path testing: with the environment variable WI_FAIL_ALLOC_AT=n (n >= 1),
+ * the n-th device allocation made for any index fails as out-of-memory; the
+ * call returns WI_ENOMEM having released what it had allocated. */
 
 /* Release the index and everything it owns (not k / v).  NULL is a no-op.
  * Synchronises the device first. */
