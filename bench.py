@@ -40,7 +40,7 @@ import kvsynth  # noqa: E402
 METRIC = "wave-index decode steps/s (batch×layer) at 128K–1M; HBM GB/s vs peak"
 UNIT = "steps/s"
 WORKLOAD = "llama3-8b-131k"
-INDEX_BYTES_PER_CLUSTER = 128 * 2 + 128 * 4 + 4   # mu bf16 + valsum fp32 + count
+INDEX_BYTES_PER_CLUSTER = 128 * 2 + 128 * 4 + 4   # mu bf16 + valsum fp32 + count (bf16 variant: 128 * 2)
 ROW_BYTES = 128 * 2 * 2                           # one K row + one V row (bf16)
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -270,6 +270,8 @@ def main():
                          "print nothing else (a small case for ncu captures)")
     ap.add_argument("--profile-dense", action="store_true",
                     help="with --profile-steps: also run the dense comparator after every decode step")
+    ap.add_argument("--valsum-bf16", action="store_true",
+                    help="the index variant whose decode reads a bf16 copy of the value sums")
     ap.add_argument("--dense-steps", type=int, default=640,
                     help="dense comparator steps timed after the wave-index region (0: skip)")
     args = ap.parse_args()
@@ -306,6 +308,8 @@ def main():
     k_dev = torch.from_numpy(k.view(np.int16)).to(dev)
     v_dev = torch.from_numpy(v.view(np.int16)).to(dev)
     cfg = wi.config_from_workload(w)
+    cfg.valsum_bf16 = 1 if args.valsum_bf16 else 0
+    vs_bytes = 2 if args.valsum_bf16 else 4
     R = args.replicas
     stream = torch.cuda.Stream(device=dev)
     replicas = []
@@ -422,10 +426,10 @@ def main():
             union += int(counts[uu][np.unique(np.concatenate(per_head))].sum()) + steady
     dedup = union / max(loaded, 1)
     hbm, tf_burst, tf_sust, peak_kind = peaks()
-    bytes_d1 = w.units * w.clusters * INDEX_BYTES_PER_CLUSTER
+    bytes_d1 = w.units * w.clusters * (INDEX_BYTES_PER_CLUSTER - 128 * (4 - vs_bytes))
     bytes_d3 = rows_per_step * dedup * ROW_BYTES
     cand = {"scores": w.units * w.clusters * (128 * 2 + 4),              # mu + count
-            "select_estimate": w.units * w.clusters * (128 * 4 + 4),     # value sums + count
+            "select_estimate": w.units * w.clusters * (128 * vs_bytes + 4),  # value sums + count
             "exact_merge": bytes_d3}
     dom = max(cand, key=lambda n: mean_us[n])
     achieved = cand[dom] / (mean_us[dom] * 1e-6) / 1e9 if mean_us[dom] > 0 else 0.0
@@ -502,7 +506,8 @@ def main():
                        "l2": f"inputs larger than L2: {R} rotating index+KV replicas "
                              f"({R * (w.units * w.n_ctx * 512 + bytes_d1) / 1e9:.1f} GB)",
                        "timing": f"CUDA graphs of {L} steps replayed; events on the launching stream",
-                       "decode_layout": wi.wi_decode_layout(replicas[0].handle)},
+                       "decode_layout": wi.wi_decode_layout(replicas[0].handle),
+                       "valsum": "bf16" if args.valsum_bf16 else "fp32"},
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_kind": peak_kind,
                          "bytes_per_launch": cand[dom], "traffic": NCU_TRAFFIC.get((w.name, dom))},

@@ -41,7 +41,8 @@ class wi_config(ctypes.Structure):
         ("seg_len", ctypes.c_int), ("clusters_per_seg", ctypes.c_int), ("iters", ctypes.c_int),
         ("n_sink", ctypes.c_int), ("local_window", ctypes.c_int), ("max_append", ctypes.c_int),
         ("budget_frac", ctypes.c_double), ("budget_k", ctypes.c_int),
-        ("reserved", ctypes.c_int * 3),
+        ("valsum_bf16", ctypes.c_int),
+        ("reserved", ctypes.c_int * 2),
     ]
 
 
@@ -105,12 +106,14 @@ def _stream(stream):
 
 
 def make_config(batch, layers, n_q_heads, n_kv_heads, n_ctx, seg_len=8192, clusters_per_seg=512, iters=10,
-                n_sink=4, local_window=64, max_append=0, budget_frac=0.018, budget_k=0, head_dim=128) -> wi_config:
+                n_sink=4, local_window=64, max_append=0, budget_frac=0.018, budget_k=0, head_dim=128,
+                valsum_bf16=0) -> wi_config:
     c = wi_config()
     c.batch, c.layers, c.n_q_heads, c.n_kv_heads, c.head_dim = batch, layers, n_q_heads, n_kv_heads, head_dim
     c.n_ctx, c.seg_len, c.clusters_per_seg, c.iters = n_ctx, seg_len, clusters_per_seg, iters
     c.n_sink, c.local_window, c.max_append = n_sink, local_window, max_append
     c.budget_frac, c.budget_k = budget_frac, budget_k
+    c.valsum_bf16 = valsum_bf16
     return c
 
 

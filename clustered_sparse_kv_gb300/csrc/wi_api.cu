@@ -51,6 +51,7 @@ struct wi_index {
   // index
   void* mu = nullptr;
   float* valsum = nullptr;
+  void* valsum16 = nullptr;  // bf16 copy read by decode when the config asks for it
   int* cnt = nullptr;
   int* off = nullptr;
   int* perm = nullptr;
@@ -110,8 +111,10 @@ int wi_geom_from_config(const wi_config* c, WiGeom* g, char* msg, size_t msglen)
     BAD("need 1 <= n_sink + local_window < n_ctx");
   if (c->max_append < 0) BAD("max_append must be >= 0");
   if (c->n_ctx + c->max_append >= (1LL << 24)) BAD("n_ctx + max_append must be < 2^24");
-  for (int i = 0; i < 3; ++i)
+  if (c->valsum_bf16 != 0 && c->valsum_bf16 != 1) BAD("valsum_bf16 must be 0 or 1");
+  for (int i = 0; i < 2; ++i)
     if (c->reserved[i]) BAD("reserved fields must be zero");
+  g->vs16 = c->valsum_bf16;
   g->U = c->batch * c->layers * c->n_kv_heads;
   g->G = c->n_q_heads / c->n_kv_heads;
   g->S = c->seg_len;
@@ -186,6 +189,7 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   if ((rc = alloc(ix, reinterpret_cast<void**>(&(ptr)), (bytes))) != WI_OK) return rc
   A(ix->mu, U * C * 128 * 2);
   A(ix->valsum, U * C * 128 * 4);
+  if (g.vs16) A(ix->valsum16, U * C * 128 * 2);
   A(ix->cnt, U * C * 4);
   A(ix->off, U * (C + 1) * 4);
   A(ix->perm, U * (size_t)g.n_idx * 4);
@@ -247,6 +251,7 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
     return fail(WI_EUNSUPPORTED, "could not encode the tensor map of the centroid table");
   b.mu = ix->mu;
   b.valsum = ix->valsum;
+  b.valsum16 = ix->valsum16;
   b.cnt = ix->cnt;
   b.off = ix->off;
   b.nonempty = ix->nonempty;
@@ -399,6 +404,7 @@ int wi_build_index(const wi_config* cfg, void* k, void* v, const void* init_cent
   }
   WI_LAUNCH(wi_launch_final_reduce(g, k, v, s.seg_counts, s.seg_offsets, s.slots, ix->mu, ix->valsum, ix->cnt,
                                    ix->off, ix->perm, ix->nonempty, st));
+  if (g.vs16) WI_LAUNCH(wi_launch_to_bf16(ix->valsum, ix->valsum16, (long long)g.U * g.C * 128, st));
   scratch_free(&s, st);
   s = BuildScratch();
   if ((rc = permute_kv(ix, st)) != WI_OK) goto done;
@@ -465,6 +471,7 @@ int wi_index_import(const wi_config* cfg, void* k, void* v, const int32_t* count
   WI_LAUNCH(cudaMemcpyAsync(ix->nonempty, hne.data(), hne.size() * 4, cudaMemcpyHostToDevice, st));
   WI_LAUNCH(cudaMemcpyAsync(ix->mu, mu, U * C * 128 * 2, cudaMemcpyDefault, st));
   WI_LAUNCH(cudaMemcpyAsync(ix->valsum, valsum, U * C * 128 * 4, cudaMemcpyDefault, st));
+  if (g.vs16) WI_LAUNCH(wi_launch_to_bf16(ix->valsum, ix->valsum16, (long long)U * C * 128, st));
   if ((rc = permute_kv(ix, st)) != WI_OK) goto done;
   // the host vectors above are pageable: finish the copies before they go away
   WI_LAUNCH(cudaStreamSynchronize(st));

@@ -32,6 +32,15 @@ __device__ __forceinline__ long long seg_slot_base(int s, int S, long long n, in
   return n_sink + a - steady_before;
 }
 
+// Four values per thread (n is a multiple of 128).
+__global__ void k_to_bf16(const float4* __restrict__ in, uint2* __restrict__ out, long long n4) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float4 x = in[i];
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
+  out[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+
 __global__ void k_invnorm(const bf16* __restrict__ K, float* __restrict__ invnorm, long long rows) {
   const int lane = threadIdx.x & 31;
   const long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -331,6 +340,14 @@ __global__ void k_scatter_back(bf16* __restrict__ K, bf16* __restrict__ V, const
 }
 
 }  // namespace
+
+cudaError_t wi_launch_to_bf16(const float* in, void* out, long long n, cudaStream_t st) {
+  const long long n4 = n / 4;
+  if (n4 <= 0) return cudaSuccess;
+  k_to_bf16<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(reinterpret_cast<const float4*>(in),
+                                                           static_cast<uint2*>(out), n4);
+  return cudaGetLastError();
+}
 
 cudaError_t wi_launch_invnorm(const void* K, float* invnorm, long long rows, cudaStream_t st) {
   const long long blocks = (rows + 7) / 8;

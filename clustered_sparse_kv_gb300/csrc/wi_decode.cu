@@ -277,21 +277,25 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
 // range, per head: m = max lam s_hj, Z = sum n_j e^{lam s - m},
 // N = sum e^{lam s - m} valsum_j (online softmax per warp, merged per CTA).
 constexpr int kEsStages = 3;
+template <typename VT>  // value sums: float, or their bf16 copy
 struct EsStage {
-  float vs[kSTile * WI_D];
+  VT vs[kSTile * WI_D];
   int cnt[kSTile];
   uint32_t sc[8][kSTile];  // score keys of up to 8 heads (0: empty cluster)
 };
-constexpr size_t kEsSmem = sizeof(EsStage) * kEsStages + 2 * kEsStages * sizeof(uint64_t) +
-                           sizeof(float) * kSWarps * 2 * 32 + sizeof(float) * kSWarps * 2 * 4 + 16;
+template <typename VT>
+constexpr size_t es_smem() {
+  return sizeof(EsStage<VT>) * kEsStages + 2 * kEsStages * sizeof(uint64_t) + sizeof(float) * kSWarps * 2 * 32 +
+         sizeof(float) * kSWarps * 2 * 4 + 16;
+}
 
-template <int G>
-__device__ void estimate_role(unsigned char* raw, const float* __restrict__ valsum, const int* __restrict__ cnt,
+template <int G, typename VT>
+__device__ void estimate_role(unsigned char* raw, const VT* __restrict__ valsum, const int* __restrict__ cnt,
                               const uint32_t* __restrict__ scores, float* __restrict__ part, int C, int u, int p,
                               int P, float lam, int* err) {
   using HG = HeadGeo<G>;
-  EsStage* st = reinterpret_cast<EsStage*>(raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(raw + sizeof(EsStage) * kEsStages);
+  EsStage<VT>* st = reinterpret_cast<EsStage<VT>*>(raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(raw + sizeof(EsStage<VT>) * kEsStages);
   uint64_t* empty = full + kEsStages;
   float* pbuf = reinterpret_cast<float*>(empty + kEsStages);  // [warps][2][32]
   float* sbuf = pbuf + kSWarps * 2 * 32;                       // [warps][2][4]
@@ -323,9 +327,9 @@ __device__ void estimate_role(unsigned char* raw, const float* __restrict__ vals
       auto issue_index = [&](int it) {
         const int s = it % kEsStages;
         const int j0 = c0 + it * kSTile, nj = min(kSTile, c1 - j0);
-        mbar_arrive_expect_tx(&full[s], (uint32_t)nj * (WI_D * 4 + 4 + 4 * G));
+        mbar_arrive_expect_tx(&full[s], (uint32_t)nj * (WI_D * (uint32_t)sizeof(VT) + 4 + 4 * G));
         const size_t row = (size_t)u * C + j0;
-        bulk_g2s(st[s].vs, valsum + row * WI_D, nj * WI_D * 4, &full[s]);
+        bulk_g2s(st[s].vs, valsum + row * WI_D, nj * WI_D * (uint32_t)sizeof(VT), &full[s]);
         bulk_g2s(st[s].cnt, cnt + row, nj * 4, &full[s]);
       };
       auto issue_scores = [&](int it) {
@@ -356,7 +360,7 @@ __device__ void estimate_role(unsigned char* raw, const float* __restrict__ vals
     for (int it = 0; it < ntile; ++it) {
       const int s = it % kEsStages, r = it / kEsStages;
       if (!mbar_wait(&full[s], r & 1, err)) { *s_abort = 1; break; }
-      const EsStage& T = st[s];
+      const EsStage<VT>& T = st[s];
       const int j0 = c0 + it * kSTile, nj = min(kSTile, c1 - j0);
       const int i0 = warp * 8;
       if (i0 < nj) {
@@ -395,7 +399,14 @@ __device__ void estimate_role(unsigned char* raw, const float* __restrict__ vals
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           if (i0 + i >= nj) break;  // rows past the tile hold stale shared memory
-          const float4 vv = *reinterpret_cast<const float4*>(&T.vs[(i0 + i) * WI_D + 4 * lane]);
+          float4 vv;
+          if constexpr (sizeof(VT) == 4) {
+            vv = *reinterpret_cast<const float4*>(&T.vs[(i0 + i) * WI_D + 4 * lane]);
+          } else {
+            float x[4];
+            unpack_bf16x4(*reinterpret_cast<const uint2*>(&T.vs[(i0 + i) * WI_D + 4 * lane]), x);
+            vv = make_float4(x[0], x[1], x[2], x[3]);
+          }
           const float2 vlo = make_float2(vv.x, vv.y), vhi = make_float2(vv.z, vv.w);
 #pragma unroll
           for (int h = 0; h < G; ++h) {
@@ -499,7 +510,7 @@ struct TopkArgs {
   const int* cnt;
   const int* off;
   const int* nonempty;
-  const float* valsum;
+  const void* valsum;  // [U][C][128] value sums: float, or bf16 (the select_estimate instance says which)
   int* sel;
   int* selcnt;
   float* subpart;
@@ -906,7 +917,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   }
 }
 
-template <int G>
+template <int G, typename VT>
 __global__ void __launch_bounds__(kSThreads, 1) k_select_estimate(TopkArgs a) {
   extern __shared__ __align__(128) unsigned char se_raw[];
   pdl_trigger();
@@ -916,7 +927,8 @@ __global__ void __launch_bounds__(kSThreads, 1) k_select_estimate(TopkArgs a) {
     select_role(se_raw, a, blockIdx.x / a.G, blockIdx.x % a.G);
   } else {
     const int e = blockIdx.x - nsel;
-    estimate_role<G>(se_raw, a.valsum, a.cnt, a.scores, a.part1, a.C, e / a.PE, e % a.PE, a.PE, a.lam, a.err);
+    estimate_role<G, VT>(se_raw, static_cast<const VT*>(a.valsum), a.cnt, a.scores, a.part1, a.C, e / a.PE,
+                         e % a.PE, a.PE, a.lam, a.err);
   }
 }
 
@@ -953,7 +965,7 @@ struct ExactArgs {
   const int4* runs;
   const int4* splits;
   const int4* sruns;
-  const float* valsum;
+  const void* valsum;  // [U][C][128] the value sums the estimate read: float, or their bf16 copy
   const int* nonempty;
   const float* part1;    // [U][G][P]
   const float* subpart;  // [U][G]
@@ -1053,6 +1065,7 @@ struct StagePacker {
   }
 };
 
+template <typename VT>
 __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
   extern __shared__ __align__(128) unsigned char d3_raw[];
   D3Stage* st = reinterpret_cast<D3Stage*>(d3_raw);
@@ -1153,7 +1166,18 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
       const int first = max(sa.x, 0) + o;
       const int last = min(sb.x + (sb.y > 0 ? 1 : 0), kk);
       const int4* runs = a.runs + uh * a.kmax;
-      const float4* vsu = reinterpret_cast<const float4*>(a.valsum + (size_t)u * a.C * WI_D) + lane;
+      // the terms subtracted are the ones the estimate added: from the same copy of the value sums
+      // (the instance's type; no pointer of the other type exists in it)
+      const VT* vsu = static_cast<const VT*>(a.valsum) + (size_t)u * a.C * WI_D + 4 * lane;
+      auto ldvs = [&](int j) -> float4 {
+        if constexpr (sizeof(VT) == 4) {
+          return __ldg(reinterpret_cast<const float4*>(vsu + (size_t)j * WI_D));
+        } else {
+          float x[4];
+          load_bf16x4(reinterpret_cast<const bf16*>(vsu) + (size_t)j * WI_D, x);
+          return make_float4(x[0], x[1], x[2], x[3]);
+        }
+      };
       auto add_terms = [&](const float (&ww)[4], const float4 (&vv)[4]) {
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
@@ -1173,7 +1197,7 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
           const bool v = c < last && o + warp + 8 * x < 32;
           const int j = (v && rr.w >= 0 && rr.w < a.C) ? rr.w : 0;
           ww[x] = v ? __int_as_float(rr.z) : 0.f;
-          vv[x] = __ldg(vsu + (size_t)j * (WI_D / 4));
+          vv[x] = ldvs(j);
         }
         add_terms(ww, vv);
       }
@@ -1187,7 +1211,7 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
           const int4 rr = c < last ? runs[c] : make_int4(0, 0, 0, 0);
           const int j = (rr.w >= 0 && rr.w < a.C) ? rr.w : 0;
           ww[x] = c < last ? __int_as_float(rr.z) : 0.f;
-          vv[x] = __ldg(vsu + (size_t)j * (WI_D / 4));
+          vv[x] = ldvs(j);
         }
         add_terms(ww, vv);
       }
@@ -1434,14 +1458,27 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+template <int G, typename VT>
+cudaError_t launch_select_vt(const WiGeom& g, const WiDecodeBufs& b, const TopkArgs& t, cudaStream_t st) {
+  const size_t sel = sel_smem_bytes(g.C, g.kmax), es = es_smem<VT>();
+  const size_t smem = sel > es ? sel : es;
+  static int smem_set = 0;
+  cudaError_t e = wi_ensure_smem(k_select_estimate<G, VT>, smem, &smem_set);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_select_estimate<G, VT>, dim3(g.U * G + g.U * b.p_es), dim3(kSThreads), smem, st, t);
+}
+
+template <typename VT>
+cudaError_t launch_exact(const WiGeom& g, const WiDecodeBufs& b, const ExactArgs& a, cudaStream_t st) {
+  static int smem_set = 0;
+  cudaError_t e = wi_ensure_smem(k_exact_merge<VT>, kD3Smem, &smem_set);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_exact_merge<VT>, dim3(b.nsplit + 1, g.G, g.U), dim3(kD3Threads), kD3Smem, st, a);
+}
+
 template <int G>
 cudaError_t launch_select(const WiGeom& g, const WiDecodeBufs& b, const TopkArgs& t, cudaStream_t st) {
-  const size_t sel = sel_smem_bytes(g.C, g.kmax);
-  const size_t smem = sel > kEsSmem ? sel : kEsSmem;
-  static int smem_set = 0;
-  cudaError_t e = wi_ensure_smem(k_select_estimate<G>, smem, &smem_set);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(k_select_estimate<G>, dim3(g.U * G + g.U * b.p_es), dim3(kSThreads), smem, st, t);
+  return b.valsum16 ? launch_select_vt<G, bf16>(g, b, t, st) : launch_select_vt<G, float>(g, b, t, st);
 }
 
 template <int G>
@@ -1463,7 +1500,7 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   t.cnt = b.cnt;
   t.off = b.off;
   t.nonempty = b.nonempty;
-  t.valsum = b.valsum;
+  t.valsum = b.valsum16 ? b.valsum16 : static_cast<const void*>(b.valsum);
   t.sel = b.sel;
   t.selcnt = b.selcnt;
   t.subpart = b.subpart;
@@ -1497,7 +1534,7 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   a.runs = b.runs;
   a.splits = b.splits;
   a.sruns = b.sruns;
-  a.valsum = b.valsum;
+  a.valsum = b.valsum16 ? b.valsum16 : static_cast<const void*>(b.valsum);
   a.subn = b.subn;
   a.C = g.C;
   a.nonempty = b.nonempty;
@@ -1517,9 +1554,7 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   a.W = g.W;
   a.max_append = g.max_append;
   a.lam = lam;
-  static int smem3_set = 0;
-  if ((e = wi_ensure_smem(k_exact_merge, kD3Smem, &smem3_set)) != cudaSuccess) return e;
-  e = launch_pdl(k_exact_merge, dim3(b.nsplit + 1, G, g.U), dim3(kD3Threads), kD3Smem, st, a);
+  e = b.valsum16 ? launch_exact<bf16>(g, b, a, st) : launch_exact<float>(g, b, a, st);
   if (e != cudaSuccess) return e;
   return mark(ev, 3, st);
 }

@@ -19,12 +19,15 @@ struct WiGeom {
   int iters;
   int kmax;       // retrieval budget
   int max_append;
+  int vs16;       // decode reads the bf16 copy of the value sums
 };
 
 int wi_geom_from_config(const wi_config* cfg, WiGeom* g, char* msg, size_t msglen);
 void wi_set_error(const char* msg);  // sets the thread-local message of wi_last_error()
 
 // ---- build kernels (wi_build.cu); all enqueue on `st` and return the launch status
+// out[i] = bf16(in[i]), round to nearest even.
+cudaError_t wi_launch_to_bf16(const float* in, void* out, long long n, cudaStream_t st);
 cudaError_t wi_launch_invnorm(const void* K, float* invnorm, long long rows, cudaStream_t st);
 cudaError_t wi_launch_init_centroids(const WiGeom& g, const void* K, void* chat, cudaStream_t st);
 cudaError_t wi_launch_assign(const WiGeom& g, const void* K, const void* chat, int32_t* assign, int* err,
@@ -52,6 +55,7 @@ struct WiDecodeBufs {
   CUtensorMap map_mu;     // mu as rows of 128 bf16, 128-row boxes, 128-byte swizzle (tensor-core scores)
   const void* mu;
   const float* valsum;
+  const void* valsum16;   // [U][C][128] bf16 copy, when the config asks decode to read it (else null)
   const int* cnt;
   const int* off;
   const int* nonempty;

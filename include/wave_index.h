@@ -72,7 +72,9 @@ typedef struct {
   int max_append;         /* capacity of the decode-time append buffer, >= 0 */
   double budget_frac;
   int budget_k;
-  int reserved[3];        /* must be zero */
+  int valsum_bf16;        /* 0: decode reads the fp32 value sums; 1: it reads a bf16 copy made at
+                             build / import (round to nearest even; half the estimation bytes) */
+  int reserved[2];        /* must be zero */
 } wi_config;
 
 /*

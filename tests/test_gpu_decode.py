@@ -271,3 +271,56 @@ def test_exact_split_counts(wi, monkeypatch, splits):
         err = rel_l2(out.reshape(w.units, w.group, 128).astype(np.float64), ref)
         assert err.max() <= OUT_REL_L2, (t, err.max())
     ix.free()
+
+
+def _bf16_valsum_index(idx):
+    """The bf16 value-sum variant's definition: the stored fp32 value sums rounded to bf16."""
+    return [{**d, "valsum": oracle.bf16_round(oracle.fp32_round(d["valsum"]))} for d in idx]
+
+
+@pytest.mark.parametrize("g", [4, 7])
+def test_valsum_bf16_variant_imported_index(wi, g):
+    w = small(n_ctx=8192, seg_len=1024, clusters_per_seg=64, iters=2, n_q_heads=2 * g, n_kv_heads=2, budget_k=8,
+              seed=21)
+    k, v, q, K, V, Q = gen(w)
+    p = params_of(w)
+    idx = oracle.build_index(K, V, p)
+    cfg = wi.config_from_workload(w)
+    cfg.valsum_bf16 = 1
+    ix = wi.WaveIndex.adopt(cfg, dev16(k), dev16(v), *index_arrays(idx))
+    for t in range(2):
+        qb = kvsynth.queries(w, step=t)
+        out = ix.decode(dev16(qb)).cpu().numpy().reshape(w.units, w.group, 128).astype(np.float64)
+        ix.check()
+        Qt = oracle.bf16_from_bits(qb).reshape(w.units, w.group, 128)
+        ref = oracle.decode(Qt, K, V, _bf16_valsum_index(idx), p, w.group)
+        err = rel_l2(out, ref)
+        assert err.max() <= OUT_REL_L2, (t, err.max())
+    ix.free()
+
+
+def test_valsum_bf16_variant_built_index(wi):
+    """The library's own build with the variant: the decode matches the oracle on the exported
+    index with its value sums rounded to bf16."""
+    w = small(batch=2, n_q_heads=8, n_kv_heads=2, n_ctx=4096, seg_len=1024, clusters_per_seg=64, iters=3,
+              budget_k=8, seed=23)
+    k, v, q, K, V, Q = gen(w)
+    p = params_of(w)
+    cfg = wi.config_from_workload(w)
+    cfg.valsum_bf16 = 1
+    kt, vt = dev16(k), dev16(v)
+    ix = wi.WaveIndex.build(cfg, kt, vt)
+    exp = {n: t.cpu().numpy() for n, t in ix.export().items()}
+    out = ix.decode(dev16(q)).cpu().numpy().reshape(w.units, w.group, 128).astype(np.float64)
+    ix.check()
+    from helpers import assignment_from_index
+    idx = [{"counts": exp["counts"][u].astype(np.int64),
+            "mu": oracle.bf16_from_bits(exp["mu"][u].view(np.uint16)).reshape(w.clusters, 128),
+            "valsum": exp["valsum"][u].astype(np.float64),
+            "assignment": assignment_from_index(exp["counts"][u], exp["perm"][u], w.n_ctx, p.n_sink)}
+           for u in range(w.units)]
+    ref = oracle.decode(Q, K, V, _bf16_valsum_index(idx), p, w.group)
+    assert rel_l2(out, ref).max() <= OUT_REL_L2
+    # information: how far the variant moves the output from the fp32 value sums' definition
+    print(f"bf16 value sums vs fp32, relative L2 max {rel_l2(out, oracle.decode(Q, K, V, idx, p, w.group)).max():.2e}")
+    ix.free()
