@@ -16,7 +16,10 @@ Parity status per function (what pins it is in ``tests/test_oracle_pins.py``):
   build_unit_index    pinned (conservation invariants; singleton clusters)
   decode_unit         pinned (all-clusters = textbook softmax attention;
                               singleton clusters exact; Jensen bound; cosh
-                              closed form; explicit per-token loop)
+                              closed form; explicit per-token loop); its
+                              group-shared top-k variant pinned (one head =
+                              the default; brute-force summed-score top-k;
+                              all clusters = full attention)
   lse_merge           pinned (associativity against the single sum)
   full_attention      pinned (equals decode_unit with every cluster
                               retrieved; one row gives its value row;

@@ -228,7 +228,8 @@ def lse_merge(parts) -> np.ndarray:
 
 
 def decode_unit(q_heads: np.ndarray, K: np.ndarray, V: np.ndarray, index: dict, p: IndexParams,
-                k_app: np.ndarray | None = None, v_app: np.ndarray | None = None, details: bool = False):
+                k_app: np.ndarray | None = None, v_app: np.ndarray | None = None, details: bool = False,
+                group_topk: bool = False):
     """Tripartite attention of the g query heads of one kv head.
 
     For each head h (summaries de/fr/zh 2.A; zones merged into one softmax):
@@ -239,6 +240,8 @@ def decode_unit(q_heads: np.ndarray, K: np.ndarray, V: np.ndarray, index: dict, 
         e_j = q . mu_j / sqrt(d), contributing n_j exp(e_j) to the
         denominator and exp(e_j) valsum_j to the numerator;
       o = N / D with M = max over both zones (single sum, float64).
+    group_topk: the variant in which the g heads share one retrieval zone, the top-k of the
+    summed scores sum_h q_h . mu_j (each head still has its own logits and estimate).
     """
     n, d = K.shape
     scale = 1.0 / math.sqrt(d)
@@ -254,10 +257,11 @@ def decode_unit(q_heads: np.ndarray, K: np.ndarray, V: np.ndarray, index: dict, 
         vsd = np.concatenate([vsd, v_app])
     out = np.zeros((q_heads.shape[0], d))
     info = []
+    R_group = select_topk(mu @ q_heads.sum(axis=0), nonempty, k) if group_topk else None
     for h in range(q_heads.shape[0]):
         q = q_heads[h]
         s = mu @ q
-        R = select_topk(s, nonempty, k)
+        R = R_group if group_topk else select_topk(s, nonempty, k)
         member = np.isin(a, R)
         kx = np.concatenate([ks, K[member]])
         vx = np.concatenate([vsd, V[member]])
@@ -278,13 +282,13 @@ def decode_unit(q_heads: np.ndarray, K: np.ndarray, V: np.ndarray, index: dict, 
 
 
 def decode(Q: np.ndarray, K: np.ndarray, V: np.ndarray, indexes: list, p: IndexParams, group: int,
-           k_app=None, v_app=None, details: bool = False):
+           k_app=None, v_app=None, details: bool = False, group_topk: bool = False):
     """Decode over all units. Q [units][g][d]; K, V [units][n][d]; appended rows [units][t][d]."""
     outs, infos = [], []
     for u in range(K.shape[0]):
         ka = None if k_app is None else k_app[u]
         va = None if v_app is None else v_app[u]
-        r = decode_unit(Q[u], K[u], V[u], indexes[u], p, ka, va, details=details)
+        r = decode_unit(Q[u], K[u], V[u], indexes[u], p, ka, va, details=details, group_topk=group_topk)
         if details:
             outs.append(r[0])
             infos.append(r[1])

@@ -397,3 +397,34 @@ def test_full_attention_closed_forms():
     perm = rng.permutation(40)
     np.testing.assert_allclose(oracle.full_attention(Q, K[:, perm], V[:, perm]), oracle.full_attention(Q, K, V),
                                rtol=0, atol=1e-13)
+
+
+# ------------------------------------------------ group-shared retrieval ----
+
+def test_group_topk_variant_pins():
+    """The variant in which a kv head's query heads share the top-k of their summed scores:
+    one head reduces to the default decode; the shared selection is the brute-force top-k of
+    sum_h q_h . mu_j (explicit loops, full sort, ties to the lowest id) for every head; with every
+    cluster retrieved it is full attention."""
+    w = tiny_workload(n=1024, S=256, Cs=16, g=4, budget_k=5, seed=17)
+    K, V, Q = gen_unit(w)
+    p = params_of(w)
+    idx = oracle.build_index(K, V, p)
+    # one head: identical to the per-head definition
+    o1 = oracle.decode(Q[:, :1], K, V, idx, p, 1, group_topk=True)
+    np.testing.assert_array_equal(o1, oracle.decode(Q[:, :1], K, V, idx, p, 1))
+    # the shared selection, brute force
+    out, info = oracle.decode_unit(Q[0], K[0], V[0], idx[0], p, details=True, group_topk=True)
+    counts, mu = idx[0]["counts"], idx[0]["mu"]
+    summed = [(-sum(float(np.dot(Q[0, h], mu[j])) for h in range(4)), j) for j in range(mu.shape[0]) if counts[j] > 0]
+    want = sorted(j for _, j in sorted(summed)[:5])
+    for h in range(4):
+        assert list(info[h]["selected"]) == want
+    # the heads' own selections differ from the shared one somewhere (the variant is not the default)
+    _, own = oracle.decode_unit(Q[0], K[0], V[0], idx[0], p, details=True)
+    assert any(list(own[h]["selected"]) != want for h in range(4))
+    assert not np.allclose(out, oracle.decode_unit(Q[0], K[0], V[0], idx[0], p))
+    # every cluster retrieved: full attention
+    wa = tiny_workload(n=1024, S=256, Cs=16, g=4, budget_k=10 ** 6, seed=17)
+    np.testing.assert_allclose(oracle.decode(Q, K, V, idx, params_of(wa), 4, group_topk=True),
+                               oracle.full_attention(Q, K, V), rtol=0, atol=1e-12)
