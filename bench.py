@@ -272,6 +272,8 @@ def main():
                     help="with --profile-steps: also run the dense comparator after every decode step")
     ap.add_argument("--valsum-bf16", action="store_true",
                     help="the index variant whose decode reads a bf16 copy of the value sums")
+    ap.add_argument("--group-topk", action="store_true",
+                    help="the variant whose query heads share one top-k per kv head (summed scores)")
     ap.add_argument("--dense-steps", type=int, default=640,
                     help="dense comparator steps timed after the wave-index region (0: skip)")
     args = ap.parse_args()
@@ -309,6 +311,7 @@ def main():
     v_dev = torch.from_numpy(v.view(np.int16)).to(dev)
     cfg = wi.config_from_workload(w)
     cfg.valsum_bf16 = 1 if args.valsum_bf16 else 0
+    cfg.group_topk = 1 if args.group_topk else 0
     vs_bytes = 2 if args.valsum_bf16 else 4
     R = args.replicas
     stream = torch.cuda.Stream(device=dev)
@@ -507,7 +510,8 @@ def main():
                              f"({R * (w.units * w.n_ctx * 512 + bytes_d1) / 1e9:.1f} GB)",
                        "timing": f"CUDA graphs of {L} steps replayed; events on the launching stream",
                        "decode_layout": wi.wi_decode_layout(replicas[0].handle),
-                       "valsum": "bf16" if args.valsum_bf16 else "fp32"},
+                       "valsum": "bf16" if args.valsum_bf16 else "fp32",
+                       "retrieval": "per kv head (summed scores)" if args.group_topk else "per query head"},
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_kind": peak_kind,
                          "bytes_per_launch": cand[dom], "traffic": NCU_TRAFFIC.get((w.name, dom))},

@@ -42,7 +42,8 @@ class wi_config(ctypes.Structure):
         ("n_sink", ctypes.c_int), ("local_window", ctypes.c_int), ("max_append", ctypes.c_int),
         ("budget_frac", ctypes.c_double), ("budget_k", ctypes.c_int),
         ("valsum_bf16", ctypes.c_int),
-        ("reserved", ctypes.c_int * 2),
+        ("group_topk", ctypes.c_int),
+        ("reserved", ctypes.c_int * 1),
     ]
 
 

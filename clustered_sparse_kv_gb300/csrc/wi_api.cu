@@ -112,9 +112,10 @@ int wi_geom_from_config(const wi_config* c, WiGeom* g, char* msg, size_t msglen)
   if (c->max_append < 0) BAD("max_append must be >= 0");
   if (c->n_ctx + c->max_append >= (1LL << 24)) BAD("n_ctx + max_append must be < 2^24");
   if (c->valsum_bf16 != 0 && c->valsum_bf16 != 1) BAD("valsum_bf16 must be 0 or 1");
-  for (int i = 0; i < 2; ++i)
-    if (c->reserved[i]) BAD("reserved fields must be zero");
+  if (c->group_topk != 0 && c->group_topk != 1) BAD("group_topk must be 0 or 1");
+  if (c->reserved[0]) BAD("reserved fields must be zero");
   g->vs16 = c->valsum_bf16;
+  g->grp = c->group_topk;
   g->U = c->batch * c->layers * c->n_kv_heads;
   g->G = c->n_q_heads / c->n_kv_heads;
   g->S = c->seg_len;
@@ -229,7 +230,8 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   b.dsplits = ds;
   A(b.dpart, U * G * (size_t)ds * WI_PART * 4);
   A(b.dticket, U * 4);
-  A(b.scores, U * G * C * 4);
+  const size_t GK = G + (size_t)g.grp;  // key rows per unit (the summed-score row, if any)
+  A(b.scores, U * GK * C * 4);
   A(b.part1, U * G * (size_t)b.p_es * WI_PART * 4);
   A(b.sel, U * G * (size_t)g.kmax * 4);
   A(b.selcnt, U * G * 4);
@@ -240,7 +242,7 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   A(b.part3, U * G * (size_t)(b.nsplit + 1) * WI_PART * 4);
   A(b.subn, U * G * (size_t)(b.nsplit + 1) * WI_PART * 4);
   A(b.ticket, U * G * 4);
-  A(b.kmaxp, U * (size_t)b.p1 * G * 4);
+  A(b.kmaxp, U * (size_t)b.p1 * GK * 4);
   A(b.rows_total, 8);
   A(ix->q_dev, U * G * 128 * 2);
   A(ix->out_dev, U * G * 128 * 4);

@@ -93,22 +93,23 @@ struct ScCfg {
   static constexpr size_t A_OFF = kScQBytes;
   static constexpr size_t CNT_OFF = A_OFF + (size_t)STAGES * kScATile;
   static constexpr size_t WMAX_OFF = CNT_OFF + sizeof(int) * STAGES * kScTile;
-  static constexpr size_t BAR_OFF = WMAX_OFF + sizeof(uint32_t) * kScEpiWarps * 8;
+  static constexpr size_t BAR_OFF = WMAX_OFF + sizeof(uint32_t) * kScEpiWarps * 9;
   static constexpr size_t SMEM = BAR_OFF + sizeof(uint64_t) * (2 * STAGES + 2 * kScAcc) + 16;
 };
 
-template <int G>
+template <int G, bool GRP>
 __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant__ CUtensorMap map_mu,
                                                          const bf16* __restrict__ q, const int* __restrict__ cnt,
                                                          uint32_t* __restrict__ keys, unsigned* __restrict__ kmaxp,
                                                          int C, int P, int* err) {
+  constexpr int GK = G + (GRP ? 1 : 0);  // key rows per unit: the heads (+ their summed score)
   using CF = ScCfg<G>;
   constexpr int STAGES = CF::STAGES;
   extern __shared__ __align__(1024) unsigned char sc_raw[];
   unsigned char* qB = sc_raw;                                              // [k half][16 rows][128 B]
   unsigned char* A = sc_raw + CF::A_OFF;                                   // [stage][k half][128 rows][128 B]
   int* cnts = reinterpret_cast<int*>(sc_raw + CF::CNT_OFF);               // [stage][128]
-  uint32_t* wmax = reinterpret_cast<uint32_t*>(sc_raw + CF::WMAX_OFF);    // [epilogue warp][G]
+  uint32_t* wmax = reinterpret_cast<uint32_t*>(sc_raw + CF::WMAX_OFF);    // [epilogue warp][GK]
   uint64_t* full = reinterpret_cast<uint64_t*>(sc_raw + CF::BAR_OFF);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
@@ -212,6 +213,7 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
     uint32_t kmx[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) kmx[h] = 0u;
+    uint32_t kmxs = 0u;  // of the summed-score keys (group-shared retrieval)
     for (int it = grp; it < ntile; it += 2) {
       const int s = it % STAGES, r = it / STAGES, b = it % kScAcc;
       const int j0 = c0 + it * kScTile, nj = min(kScTile, c1 - j0);
@@ -239,26 +241,34 @@ __global__ void __launch_bounds__(kScThreads, 1) k_scores(const __grid_constant_
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           const uint32_t key = cn > 0 ? float_key(__uint_as_float(rr[h])) : 0u;
-          keys[((size_t)u * G + h) * C + j0 + row] = key;
+          keys[((size_t)u * GK + h) * C + j0 + row] = key;
           kmx[h] = max(kmx[h], key);
+        }
+        if constexpr (GRP) {  // group-shared retrieval: row G holds the key of the heads' summed score
+          float sum = 0.f;
+#pragma unroll
+          for (int h = 0; h < G; ++h) sum += __uint_as_float(rr[h]);
+          const uint32_t key = cn > 0 ? float_key(sum) : 0u;
+          keys[((size_t)u * GK + G) * C + j0 + row] = key;
+          kmxs = max(kmxs, key);
         }
       }
     }
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      uint32_t m = kmx[h];
+    for (int h = 0; h < GK; ++h) {
+      uint32_t m = h < G ? kmx[h < G ? h : 0] : kmxs;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) wmax[(warp - 2) * G + h] = m;
+      if (lane == 0) wmax[(warp - 2) * GK + h] = m;
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (tid < G) {  // this CTA's largest key per head: plain stores, the top-k takes the max over CTAs
+  if (tid < GK) {  // this CTA's largest key per row: plain stores, the top-k takes the max over CTAs
     uint32_t m = 0u;
 #pragma unroll
-    for (int w8 = 0; w8 < kScEpiWarps; ++w8) m = max(m, wmax[w8 * G + tid]);
-    kmaxp[((size_t)u * P + p) * G + tid] = m;
+    for (int w8 = 0; w8 < kScEpiWarps; ++w8) m = max(m, wmax[w8 * GK + tid]);
+    kmaxp[((size_t)u * P + p) * GK + tid] = m;
   }
   if (warp == 1) {
     tc_fence_after();
@@ -289,7 +299,7 @@ constexpr size_t es_smem() {
          sizeof(float) * kSWarps * 2 * 4 + 16;
 }
 
-template <int G, typename VT>
+template <int G, typename VT, int GK>
 __device__ void estimate_role(unsigned char* raw, const VT* __restrict__ valsum, const int* __restrict__ cnt,
                               const uint32_t* __restrict__ scores, float* __restrict__ part, int C, int u, int p,
                               int P, float lam, int* err) {
@@ -335,7 +345,7 @@ __device__ void estimate_role(unsigned char* raw, const VT* __restrict__ valsum,
       auto issue_scores = [&](int it) {
         const int s = it % kEsStages;
         const int j0 = c0 + it * kSTile, nj = min(kSTile, c1 - j0);
-        for (int h = 0; h < G; ++h) bulk_g2s(st[s].sc[h], scores + ((size_t)u * G + h) * C + j0, nj * 4, &full[s]);
+        for (int h = 0; h < G; ++h) bulk_g2s(st[s].sc[h], scores + ((size_t)u * GK + h) * C + j0, nj * 4, &full[s]);
       };
       const int pre = min(ntile, kEsStages);
       for (int it = 0; it < pre; ++it) issue_index(it);
@@ -675,10 +685,14 @@ __device__ __noinline__ void take_in_bin_radix(const KeySrc key_of, int C, uint3
   }
 }
 
+// Top-k of key row h of unit u (a query head's scores, or with group-shared retrieval the heads'
+// summed scores, row G), written out for that head or for every head of the unit.
+template <bool GRP>
 __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& a, int u, int h) {
   SelSmem& sm = *reinterpret_cast<SelSmem*>(raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const size_t uh = (size_t)u * a.G + h;
+  const int GK = a.G + (GRP ? 1 : 0);    // key rows per unit
+  const size_t uk = (size_t)u * GK + h;  // key row
   const int C = a.C, nch = (C + 31) / 32, kmax = a.kmax;
   uint32_t* ks = reinterpret_cast<uint32_t*>(raw + sizeof(SelSmem));                        // [C] if cached
   uint32_t* tmask = reinterpret_cast<uint32_t*>(raw + sizeof(SelSmem) + sel_keys_bytes(C, kmax));  // [nch]
@@ -686,9 +700,8 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   int* nc_s = sel_s + kmax;                                                                   // [kmax] rows
   int* of_s = nc_s + kmax;                                                                    // [kmax] first row
   int* rp_s = of_s + kmax;  // [kmax] first row among the selected rows
-  const uint32_t* s = a.scores + uh * C;
+  const uint32_t* s = a.scores + uk * C;
   const int* cn = a.cnt + (size_t)u * C;
-  int* out = a.sel + uh * kmax;
   const bool cached = C <= kSelKeysMax;
   bool rows_async = sel_rows_async(C, kmax);                  // uniform
   int* nc_a = reinterpret_cast<int*>(ks + C);                 // [C] counts of taken clusters, if rows_async
@@ -716,7 +729,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   // K0 = the largest key of a non-empty cluster, from k_scores' per-CTA maxima of the same
   // scores (every warp reduces them itself: no barrier)
   uint32_t K0 = 0u;
-  for (int i = lane; i < a.P1; i += 32) K0 = max(K0, __ldcg(a.kmaxp + ((size_t)u * a.P1 + i) * a.G + h));
+  for (int i = lane; i < a.P1; i += 32) K0 = max(K0, __ldcg(a.kmaxp + ((size_t)u * a.P1 + i) * GK + h));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) K0 = max(K0, __shfl_xor_sync(0xffffffffu, K0, o));
   for (int i = tid; i < kTopkBins; i += kSThreads) sm.hist[0][i] = 0;
@@ -858,77 +871,157 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
     R += t;
     __syncthreads();  // s_wt is reused by the next round; the position arrays are complete
   }
-  // ---- NSP = NS + 1 row-balanced splits of the head's exact rows [steady rows | selected rows]
-  // (T = S + R rows): split b starts at row floor(T b / NSP), i.e. at selected row
-  // max(0, floor(T b / NSP) - S): (position of the cluster holding that row, row inside it, the
-  // selected row); entry NSP is the end.  Split 0 also takes the S steady rows.
-  const float m_sub = kk > 0 ? a.lam * key_float(K0) : -INFINITY;
-  const int NSP = a.NS + 1;
-  int4* runs = a.runs + uh * kmax;
-  int4* splits = a.splits + uh * (NSP + 1);
-  int4* sruns = a.sruns + uh * NSP * 32;
-  if (tid < NSP) {
-    int4 sp = make_int4(0, 0, 0, 0);
-    const long long S = (long long)a.n_sink + a.W + max(*a.app_count, 0), T = S + R;
-    const int rb = (int)max(0LL, (T * tid) / NSP - S);
-    if (R > 0 && rb < R) {
-      int lo = 0, hi = kk - 1;  // largest position whose first row is <= rb
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (rp_s[mid] <= rb) lo = mid; else hi = mid - 1;
+  if constexpr (!GRP) {
+    const size_t uh = uk;  // key row = output head
+    int* out = a.sel + uh * kmax;
+    // ---- NSP = NS + 1 row-balanced splits of the head's exact rows [steady rows | selected rows]
+    // (T = S + R rows): split b starts at row floor(T b / NSP), i.e. at selected row
+    // max(0, floor(T b / NSP) - S): (position of the cluster holding that row, row inside it, the
+    // selected row); entry NSP is the end.  Split 0 also takes the S steady rows.
+    const float m_sub = kk > 0 ? a.lam * key_float(K0) : -INFINITY;
+    const int NSP = a.NS + 1;
+    int4* runs = a.runs + uh * kmax;
+    int4* splits = a.splits + uh * (NSP + 1);
+    int4* sruns = a.sruns + uh * NSP * 32;
+    if (tid < NSP) {
+      int4 sp = make_int4(0, 0, 0, 0);
+      const long long S = (long long)a.n_sink + a.W + max(*a.app_count, 0), T = S + R;
+      const int rb = (int)max(0LL, (T * tid) / NSP - S);
+      if (R > 0 && rb < R) {
+        int lo = 0, hi = kk - 1;  // largest position whose first row is <= rb
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (rp_s[mid] <= rb) lo = mid; else hi = mid - 1;
+        }
+        sp = make_int4(lo, rb - rp_s[lo], rb, 0);
+      } else {
+        sp = make_int4(kk, 0, R, 0);
       }
-      sp = make_int4(lo, rb - rp_s[lo], rb, 0);
-    } else {
-      sp = make_int4(kk, 0, R, 0);
+      splits[tid] = sp;
+      sm.s_spos[tid] = sp.x;
     }
-    splits[tid] = sp;
-    sm.s_spos[tid] = sp.x;
-  }
-  __syncthreads();
-  // ---- row run and weight per selected cluster; copies into the run windows of the splits
-  float zpart = 0.f;
-  for (int p = tid; p < kk; p += kSThreads) {
-    const int j = sel_s[p], nc = nc_s[p];
-    const float w = __expf(a.lam * key_float(key_of(j)) - m_sub);
-    const int4 run = make_int4(of_s[p], nc, __float_as_int(w), j);
-    out[p] = j;
-    runs[p] = run;
-    for (int b = 0; b < NSP; ++b) {
-      const int p0 = sm.s_spos[b];
-      if (p0 > p) break;
-      if (p < p0 + 32) sruns[b * 32 + (p - p0)] = run;
+    __syncthreads();
+    // ---- row run and weight per selected cluster; copies into the run windows of the splits
+    float zpart = 0.f;
+    for (int p = tid; p < kk; p += kSThreads) {
+      const int j = sel_s[p], nc = nc_s[p];
+      const float w = __expf(a.lam * key_float(key_of(j)) - m_sub);
+      const int4 run = make_int4(of_s[p], nc, __float_as_int(w), j);
+      out[p] = j;
+      runs[p] = run;
+      for (int b = 0; b < NSP; ++b) {
+        const int p0 = sm.s_spos[b];
+        if (p0 > p) break;
+        if (p < p0 + 32) sruns[b * 32 + (p - p0)] = run;
+      }
+      zpart = fmaf((float)nc, w, zpart);
     }
-    zpart = fmaf((float)nc, w, zpart);
-  }
-  for (int i = kk + tid; i < kmax; i += kSThreads) out[i] = -1;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) zpart += __shfl_xor_sync(0xffffffffu, zpart, o);
-  if (lane == 0) sm.s_wf[warp] = zpart;
-  __syncthreads();
-  // the retrieved clusters' value-sum terms are summed by the exact-attention CTAs that load them
-  if (tid == 0) {
-    a.selcnt[uh] = kk;
-    splits[NSP] = make_int4(kk, 0, R, 0);
-    float zz = 0.f;
-    for (int w = 0; w < kSNW; ++w) zz += sm.s_wf[w];
-    float* sp = a.subpart + uh * WI_PART;
-    sp[0] = m_sub;
-    sp[1] = zz;
+    for (int i = kk + tid; i < kmax; i += kSThreads) out[i] = -1;
+  #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) zpart += __shfl_xor_sync(0xffffffffu, zpart, o);
+    if (lane == 0) sm.s_wf[warp] = zpart;
+    __syncthreads();
+    // the retrieved clusters' value-sum terms are summed by the exact-attention CTAs that load them
+    if (tid == 0) {
+      a.selcnt[uh] = kk;
+      splits[NSP] = make_int4(kk, 0, R, 0);
+      float zz = 0.f;
+      for (int w = 0; w < kSNW; ++w) zz += sm.s_wf[w];
+      float* sp = a.subpart + uh * WI_PART;
+      sp[0] = m_sub;
+      sp[1] = zz;
+    }
+  } else {
+    // ---- NSP = NS + 1 row-balanced splits of the head's exact rows [steady rows | selected rows]
+    // (T = S + R rows): split b starts at row floor(T b / NSP), i.e. at selected row
+    // max(0, floor(T b / NSP) - S): (position of the cluster holding that row, row inside it, the
+    // selected row); entry NSP is the end.  Split 0 also takes the S steady rows.  The rows do not
+    // depend on the head: with group-shared retrieval every head of the unit gets these splits.
+    const int NSP = a.NS + 1;
+    int4 sp = make_int4(kk, 0, R, 0);
+    if (tid < NSP) {
+      const long long S = (long long)a.n_sink + a.W + max(*a.app_count, 0), T = S + R;
+      const int rb = (int)max(0LL, (T * tid) / NSP - S);
+      if (R > 0 && rb < R) {
+        int lo = 0, hi = kk - 1;  // largest position whose first row is <= rb
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (rp_s[mid] <= rb) lo = mid; else hi = mid - 1;
+        }
+        sp = make_int4(lo, rb - rp_s[lo], rb, 0);
+      }
+      sm.s_spos[tid] = sp.x;
+    }
+    __syncthreads();
+    // ---- per output head: row run and weight e^{lam s_hj - m_sub} per selected cluster (the head's
+    // own score), copies into the run windows of the splits, and the retrieved clusters' Z term
+    const int nh = GRP ? a.G : 1;
+    for (int hh = 0; hh < nh; ++hh) {  // uniform
+      const int ho = GRP ? hh : h;
+      const size_t uo = (size_t)u * a.G + ho;
+      uint32_t K0h = K0;  // the head's largest key: its m_sub
+      if constexpr (GRP) {
+        K0h = 0u;
+        for (int i = lane; i < a.P1; i += 32) K0h = max(K0h, __ldcg(a.kmaxp + ((size_t)u * a.P1 + i) * GK + ho));
+  #pragma unroll
+        for (int o = 16; o > 0; o >>= 1) K0h = max(K0h, __shfl_xor_sync(0xffffffffu, K0h, o));
+      }
+      const float m_sub = kk > 0 ? a.lam * key_float(K0h) : -INFINITY;
+      int* out = a.sel + uo * kmax;
+      int4* runs = a.runs + uo * kmax;
+      int4* splits = a.splits + uo * (NSP + 1);
+      int4* sruns = a.sruns + uo * NSP * 32;
+      if (tid < NSP) splits[tid] = sp;
+      float zpart = 0.f;
+      for (int p = tid; p < kk; p += kSThreads) {
+        const int j = sel_s[p], nc = nc_s[p];
+        uint32_t key;
+        if constexpr (GRP) key = __ldcg(a.scores + ((size_t)u * GK + ho) * C + j);  // the head's own score
+        else key = key_of(j);
+        const float w = __expf(a.lam * key_float(key) - m_sub);
+        const int4 run = make_int4(of_s[p], nc, __float_as_int(w), j);
+        out[p] = j;
+        runs[p] = run;
+        for (int b = 0; b < NSP; ++b) {
+          const int p0 = sm.s_spos[b];
+          if (p0 > p) break;
+          if (p < p0 + 32) sruns[b * 32 + (p - p0)] = run;
+        }
+        zpart = fmaf((float)nc, w, zpart);
+      }
+      for (int i = kk + tid; i < kmax; i += kSThreads) out[i] = -1;
+  #pragma unroll
+      for (int o = 16; o > 0; o >>= 1) zpart += __shfl_xor_sync(0xffffffffu, zpart, o);
+      if (lane == 0) sm.s_wf[warp] = zpart;
+      __syncthreads();
+      // the retrieved clusters' value-sum terms are summed by the exact-attention CTAs that load them
+      if (tid == 0) {
+        a.selcnt[uo] = kk;
+        splits[NSP] = make_int4(kk, 0, R, 0);
+        float zz = 0.f;
+        for (int w = 0; w < kSNW; ++w) zz += sm.s_wf[w];
+        float* spp = a.subpart + uo * WI_PART;
+        spp[0] = m_sub;
+        spp[1] = zz;
+      }
+      if constexpr (GRP) __syncthreads();  // s_wf is written again for the next head
+    }
   }
 }
 
-template <int G, typename VT>
+template <int G, typename VT, bool GRP>
 __global__ void __launch_bounds__(kSThreads, 1) k_select_estimate(TopkArgs a) {
   extern __shared__ __align__(128) unsigned char se_raw[];
   pdl_trigger();
-  const int nsel = a.U * a.G;
+  const int nsel = GRP ? a.U : a.U * a.G;
   if ((int)blockIdx.x < nsel) {
     pdl_wait();
-    select_role(se_raw, a, blockIdx.x / a.G, blockIdx.x % a.G);
+    // a query head's row, or with group-shared retrieval the unit's summed-score row G
+    select_role<GRP>(se_raw, a, GRP ? (int)blockIdx.x : (int)blockIdx.x / a.G, GRP ? a.G : (int)blockIdx.x % a.G);
   } else {
     const int e = blockIdx.x - nsel;
-    estimate_role<G, VT>(se_raw, static_cast<const VT*>(a.valsum), a.cnt, a.scores, a.part1, a.C, e / a.PE,
-                         e % a.PE, a.PE, a.lam, a.err);
+    estimate_role<G, VT, G + (GRP ? 1 : 0)>(se_raw, static_cast<const VT*>(a.valsum), a.cnt, a.scores, a.part1,
+                                            a.C, e / a.PE, e % a.PE, a.PE, a.lam, a.err);
   }
 }
 
@@ -1458,14 +1551,24 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-template <int G, typename VT>
+template <int G, typename VT, bool GRP>
 cudaError_t launch_select_vt(const WiGeom& g, const WiDecodeBufs& b, const TopkArgs& t, cudaStream_t st) {
   const size_t sel = sel_smem_bytes(g.C, g.kmax), es = es_smem<VT>();
   const size_t smem = sel > es ? sel : es;
   static int smem_set = 0;
-  cudaError_t e = wi_ensure_smem(k_select_estimate<G, VT>, smem, &smem_set);
+  cudaError_t e = wi_ensure_smem(k_select_estimate<G, VT, GRP>, smem, &smem_set);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_select_estimate<G, VT>, dim3(g.U * G + g.U * b.p_es), dim3(kSThreads), smem, st, t);
+  const int nsel = GRP ? g.U : g.U * G;
+  return launch_pdl(k_select_estimate<G, VT, GRP>, dim3(nsel + g.U * b.p_es), dim3(kSThreads), smem, st, t);
+}
+
+template <int G, bool GRP>
+cudaError_t launch_scores(const WiGeom& g, const WiDecodeBufs& b, const bf16* q, cudaStream_t st) {
+  static int smem_set = 0;
+  cudaError_t e = wi_ensure_smem(k_scores<G, GRP>, ScCfg<G>::SMEM, &smem_set);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_scores<G, GRP>, dim3(b.p1, g.U), dim3(kScThreads), ScCfg<G>::SMEM, st, b.map_mu, q, b.cnt,
+                    reinterpret_cast<uint32_t*>(b.scores), b.kmaxp, g.C, b.p1, b.err);
 }
 
 template <typename VT>
@@ -1478,7 +1581,9 @@ cudaError_t launch_exact(const WiGeom& g, const WiDecodeBufs& b, const ExactArgs
 
 template <int G>
 cudaError_t launch_select(const WiGeom& g, const WiDecodeBufs& b, const TopkArgs& t, cudaStream_t st) {
-  return b.valsum16 ? launch_select_vt<G, bf16>(g, b, t, st) : launch_select_vt<G, float>(g, b, t, st);
+  if (g.grp)
+    return b.valsum16 ? launch_select_vt<G, bf16, true>(g, b, t, st) : launch_select_vt<G, float, true>(g, b, t, st);
+  return b.valsum16 ? launch_select_vt<G, bf16, false>(g, b, t, st) : launch_select_vt<G, float, false>(g, b, t, st);
 }
 
 template <int G>
@@ -1489,11 +1594,7 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   cudaError_t e = mark(ev, 0, st);
   if (e != cudaSuccess) return e;
   // scores
-  static int smem_sc = 0;
-  if ((e = wi_ensure_smem(k_scores<G>, ScCfg<G>::SMEM, &smem_sc)) != cudaSuccess) return e;
-  e = launch_pdl(k_scores<G>, dim3(b.p1, g.U), dim3(kScThreads), ScCfg<G>::SMEM, st, b.map_mu, q, b.cnt,
-                 reinterpret_cast<uint32_t*>(b.scores), b.kmaxp, g.C,
-                 b.p1, b.err);
+  e = g.grp ? launch_scores<G, true>(g, b, q, st) : launch_scores<G, false>(g, b, q, st);
   if (e != cudaSuccess || (e = mark(ev, 1, st)) != cudaSuccess) return e;
   TopkArgs t;
   t.scores = reinterpret_cast<const uint32_t*>(b.scores);

@@ -20,6 +20,7 @@ struct WiGeom {
   int kmax;       // retrieval budget
   int max_append;
   int vs16;       // decode reads the bf16 copy of the value sums
+  int grp;        // group-shared retrieval: one top-k per kv head from the heads' summed scores
 };
 
 int wi_geom_from_config(const wi_config* cfg, WiGeom* g, char* msg, size_t msglen);

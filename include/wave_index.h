@@ -74,7 +74,10 @@ typedef struct {
   int budget_k;
   int valsum_bf16;        /* 0: decode reads the fp32 value sums; 1: it reads a bf16 copy made at
                              build / import (round to nearest even; half the estimation bytes) */
-  int reserved[2];        /* must be zero */
+  int group_topk;         /* 0: each query head takes its own top-k; 1: the query heads of a kv head
+                             share the top-k of their summed scores (each head keeps its own logits,
+                             estimate and retrieved-term weights) */
+  int reserved[1];        /* must be zero */
 } wi_config;
 
 /*

@@ -73,9 +73,18 @@ def test_build_rejects_bad_config(wi, kw, code):
 
 def test_reserved_fields_must_be_zero(wi):
     cfg = good_cfg(wi)
-    cfg.reserved[1] = 7
+    cfg.reserved[0] = 7
     out = ctypes.c_void_p()
     assert wi.lib.wi_build_index(ctypes.byref(cfg), 16, 16, None, None, ctypes.byref(out)) == -1
+
+
+@pytest.mark.parametrize("field", ["valsum_bf16", "group_topk"])
+def test_variant_flags_are_zero_or_one(wi, field):
+    cfg = good_cfg(wi)
+    setattr(cfg, field, 2)
+    out = ctypes.c_void_p()
+    assert wi.lib.wi_build_index(ctypes.byref(cfg), 16, 16, None, None, ctypes.byref(out)) == -1
+    assert field in wi.lib.wi_last_error().decode()
 
 
 def test_null_and_misaligned_pointers_rejected(wi):

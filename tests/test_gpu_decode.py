@@ -324,3 +324,40 @@ def test_valsum_bf16_variant_built_index(wi):
     # information: how far the variant moves the output from the fp32 value sums' definition
     print(f"bf16 value sums vs fp32, relative L2 max {rel_l2(out, oracle.decode(Q, K, V, idx, p, w.group)).max():.2e}")
     ix.free()
+
+
+@pytest.mark.parametrize("g", [4, 7])
+def test_group_topk_variant(wi, g):
+    """Group-shared retrieval: every query head of a kv head takes the top-k of the heads' summed
+    scores (the same ids for all of them), with its own logits, estimate and retrieved-term
+    weights; parity with the oracle's variant over three steps with appended tokens."""
+    w = small(batch=2, n_q_heads=2 * g, n_kv_heads=2, n_ctx=8192, seg_len=1024, clusters_per_seg=64, iters=2,
+              budget_k=8, seed=29)
+    k, v, q, K, V, Q = gen(w)
+    p = params_of(w)
+    idx = oracle.build_index(K, V, p)
+    T = 3
+    cfg = wi.config_from_workload(w, max_append=T)
+    cfg.group_topk = 1
+    ix = wi.WaveIndex.adopt(cfg, dev16(k), dev16(v), *index_arrays(idx))
+    ka, va = kvsynth.kv_cache(w, p0=w.n_ctx, p1=w.n_ctx + T)
+    KA = oracle.bf16_from_bits(ka).reshape(w.units, T, 128)
+    VA = oracle.bf16_from_bits(va).reshape(w.units, T, 128)
+    kk = oracle.budget_k(w.clusters, p)
+    for t in range(T):
+        qb = kvsynth.queries(w, step=t)
+        out = ix.decode(dev16(qb), dev16(ka[:, :, :, t]), dev16(va[:, :, :, t]))
+        ids, cnt = ix.selection()
+        torch.cuda.synchronize()
+        ix.check()
+        Qt = oracle.bf16_from_bits(qb).reshape(w.units, w.group, 128)
+        ref = oracle.decode(Qt, K, V, idx, p, w.group, k_app=KA[:, :t], v_app=VA[:, :t], group_topk=True)
+        got = out.cpu().numpy().reshape(w.units, w.group, 128).astype(np.float64)
+        assert rel_l2(got, ref).max() <= OUT_REL_L2, t
+        ids, cnt = ids.cpu().numpy(), cnt.cpu().numpy()
+        for u in range(w.units):
+            summed = idx[u]["mu"] @ Qt[u].sum(axis=0)
+            for h in range(w.group):
+                np.testing.assert_array_equal(ids[u, h], ids[u, 0])
+                check_topk(ids[u, h], cnt[u, h], summed, idx[u]["counts"] > 0, kk)
+    ix.free()
