@@ -210,7 +210,7 @@ def run_reference(args, w, rank, world):
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of the
 # current kernels on this workload (profiles/decode_kernels_llama3-8b-131k.md); to be retaken whenever
 # a kernel changes.
-NCU_TRAFFIC = {("llama3-8b-131k", "exact_merge"): 38_800_384 + 18_176}
+NCU_TRAFFIC = {("llama3-8b-131k", "exact_merge"): 38_799_104 + 20_992}
 
 
 def rank_seed(w, rank):

@@ -687,7 +687,7 @@ __device__ __noinline__ void take_in_bin_radix(const KeySrc key_of, int C, uint3
 
 // Top-k of key row h of unit u (a query head's scores, or with group-shared retrieval the heads'
 // summed scores, row G), written out for that head or for every head of the unit.
-template <bool GRP>
+template <int G, bool GRP>
 __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& a, int u, int h) {
   SelSmem& sm = *reinterpret_cast<SelSmem*>(raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -917,7 +917,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
       zpart = fmaf((float)nc, w, zpart);
     }
     for (int i = kk + tid; i < kmax; i += kSThreads) out[i] = -1;
-  #pragma unroll
+#pragma unroll
     for (int o = 16; o > 0; o >>= 1) zpart += __shfl_xor_sync(0xffffffffu, zpart, o);
     if (lane == 0) sm.s_wf[warp] = zpart;
     __syncthreads();
@@ -953,19 +953,27 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
       sm.s_spos[tid] = sp.x;
     }
     __syncthreads();
-    // ---- per output head: row run and weight e^{lam s_hj - m_sub} per selected cluster (the head's
-    // own score), copies into the run windows of the splits, and the retrieved clusters' Z term
-    const int nh = GRP ? a.G : 1;
-    for (int hh = 0; hh < nh; ++hh) {  // uniform
-      const int ho = GRP ? hh : h;
+    // every head's largest key (its m_sub) and its key of this thread's first selected cluster,
+    // requested together: one round trip for all heads
+    uint32_t K0g[G], keyg[G];
+    const int pf = tid < kk ? sel_s[tid] : 0;
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      K0g[hh] = 0u;
+      for (int i = lane; i < a.P1; i += 32) K0g[hh] = max(K0g[hh], __ldcg(a.kmaxp + ((size_t)u * a.P1 + i) * GK + hh));
+      keyg[hh] = tid < kk ? __ldcg(a.scores + ((size_t)u * GK + hh) * C + pf) : 0u;
+    }
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) K0g[hh] = max(K0g[hh], __shfl_xor_sync(0xffffffffu, K0g[hh], o));
+    }
+    // ---- per head: row run and weight e^{lam s_hj - m_sub} per selected cluster (the head's own
+    // score), copies into the run windows of the splits, and the retrieved clusters' Z term
+#pragma unroll
+    for (int ho = 0; ho < G; ++ho) {
       const size_t uo = (size_t)u * a.G + ho;
-      uint32_t K0h = K0;  // the head's largest key: its m_sub
-      if constexpr (GRP) {
-        K0h = 0u;
-        for (int i = lane; i < a.P1; i += 32) K0h = max(K0h, __ldcg(a.kmaxp + ((size_t)u * a.P1 + i) * GK + ho));
-  #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) K0h = max(K0h, __shfl_xor_sync(0xffffffffu, K0h, o));
-      }
+      const uint32_t K0h = K0g[ho];
       const float m_sub = kk > 0 ? a.lam * key_float(K0h) : -INFINITY;
       int* out = a.sel + uo * kmax;
       int4* runs = a.runs + uo * kmax;
@@ -975,9 +983,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
       float zpart = 0.f;
       for (int p = tid; p < kk; p += kSThreads) {
         const int j = sel_s[p], nc = nc_s[p];
-        uint32_t key;
-        if constexpr (GRP) key = __ldcg(a.scores + ((size_t)u * GK + ho) * C + j);  // the head's own score
-        else key = key_of(j);
+        const uint32_t key = p == tid ? keyg[ho] : __ldcg(a.scores + ((size_t)u * GK + ho) * C + j);
         const float w = __expf(a.lam * key_float(key) - m_sub);
         const int4 run = make_int4(of_s[p], nc, __float_as_int(w), j);
         out[p] = j;
@@ -990,7 +996,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
         zpart = fmaf((float)nc, w, zpart);
       }
       for (int i = kk + tid; i < kmax; i += kSThreads) out[i] = -1;
-  #pragma unroll
+#pragma unroll
       for (int o = 16; o > 0; o >>= 1) zpart += __shfl_xor_sync(0xffffffffu, zpart, o);
       if (lane == 0) sm.s_wf[warp] = zpart;
       __syncthreads();
@@ -1004,7 +1010,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
         spp[0] = m_sub;
         spp[1] = zz;
       }
-      if constexpr (GRP) __syncthreads();  // s_wf is written again for the next head
+      __syncthreads();  // s_wf is written again for the next head
     }
   }
 }
@@ -1017,7 +1023,7 @@ __global__ void __launch_bounds__(kSThreads, 1) k_select_estimate(TopkArgs a) {
   if ((int)blockIdx.x < nsel) {
     pdl_wait();
     // a query head's row, or with group-shared retrieval the unit's summed-score row G
-    select_role<GRP>(se_raw, a, GRP ? (int)blockIdx.x : (int)blockIdx.x / a.G, GRP ? a.G : (int)blockIdx.x % a.G);
+    select_role<G, GRP>(se_raw, a, GRP ? (int)blockIdx.x : (int)blockIdx.x / a.G, GRP ? a.G : (int)blockIdx.x % a.G);
   } else {
     const int e = blockIdx.x - nsel;
     estimate_role<G, VT, G + (GRP ? 1 : 0)>(se_raw, static_cast<const VT*>(a.valsum), a.cnt, a.scores, a.part1,
