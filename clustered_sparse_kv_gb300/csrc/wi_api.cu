@@ -554,16 +554,16 @@ static void drop_host_graph(wi_index* ix) {
 }
 
 // Capture the host-buffer step as a graph: a copy kernel reads the query from mapped host memory,
-// the decode chain runs, a copy kernel writes the output to mapped host memory (no DMA setup per
-// step).  False if the runtime refuses (the caller then launches directly).
+// the decode chain runs and its merge writes the output straight into mapped host memory (no DMA
+// setup per step).  False if the runtime refuses (the caller then launches directly).
 static bool capture_host_graph(wi_index* ix, const void* qd, void* od, size_t qb, size_t ob) {
   if (!ix->cap_stream && cudaStreamCreateWithFlags(&ix->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
     return false;
   cudaStream_t cs = ix->cap_stream;
   if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) return false;
+  (void)ob;
   bool ok = wi_launch_copy16(qd, ix->q_dev, qb, cs) == cudaSuccess &&
-            wi_launch_decode(ix->g, ix->b, ix->q_dev, ix->out_dev, cs, nullptr) == cudaSuccess &&
-            wi_launch_copy16(ix->out_dev, od, ob, cs) == cudaSuccess;
+            wi_launch_decode(ix->g, ix->b, ix->q_dev, static_cast<float*>(od), cs, nullptr) == cudaSuccess;
   cudaGraph_t graph = nullptr;
   ok = cudaStreamEndCapture(cs, &graph) == cudaSuccess && ok && graph;
   cudaGraphExec_t exec = nullptr;

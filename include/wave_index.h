@@ -138,11 +138,11 @@ int wi_decode_step(wi_index* ix, const void* q, const void* k_new, const void* v
  * copies asynchronous DMA; pageable memory works but is slower.  A step with
  * pinned (device-mapped, 16-byte aligned) q and out, no append and decode
  * profiling off runs as one CUDA graph that the index captures for that pair
- * of buffers: a copy kernel reads q from host memory, the decode kernels run,
- * a copy kernel writes out to host memory.  The index owns a stream and the
- * graph until wi_free; a call with other buffers captures again, and after a
- * few such changes the index launches directly, as it does for every other
- * step.  Results are identical either way.
+ * of buffers: a copy kernel reads q from host memory, the decode kernels run
+ * and the final merge writes out straight to host memory.  The index owns a
+ * stream and the graph until wi_free; a call with other buffers captures
+ * again, and after a few such changes the index launches directly, as it
+ * does for every other step.  Results are identical either way.
  */
 int wi_decode_step_host(wi_index* ix, const void* q_host, const void* k_new_host, const void* v_new_host,
                         float* out_host, void* stream);
