@@ -968,49 +968,62 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) K0g[hh] = max(K0g[hh], __shfl_xor_sync(0xffffffffu, K0g[hh], o));
     }
-    // ---- per head: row run and weight e^{lam s_hj - m_sub} per selected cluster (the head's own
-    // score), copies into the run windows of the splits, and the retrieved clusters' Z term
+    // ---- every (selected cluster, head) pair in one pass: the head's row run with its weight
+    // e^{lam s_hj - m_sub_h}, the copies into its split windows, its share of the retrieved Z term
+    float msub[G], zp[G];
 #pragma unroll
     for (int ho = 0; ho < G; ++ho) {
-      const size_t uo = (size_t)u * a.G + ho;
-      const uint32_t K0h = K0g[ho];
-      const float m_sub = kk > 0 ? a.lam * key_float(K0h) : -INFINITY;
-      int* out = a.sel + uo * kmax;
-      int4* runs = a.runs + uo * kmax;
-      int4* splits = a.splits + uo * (NSP + 1);
-      int4* sruns = a.sruns + uo * NSP * 32;
-      if (tid < NSP) splits[tid] = sp;
-      float zpart = 0.f;
-      for (int p = tid; p < kk; p += kSThreads) {
-        const int j = sel_s[p], nc = nc_s[p];
+      msub[ho] = kk > 0 ? a.lam * key_float(K0g[ho]) : -INFINITY;
+      zp[ho] = 0.f;
+    }
+    for (int p = tid; p < kk; p += kSThreads) {
+      const int j = sel_s[p], nc = nc_s[p], of = of_s[p];
+#pragma unroll
+      for (int ho = 0; ho < G; ++ho) {
+        const size_t uo = (size_t)u * a.G + ho;
         const uint32_t key = p == tid ? keyg[ho] : __ldcg(a.scores + ((size_t)u * GK + ho) * C + j);
-        const float w = __expf(a.lam * key_float(key) - m_sub);
-        const int4 run = make_int4(of_s[p], nc, __float_as_int(w), j);
-        out[p] = j;
-        runs[p] = run;
+        const float w = __expf(a.lam * key_float(key) - msub[ho]);
+        const int4 run = make_int4(of, nc, __float_as_int(w), j);
+        a.sel[uo * kmax + p] = j;
+        a.runs[uo * kmax + p] = run;
+        int4* sruns = a.sruns + uo * NSP * 32;
         for (int b = 0; b < NSP; ++b) {
           const int p0 = sm.s_spos[b];
           if (p0 > p) break;
           if (p < p0 + 32) sruns[b * 32 + (p - p0)] = run;
         }
-        zpart = fmaf((float)nc, w, zpart);
+        zp[ho] = fmaf((float)nc, w, zp[ho]);
       }
-      for (int i = kk + tid; i < kmax; i += kSThreads) out[i] = -1;
+    }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) zpart += __shfl_xor_sync(0xffffffffu, zpart, o);
-      if (lane == 0) sm.s_wf[warp] = zpart;
-      __syncthreads();
-      // the retrieved clusters' value-sum terms are summed by the exact-attention CTAs that load them
-      if (tid == 0) {
-        a.selcnt[uo] = kk;
-        splits[NSP] = make_int4(kk, 0, R, 0);
+    for (int ho = 0; ho < G; ++ho) {
+      const size_t uo = (size_t)u * a.G + ho;
+      for (int i = kk + tid; i < kmax; i += kSThreads) a.sel[uo * kmax + i] = -1;
+      if (tid < NSP) a.splits[uo * (NSP + 1) + tid] = sp;
+    }
+    // per-head Z terms: warp sums into shared scratch (the second histogram is free by now)
+    float* wz = reinterpret_cast<float*>(sm.hist[1]);  // [warps][G]
+#pragma unroll
+    for (int ho = 0; ho < G; ++ho) {
+      float z = zp[ho];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+      if (lane == 0) wz[warp * G + ho] = z;
+    }
+    __syncthreads();
+    // the retrieved clusters' value-sum terms are summed by the exact-attention CTAs that load them
+#pragma unroll
+    for (int ho = 0; ho < G; ++ho) {
+      if (tid == ho) {
+        const size_t uo = (size_t)u * a.G + ho;
         float zz = 0.f;
-        for (int w = 0; w < kSNW; ++w) zz += sm.s_wf[w];
+        for (int w = 0; w < kSNW; ++w) zz += wz[w * G + ho];
+        a.selcnt[uo] = kk;
+        a.splits[uo * (NSP + 1) + NSP] = make_int4(kk, 0, R, 0);
         float* spp = a.subpart + uo * WI_PART;
-        spp[0] = m_sub;
+        spp[0] = msub[ho];
         spp[1] = zz;
       }
-      __syncthreads();  // s_wf is written again for the next head
     }
   }
 }
