@@ -71,3 +71,22 @@ def test_reference_arm_only_on_rank_zero(capsys):
 
     bench.run_reference(A(), w, rank=1, world=2)
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_on_rank_zero(capsys):
+    """The reference arm (the float64 oracle on the host cores) prints one JSON line with the
+    contract's keys, on the workload it is given."""
+    import json
+    import bench
+    import kvsynth
+    w = kvsynth.get_workload("tiny-8k")
+
+    class A:
+        steps, warmup = 2, 0
+
+    bench.run_reference(A(), w, rank=0, world=1)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "steps/s" and line["higher_is_better"] is True
+    assert line["value"] > 0 and line["config"]["workload"] == "tiny-8k"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
