@@ -22,6 +22,10 @@
 //                     into shared memory), plus the retrieved clusters' value-sum
 //                     terms; the last CTA of a head merges estimate - retrieved
 //                     terms + exact partials by LSE.
+// Index variants are separate kernel instances (the default ones carry none of
+// their code): value sums read as a bf16 copy (the estimation role and the
+// exact kernel per value type), and group-shared retrieval (k_scores also keys
+// the heads' summed score; one top-k per kv head, written out for each head).
 #include <cuda_runtime.h>
 
 #include "wi_common.cuh"
