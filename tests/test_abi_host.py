@@ -125,3 +125,27 @@ def test_error_is_thread_local(wi):
     t.join()
     assert seen["msg"] == ""
     assert "head_dim" in wi.lib.wi_last_error().decode()
+
+
+def test_header_is_c_and_config_layout_matches_binding(wi, tmp_path):
+    """The header compiles as plain C99, and wi_config has the same size and field offsets in C as
+    in the ctypes binding (a mismatch would pass wrong shapes silently)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [name for name, _ in wi.wi_config._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "wave_index.h"\nint main(void) {\n'
+                   '  printf("size %zu\\n", sizeof(wi_config));\n'
+                   + "".join(f'  printf("{f} %zu\\n", offsetof(wi_config, {f}));\n' for f in fields)
+                   + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)],
+                   check=True)
+    out = dict(line.split() for line in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                       text=True).stdout.splitlines())
+    assert int(out["size"]) == ctypes.sizeof(wi.wi_config)
+    for f in fields:
+        assert int(out[f]) == getattr(wi.wi_config, f).offset, f
