@@ -62,6 +62,7 @@ _SIGS = {
     "wi_decode_layout": [_vp, _ip, _ip, _ip],
     "wi_kmeans_step": [_cfgp, _vp, _vp, _vp, _vp, _vp],
     "wi_kmeans_step_noalloc": [_cfgp, _vp, _vp, _vp, _vp, _vp],
+    "wi_init_centroids": [_cfgp, _vp, _vp, _vp],
     "wi_check_device": [_vp],
     "wi_profile_begin": [_vp, ctypes.c_int],
     "wi_index_build_stats": [_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), _ip],
@@ -178,6 +179,10 @@ def wi_decode_layout(ix: int) -> dict:
 def wi_kmeans_step(cfg: wi_config, k, centroids, assign, new_centroids, stream=None):
     _check(lib.wi_kmeans_step(ctypes.byref(cfg), _ptr(k), _ptr(centroids), _ptr(assign), _ptr(new_centroids),
                               _stream(stream)))
+
+
+def wi_init_centroids(cfg: wi_config, k, centroids, stream=None):
+    _check(lib.wi_init_centroids(ctypes.byref(cfg), _ptr(k), _ptr(centroids), _stream(stream)))
 
 
 def wi_kmeans_step_noalloc(cfg: wi_config, k, centroids, assign, new_centroids, stream=None):

@@ -689,6 +689,16 @@ done:
   return rc;
 }
 
+int wi_init_centroids(const wi_config* cfg, const void* k, void* centroids, void* stream) {
+  g_err[0] = 0;
+  WiGeom g;
+  int rc = wi_geom_from_config(cfg, &g, g_err, sizeof(g_err));
+  if (rc != WI_OK) return rc;
+  if (!k || !centroids) return fail(WI_EINVAL, "k and centroids must be non-NULL");
+  WI_CUDA(wi_launch_init_centroids(g, k, centroids, static_cast<cudaStream_t>(stream)));
+  return WI_OK;
+}
+
 int wi_profile_begin(wi_index* ix, int max_steps) {
   g_err[0] = 0;
   if (!ix || max_steps < 0) return fail(WI_EINVAL, "index is NULL or max_steps < 0");

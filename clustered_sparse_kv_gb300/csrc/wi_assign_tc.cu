@@ -324,8 +324,8 @@ cudaError_t wi_launch_assign_tc(const WiGeom& g, const void* K, const void* chat
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = P.total_tiles < sms ? P.total_tiles : sms;
   const size_t smem = sizeof(TcSmem);
-  static int smem_set = 0;
-  cudaError_t e = wi_ensure_smem(k_assign_tc, smem, &smem_set);
+  static int smem_set[kWiSmemDevices] = {};
+  cudaError_t e = wi_ensure_smem(k_assign_tc, smem, smem_set);
   if (e != cudaSuccess) return e;
   k_assign_tc<<<grid, kThreads, smem, st>>>(map_k, map_c, P);
   return cudaGetLastError();

@@ -370,8 +370,8 @@ cudaError_t wi_launch_assign(const WiGeom& g, const void* K, const void* chat, i
                              cudaStream_t st) {
   if (wi_assign_tc_supported(g)) return wi_launch_assign_tc(g, K, chat, assign, err, st);
   const size_t smem = wi_assign_smem_bytes(g);
-  static int smem_set = 0;
-  cudaError_t e = wi_ensure_smem(k_assign_simt, smem, &smem_set);
+  static int smem_set[kWiSmemDevices] = {};
+  cudaError_t e = wi_ensure_smem(k_assign_simt, smem, smem_set);
   if (e != cudaSuccess) return e;
   dim3 grid(g.S / kAsgTok, g.nseg, g.U);
   k_assign_simt<<<grid, 256, smem, st>>>(static_cast<const bf16*>(K), static_cast<const bf16*>(chat), assign, g.S,
@@ -382,8 +382,8 @@ cudaError_t wi_launch_assign(const WiGeom& g, const void* K, const void* chat, i
 cudaError_t wi_launch_segment_sort(const WiGeom& g, const int32_t* assign, int* seg_counts, int* seg_offsets,
                                    int* slots, int* err, cudaStream_t st) {
   const size_t smem = sizeof(int) * ((size_t)3 * g.Cs + 1 + 32 + 2 * (size_t)g.S);
-  static int smem_set = 0;
-  cudaError_t e = wi_ensure_smem(k_segment_sort, smem, &smem_set);
+  static int smem_set[kWiSmemDevices] = {};
+  cudaError_t e = wi_ensure_smem(k_segment_sort, smem, smem_set);
   if (e != cudaSuccess) return e;
   k_segment_sort<<<g.U * g.nseg, 512, smem, st>>>(assign, seg_counts, seg_offsets, slots, g.S, g.Cs, g.nseg, g.n,
                                                    err);

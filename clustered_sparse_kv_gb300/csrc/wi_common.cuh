@@ -97,13 +97,20 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* tmp, int* total)
   return base + inc - v;
 }
 
-// Raise a kernel's dynamic shared-memory limit once per size increase (not
-// on every launch, so that launches inside a stream capture make no
-// attribute calls once warmed up).  `cur` is a per-kernel static.
+// Raise a kernel's dynamic shared-memory limit once per size increase and per
+// device (not on every launch, so that launches inside a stream capture make
+// no attribute calls once warmed up; the attribute belongs to the current
+// device's context, so a process that uses several devices sets it on each).
+// `cur` is a per-kernel static array indexed by device ordinal.
+constexpr int kWiSmemDevices = 64;
 template <typename F>
-inline cudaError_t wi_ensure_smem(F* func, size_t bytes, int* cur) {
-  if ((int)bytes <= *cur) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess) *cur = (int)bytes;
+inline cudaError_t wi_ensure_smem(F* func, size_t bytes, int (&cur)[kWiSmemDevices]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < kWiSmemDevices;
+  if (cached && (int)bytes <= cur[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && cached) cur[dev] = (int)bytes;
   return e;
 }

@@ -1578,8 +1578,8 @@ template <int G, typename VT, bool GRP>
 cudaError_t launch_select_vt(const WiGeom& g, const WiDecodeBufs& b, const TopkArgs& t, cudaStream_t st) {
   const size_t sel = sel_smem_bytes(g.C, g.kmax), es = es_smem<VT>();
   const size_t smem = sel > es ? sel : es;
-  static int smem_set = 0;
-  cudaError_t e = wi_ensure_smem(k_select_estimate<G, VT, GRP>, smem, &smem_set);
+  static int smem_set[kWiSmemDevices] = {};
+  cudaError_t e = wi_ensure_smem(k_select_estimate<G, VT, GRP>, smem, smem_set);
   if (e != cudaSuccess) return e;
   const int nsel = GRP ? g.U : g.U * G;
   return launch_pdl(k_select_estimate<G, VT, GRP>, dim3(nsel + g.U * b.p_es), dim3(kSThreads), smem, st, t);
@@ -1587,8 +1587,8 @@ cudaError_t launch_select_vt(const WiGeom& g, const WiDecodeBufs& b, const TopkA
 
 template <int G, bool GRP>
 cudaError_t launch_scores(const WiGeom& g, const WiDecodeBufs& b, const bf16* q, cudaStream_t st) {
-  static int smem_set = 0;
-  cudaError_t e = wi_ensure_smem(k_scores<G, GRP>, ScCfg<G>::SMEM, &smem_set);
+  static int smem_set[kWiSmemDevices] = {};
+  cudaError_t e = wi_ensure_smem(k_scores<G, GRP>, ScCfg<G>::SMEM, smem_set);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_scores<G, GRP>, dim3(b.p1, g.U), dim3(kScThreads), ScCfg<G>::SMEM, st, b.map_mu, q, b.cnt,
                     reinterpret_cast<uint32_t*>(b.scores), b.kmaxp, g.C, b.p1, b.err);
@@ -1596,8 +1596,8 @@ cudaError_t launch_scores(const WiGeom& g, const WiDecodeBufs& b, const bf16* q,
 
 template <typename VT>
 cudaError_t launch_exact(const WiGeom& g, const WiDecodeBufs& b, const ExactArgs& a, cudaStream_t st) {
-  static int smem_set = 0;
-  cudaError_t e = wi_ensure_smem(k_exact_merge<VT>, kD3Smem, &smem_set);
+  static int smem_set[kWiSmemDevices] = {};
+  cudaError_t e = wi_ensure_smem(k_exact_merge<VT>, kD3Smem, smem_set);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_exact_merge<VT>, dim3(b.nsplit + 1, g.G, g.U), dim3(kD3Threads), kD3Smem, st, a);
 }

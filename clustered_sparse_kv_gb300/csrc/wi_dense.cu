@@ -278,8 +278,8 @@ __global__ void __launch_bounds__(kDnThreads, G <= 4 ? 2 : 1) k_dense_decode(Den
 
 template <int G>
 cudaError_t launch_dense_g(const WiGeom& g, const WiDecodeBufs& b, const void* q, float* out, cudaStream_t st) {
-  static int smem_set = 0;
-  cudaError_t e = wi_ensure_smem(k_dense_decode<G>, kDnSmem, &smem_set);
+  static int smem_set[kWiSmemDevices] = {};
+  cudaError_t e = wi_ensure_smem(k_dense_decode<G>, kDnSmem, smem_set);
   if (e != cudaSuccess) return e;
   DenseArgs a;
   a.q = static_cast<const bf16*>(q);

@@ -15,12 +15,13 @@
 // different host threads without ordering) race on it; calls on one stream
 // are ordered and safe.  The array keeps the previous call's contents; the
 // only part that must start at zero, the device error word, is cleared on
-// every call.  The first call on a device looks up the array's device address
-// (cudaGetSymbolAddress) with that device current.
+// every call.  Every call looks up the array's device address
+// (cudaGetSymbolAddress, which allocates nothing) with the caller's device
+// current, so the address stays right after the device's context has been
+// torn down and made again (a cudaDeviceReset reloads the module).
 #include <cuda_runtime.h>
 
 #include <cstdio>
-#include <mutex>
 
 #include "wave_index.h"
 #include "wi_internal.h"
@@ -28,14 +29,8 @@
 namespace {
 
 constexpr size_t kWiNoallocScratchBytes = (size_t)8 << 20;
-constexpr int kWiMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_wi_noalloc_scratch[kWiNoallocScratchBytes];
-
-// Device address of the array per device ordinal, looked up once per device
-// (host code may not use the symbol itself as a device pointer).
-void* g_scratch_addr[kWiMaxDevices] = {};
-std::mutex g_scratch_mu;
 
 int nfail(int code, const char* msg, cudaError_t e = cudaSuccess) {
   char buf[512];
@@ -78,21 +73,11 @@ extern "C" int wi_kmeans_step_noalloc(const wi_config* cfg, const void* k, const
              need, kWiNoallocScratchBytes);
     return nfail(WI_EINVAL, msg);
   }
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return nfail(WI_ECUDA, "cudaGetDevice", e);
-  if (dev < 0 || dev >= kWiMaxDevices) return nfail(WI_EUNSUPPORTED, "device ordinal out of range");
-  unsigned char* base = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-      void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_wi_noalloc_scratch);
-      if (e != cudaSuccess || !p) return nfail(WI_ECUDA, "cudaGetSymbolAddress(no-allocation scratch)", e);
-      g_scratch_addr[dev] = p;
-    }
-    base = static_cast<unsigned char*>(g_scratch_addr[dev]);
-  }
+  // host code may not use the symbol itself as a device pointer: ask for this device's address
+  void* sym = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&sym, g_wi_noalloc_scratch);
+  if (e != cudaSuccess || !sym) return nfail(WI_ECUDA, "cudaGetSymbolAddress(no-allocation scratch)", e);
+  unsigned char* base = static_cast<unsigned char*>(sym);
   int* err = reinterpret_cast<int*>(base + o_err);
   float* invnorm = reinterpret_cast<float*>(base + o_inv);
   int* seg_counts = reinterpret_cast<int*>(base + o_cnt);

@@ -81,7 +81,10 @@ typedef struct {
 } wi_config;
 
 /*
- * Build the index (prefill).  k, v: device bf16 [batch][layers][n_kv_heads]
+ * Build the index (prefill): segmented spherical k-means and the per-cluster
+ * count, mean key and value sum of every unit (summaries de/fr/zh 2.A
+ * "segmented clustering", fr 2.A.2 "spherical k-means", zh 2.A "precomputed
+ * value sum").  k, v: device bf16 [batch][layers][n_kv_heads]
  * [n_ctx][128], caller-owned.  The library permutes their clustered rows IN
  * PLACE into cluster-contiguous order (cluster by cluster, by position inside
  * a cluster; steady rows stay where they are) and keeps pointing at them: the
@@ -119,7 +122,10 @@ int wi_index_export(const wi_index* ix, int32_t* counts, int32_t* offsets, int32
                     float* valsum, void* stream);
 
 /*
- * One decode step.  q: device bf16 [batch][layers][n_q_heads][128], the
+ * One decode step of the tripartite attention approximation (summaries
+ * de/fr/zh 2.A: steady and retrieval zones exact, estimation zone from each
+ * cluster's mean key, count and value sum, merged by log-sum-exp; zh section 3
+ * for the ~1.8% retrieval budget).  q: device bf16 [batch][layers][n_q_heads][128], the
  * queries of the step (already rotated), 16-byte aligned; out: device fp32 [batch][layers]
  * [n_q_heads][128], attention output per query head.  Attention runs over
  * the current context: the n_ctx built tokens plus every token appended so
@@ -197,6 +203,19 @@ int wi_kmeans_step(const wi_config* cfg, const void* k, const void* centroids, i
                    void* new_centroids, void* stream);
 
 /*
+ * The default first-round centroids of every segment, for per-step checking
+ * of the k-means initialisation (segmented spherical k-means: summaries
+ * de/fr/zh 2.A, fr 2.A.2; seeding is not stated there, and this build takes
+ * the first key of each stride-(seg_len/clusters_per_seg) block of the
+ * segment, steady positions included): centroids[u][s][j] =
+ * bf16(K[u][s*seg_len + j*stride] / |K[u][s*seg_len + j*stride]|), the
+ * centroids that wi_build_index uses when init_centroids is NULL.
+ * k: device bf16 keys as in wi_build_index (not modified); centroids: device
+ * bf16 [units][n_segments][clusters_per_seg][128].  Asynchronous on `stream`.
+ */
+int wi_init_centroids(const wi_config* cfg, const void* k, void* centroids, void* stream);
+
+/*
  * Per-kernel timing of decode steps (benchmarking aid).  After
  * wi_profile_begin(ix, max_steps), every decode step on this index records
  * CUDA events around each of its WI_NUM_DECODE_KERNELS kernels (centroid
@@ -227,9 +246,9 @@ int wi_profile_read(wi_index* ix, double* kernel_ms, int* steps, unsigned long l
  * exits.  Problems that need more scratch (about 340K tokens in total at 512
  * clusters per 8192-token segment) return WI_EINVAL with a message.
  * All calls share the array: calls whose work overlaps on the GPU race on it
- * (order them on one stream).  The first call on a device looks up the
- * array's device address with that device current.  Synchronises `stream`
- * before returning.
+ * (order them on one stream).  Every call looks up the array's device
+ * address with the caller's device current (no allocation), so a device
+ * reset between calls is harmless.  Synchronises `stream` before returning.
  */
 int wi_kmeans_step_noalloc(const wi_config* cfg, const void* k, const void* centroids, int32_t* assign,
                            void* new_centroids, void* stream);

@@ -116,6 +116,96 @@ def queries(w: Workload, step: int = 0, seed: int | None = None) -> np.ndarray:
     return q
 
 
+# ----------------------------------------------------------- on the GPU ----
+# kvsynth_cuda.cu: the same generator as CUDA kernels (same draws, transforms and rounding),
+# for caches too large to generate on the host.  Built by build_cuda(); needs a CUDA device.
+
+_CU_SRC = os.path.join(_HERE, "kvsynth_cuda.cu")
+_CU_LIB_PATH = os.path.join(_HERE, "libkvsynth_cuda.so")
+_cu_lib = None
+
+
+def build_cuda(force: bool = False) -> str:
+    """Compile ``kvsynth_cuda.cu`` into ``libkvsynth_cuda.so`` beside it (nvcc, sm_103a, no FMA
+    contraction so that every double operation rounds like the host build)."""
+    if force or not os.path.exists(_CU_LIB_PATH) or os.path.getmtime(_CU_LIB_PATH) < os.path.getmtime(_CU_SRC):
+        import shutil
+        nvcc = next((c for c in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc")
+                     if c and os.path.exists(c)), None)
+        if nvcc is None:
+            raise RuntimeError("nvcc not found")
+        tmp = _CU_LIB_PATH + f".tmp{os.getpid()}"
+        cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-fmad=false", "-Xcompiler", "-fPIC",
+               "-shared", "-o", tmp, _CU_SRC]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _CU_LIB_PATH)
+    return _CU_LIB_PATH
+
+
+def _load_cuda():
+    global _cu_lib
+    with _lock:
+        if _cu_lib is None:
+            lib = ctypes.CDLL(build_cuda())
+            vp = ctypes.c_void_p
+            pp = ctypes.POINTER(_Params)
+            lib.kvs_topics_dev.argtypes = [pp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp]
+            lib.kvs_cache_dev.argtypes = [pp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_long, ctypes.c_long,
+                                          vp, vp, vp, vp]
+            lib.kvs_queries_dev.argtypes = [pp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_long, ctypes.c_int, vp, vp, vp]
+            for f in (lib.kvs_topics_dev, lib.kvs_cache_dev, lib.kvs_queries_dev):
+                f.restype = ctypes.c_int
+            _cu_lib = lib
+    return _cu_lib
+
+
+class DeviceGen:
+    """The generator of one workload and seed on a CUDA device: topic centres computed once,
+    then key/value rows of any position range and the queries of any step, as int16 torch
+    tensors holding bf16 bits (same shapes as kv_cache / queries)."""
+
+    def __init__(self, w: Workload, seed: int | None = None, device="cuda", stream=None):
+        import torch
+        self.w, self.seed = w, (w.seed if seed is None else seed)
+        self.torch, self.device = torch, torch.device(device)
+        self.prm = _params(w, self.seed)
+        self.lib = _load_cuda()
+        self.topics = torch.empty((w.units, w.n_topics, w.head_dim), dtype=torch.float64, device=self.device)
+        self._call(self.lib.kvs_topics_dev, ctypes.byref(self.prm), w.batch, w.layers, w.n_kv_heads,
+                   self.topics.data_ptr(), self._stream(stream))
+
+    def _stream(self, stream):
+        torch = self.torch
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        return s.cuda_stream if isinstance(s, torch.cuda.Stream) else int(s)
+
+    @staticmethod
+    def _call(f, *args):
+        rc = f(*args)
+        if rc != 0:
+            raise RuntimeError(f"kvsynth (device): CUDA error {rc}")
+
+    def kv_cache(self, p0: int = 0, p1: int | None = None, out_k=None, out_v=None, stream=None):
+        w, torch = self.w, self.torch
+        p1 = w.n_ctx if p1 is None else p1
+        shape = (w.batch, w.layers, w.n_kv_heads, p1 - p0, w.head_dim)
+        k = torch.empty(shape, dtype=torch.int16, device=self.device) if out_k is None else out_k
+        v = torch.empty(shape, dtype=torch.int16, device=self.device) if out_v is None else out_v
+        assert tuple(k.shape) == shape and tuple(v.shape) == shape and k.is_contiguous() and v.is_contiguous()
+        self._call(self.lib.kvs_cache_dev, ctypes.byref(self.prm), w.batch, w.layers, w.n_kv_heads, p0, p1,
+                   self.topics.data_ptr(), k.data_ptr(), v.data_ptr(), self._stream(stream))
+        return k, v
+
+    def queries(self, step: int = 0, out=None, stream=None):
+        w, torch = self.w, self.torch
+        shape = (w.batch, w.layers, w.n_q_heads, w.head_dim)
+        q = torch.empty(shape, dtype=torch.int16, device=self.device) if out is None else out
+        self._call(self.lib.kvs_queries_dev, ctypes.byref(self.prm), w.batch, w.layers, w.n_q_heads, w.n_kv_heads,
+                   w.n_ctx + step, step, self.topics.data_ptr(), q.data_ptr(), self._stream(stream))
+        return q
+
+
 def bf16_bits(x: float) -> int:
     """The generator's own double -> bf16 rounding (used to pin it in tests)."""
     return int(_load().kvs_bf16(float(x)))

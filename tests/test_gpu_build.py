@@ -11,7 +11,7 @@ import torch
 
 import kvsynth
 import oracle
-from helpers import (assignment_from_index, bf16_ulp, compare_assignment, gen, params_of, small)
+from helpers import (assignment_from_index, bf16_ulp, compare_assignment, gen, near_tie, params_of, small)
 
 pytestmark = pytest.mark.gpu
 
@@ -201,3 +201,73 @@ def test_default_build_invariants_and_quality(wi):
     og, orf = objective(a_gpu), objective(ref[0]["assignment"])
     assert abs(og - orf) <= 0.01 * orf, (og, orf)
     ix.free()
+
+
+# ------------------------------------------------- B1 seeding, tie rule ----
+
+@pytest.mark.parametrize("shape", [dict(n_ctx=4096, seg_len=1024, clusters_per_seg=64),
+                                   dict(n_ctx=16384, seg_len=8192, clusters_per_seg=512),
+                                   dict(n_ctx=1536, seg_len=768, clusters_per_seg=48)])
+def test_default_seeds_match_oracle_init(wi, shape):
+    """k_init_centroids (the centroids of the first round when none are given) element by
+    element against oracle.init_centroids, within one bf16 step (fp32 vs float64 norm)."""
+    w = small(batch=2, layers=2, n_q_heads=4, n_kv_heads=2, iters=1, budget_k=4, seed=83, **shape)
+    k, v, q, K, V, Q = gen(w)
+    p = params_of(w)
+    cfg = wi.config_from_workload(w)
+    c = torch.empty((w.units, w.n_segments, w.clusters_per_seg, 128), dtype=torch.int16, device=DEV)
+    wi.wi_init_centroids(cfg, dev16(k), c)
+    torch.cuda.synchronize()
+    got = from16(c).reshape(w.units, w.n_segments, w.clusters_per_seg, 128)
+    ref = np.stack([np.stack([oracle.init_centroids(K[u][s * w.seg_len:(s + 1) * w.seg_len], p)
+                              for s in range(w.n_segments)]) for u in range(w.units)])
+    diff = np.abs(got - ref)
+    assert np.all(diff <= bf16_ulp(ref) * 1.0000001), diff.max()
+    assert np.mean(diff == 0) > 0.99   # rounding differences are rare
+    # and the default one-round build assigns by exactly those seeds
+    ix = wi.WaveIndex.build(cfg, dev16(k), dev16(v))
+    exp = ix.export()
+    torch.cuda.synchronize()
+    ix.check()
+    for u in range(w.units):
+        a_gpu = assignment_from_index(exp["counts"][u].cpu().numpy(), exp["perm"][u].cpu().numpy(), w.n_ctx,
+                                      w.n_sink)
+        a_ref = oracle.build_unit_index(K[u], V[u], p, iters=1)["assignment"]
+        dis = compare_assignment(a_gpu, a_ref, K[u], lambda s: ref[u, s], w.seg_len, w.clusters_per_seg)
+        assert dis <= 1e-3 * (w.n_ctx - w.n_sink - w.local_window)
+    ix.free()
+
+
+@pytest.mark.parametrize("cs,base,seg", [(512, 128, 1024), (256, 64, 1024), (64, 16, 1024), (48, 16, 768)])
+def test_assignment_ties_go_to_lowest_id_exactly(wi, cs, base, seg):
+    """Centroid j repeats centroid j mod `base`: every score has exact ties, across the
+    accumulator halves and column groups of the tensor-core epilogue (Cs = 512, 256) and in
+    the SIMT path (Cs = 48).  Every token must take the lowest id of its best centroid --
+    no near-tie excuse -- and equal the oracle (first maximum) wherever the best distinct
+    centroid leads by a relative 1e-5."""
+    w = small(batch=1, n_q_heads=1, n_kv_heads=1, n_ctx=2 * seg, seg_len=seg, clusters_per_seg=cs, iters=1,
+              budget_k=2, seed=84)
+    k, v, q, K, V, Q = gen(w)
+    p = params_of(w)
+    rng = np.random.default_rng(85)
+    distinct = oracle.bf16_round(rng.standard_normal((w.units, w.n_segments, base, 128)) / np.sqrt(128))
+    c = distinct[:, :, np.arange(cs) % base]
+    cfg = wi.config_from_workload(w)
+    assign = torch.empty((w.units, w.n_ctx), dtype=torch.int32, device=DEV)
+    new_c = torch.empty(c.shape, dtype=torch.int16, device=DEV)
+    wi.wi_kmeans_step(cfg, dev16(k), dev16(oracle.bf16_to_bits(c)), assign, new_c)
+    torch.cuda.synchronize()
+    a_gpu = assign.cpu().numpy().astype(np.int64)[0]
+    steady = oracle.steady_positions(w.n_ctx, p)
+    I = oracle.indexed_positions(w.n_ctx, p)
+    assert np.all(a_gpu[steady] == -1)
+    loc = a_gpu[I] - (I // w.seg_len) * cs
+    assert np.all((loc >= 0) & (loc < base)), "a tie went to a higher duplicate id"
+    for s in range(w.n_segments):
+        pos = I[I // w.seg_len == s]
+        a_ref = oracle.assign(K[0][pos], c[0, s])
+        assert np.all(a_ref < base)
+        gap = near_tie(K[0][pos], distinct[0, s])
+        firm = gap >= 1e-5
+        np.testing.assert_array_equal((a_gpu[pos] - s * cs)[firm], a_ref[firm])
+        assert firm.mean() > 0.99

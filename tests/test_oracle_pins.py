@@ -256,6 +256,70 @@ def test_planted_clusters_recovered():
     np.testing.assert_array_equal(a, label)
 
 
+def _axis_keys(norms, d=D):
+    """Keys norms[i] * e_i (exactly representable in bf16 for the norms used below)."""
+    k = np.zeros((len(norms), d))
+    for i, s in enumerate(norms):
+        k[i, i] = s
+    return k
+
+
+def test_update_sums_unit_vectors_hand_value():
+    """Spherical update (RetroInfer fr 2.A.2, spherical k-means): the new centroid is the
+    normalised sum of the members' UNIT vectors, rounded to bf16.
+
+    Members 3 e0, 0.5 e1, 2 e2 have unequal norms.  Their unit vectors sum to
+    (1, 1, 1), normalised 1/sqrt(3) = 0.57735... per coordinate, binary
+    0.10010011|1101...: eight significant bits round up to 0.10010100 = 148/256.
+    Two members 3 e0 and e1 give (1, 1)/sqrt(2) = 0.70710678... = 0.10110101|0000...,
+    which rounds down to 181/256.  A sum of the raw keys would give (3, .5, 2)/|.|
+    and (3, 1)/|.| instead."""
+    c_prev = oracle.bf16_round(np.random.default_rng(61).standard_normal((2, D)))
+    k3 = _axis_keys([3.0, 0.5, 2.0])
+    c = oracle.update(k3, np.zeros(3, np.int64), c_prev)
+    want = np.zeros(D)
+    want[:3] = 148.0 / 256.0
+    np.testing.assert_array_equal(c[0], want)
+    k2 = _axis_keys([3.0, 1.0])
+    c = oracle.update(k2, np.array([1, 1]), c_prev)
+    want = np.zeros(D)
+    want[:2] = 181.0 / 256.0
+    np.testing.assert_array_equal(c[1], want)
+
+
+def test_update_empty_cluster_keeps_previous_centroid():
+    """A cluster with no member keeps its centroid bit for bit (neither zeroed nor renormalised)."""
+    rng = np.random.default_rng(62)
+    c_prev = oracle.bf16_round(0.37 * rng.standard_normal((4, D)))   # deliberately not unit-norm
+    k = oracle.bf16_round(rng.standard_normal((5, D)))
+    a = np.array([0, 0, 3, 3, 0])
+    c = oracle.update(k, a, c_prev)
+    np.testing.assert_array_equal(c[1], c_prev[1])
+    np.testing.assert_array_equal(c[2], c_prev[2])
+    for j in (0, 3):   # members' unit vectors, summed and normalised (exact sum order is irrelevant at bf16)
+        u = sum(k[i] / np.linalg.norm(k[i]) for i in np.nonzero(a == j)[0])
+        np.testing.assert_array_equal(c[j], oracle.bf16_round(u / np.linalg.norm(u)))
+
+
+def test_kmeans_second_round_centroid_hand_value():
+    """Inside spherical_kmeans the second round's centroids come from the first round's
+    assignment by the same spherical update.  Segment of 4 keys 3 e0, 0.5 e1, 2 e2, 4 e3 and
+    2 clusters seeded at positions 0 and 2 (stride 2): centroids e0 and e2.  Key 3 e0 scores
+    (3, 0) and joins cluster 0; 0.5 e1 and 4 e3 score (0, 0), a tie that goes to the lowest
+    id, 0; 2 e2 scores (0, 2) and joins cluster 1.  Cluster 0 = {3 e0, 0.5 e1, 4 e3}: unit
+    sum e0 + e1 + e3, normalised 1/sqrt(3) -> 148/256 on those axes; cluster 1 = {2 e2}
+    -> e2 exactly."""
+    K = _axis_keys([3.0, 0.5, 2.0, 4.0])
+    p = IndexParams(seg_len=4, clusters_per_seg=2, iters=2, n_sink=0, local_window=0)
+    a, hist = oracle.spherical_kmeans(K, np.arange(4), p)
+    e = np.eye(D)
+    np.testing.assert_array_equal(hist[0], np.stack([e[0], e[2]]))
+    want0 = np.zeros(D)
+    want0[[0, 1, 3]] = 148.0 / 256.0
+    np.testing.assert_array_equal(hist[1][0], want0)
+    np.testing.assert_array_equal(hist[1][1], e[2])
+
+
 def test_kmeans_objective_non_decreasing():
     w = tiny_workload(n=2048, S=2048, Cs=64, iters=8)
     K, V, _ = gen_unit(w)
