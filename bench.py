@@ -1,28 +1,39 @@
 #!/usr/bin/env python
 """Wave-index decode benchmark (one JSON line on rank 0).
 
-Workload: the Llama-3-8B-shaped single-layer decode -- 131072 tokens, 32 query
-heads over 8 kv heads, head size 128, bf16 KV, 16 segments x 512 clusters per
-kv head, retrieval budget 148 clusters (1.8%), steady zone 4 + 64 tokens --
-on seeded synthetic data (kvsynth).  A step is one decode step of the whole
-batch: centroid scoring with the fused estimation, top-k, union, exact
-attention over steady + retrieved rows, LSE merge.
+Main line: the Llama-3-8B-shaped single-layer decode -- 131072 tokens, 32
+query heads over 8 kv heads, head size 128, bf16 KV, 16 segments x 512
+clusters per kv head, retrieval budget 148 clusters (1.8%), steady zone 4 + 64
+tokens -- on seeded synthetic data (kvsynth).  A step is one decode step of the
+whole batch: centroid scoring, top-k with the estimation over all clusters,
+exact attention over steady + retrieved rows, LSE merge.
 
-Timing: the decode steps are captured in CUDA graphs and replayed; each
-step runs on one of R independent index + KV replicas in turn (R x ~90 MB
-of index and retrieved rows per step, 4.7 GB of replicas in total, far above
-the 129 MB L2), with a different query per step.  Kernel durations come from
-CUDA events that the library records around each kernel on the launching
-stream inside the same timed region.
+Timing: the decode steps are captured in CUDA graphs and replayed (every graph
+is replayed once untimed first); each step runs on one of R independent index +
+KV replicas in turn (4.7 GB of replicas in total, far above the 129 MB L2),
+with a different query per step.  Each decode kernel is also timed alone: a
+graph of launches of that kernel only (wi_decode_kernel), over the same
+rotating replicas, gives its average launch duration without events between
+kernels; the roofline of the line is the longest of those kernels.
+
+`configs` adds the other workloads at full size, generated on the device
+(kvsynth_cuda): batch 16 at 120K tokens, one million tokens across 32 layers,
+and the Qwen2.5-7B-shaped batch 8 at 262K tokens (its index build and 64
+decode steps that each append a token).  Each gets steps/s, its step's
+algorithmic bytes and HBM rate, its kernels alone, its build, and the dense
+comparator.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
 from __future__ import annotations
 
 import argparse
+import glob
+import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -207,10 +218,35 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of the
-# current kernels on this workload (profiles/decode_kernels_llama3-8b-131k.md); to be retaken whenever
-# a kernel changes.
-NCU_TRAFFIC = {("llama3-8b-131k", "exact_merge"): 38_799_104 + 20_992}
+CSRC = os.path.join(ROOT, "clustered_sparse_kv_gb300", "csrc")
+DECODE_SOURCES = ["wi_decode.cu", "wi_pipe.cuh", "wi_tc.cuh", "wi_common.cuh", "wi_internal.h"]
+KERNEL_NAMES = {"scores": "k_scores", "select_estimate": "k_select_estimate", "exact_merge": "k_exact_merge"}
+EXTRA_CONFIGS = ["llama3-8b-b16-120k", "llama3-8b-1m-32l", "qwen2.5-7b-b8-262k"]
+
+
+def decode_source_hash() -> str:
+    """Hash of the decode kernels' sources: names the build that an ncu capture measured."""
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+_TRAFFIC_RE = re.compile(r"traffic: kernel=(\S+) workload=(\S+) source=([0-9a-f]{16}) dram_bytes_per_launch=(\d+)")
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of `kernel` on
+    `workload`, from a `traffic:` line of an ncu summary under profiles/ that was captured from
+    the current decode sources (same hash); None when no capture matches them."""
+    want = decode_source_hash()
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        with open(path) as f:
+            for m in _TRAFFIC_RE.finditer(f.read()):
+                if m.group(1) == kernel and m.group(2) == workload and m.group(3) == want:
+                    return int(m.group(4))
+    return None
 
 
 def rank_seed(w, rank):
@@ -233,28 +269,286 @@ def job_value(world, steps, batch, layers, seconds):
     return world * steps * batch * layers / seconds
 
 
-def profile_run(wi, torch, w, dev, steps, dense=False):
+def profile_run(wi, torch, w, dev, steps, dense=False, device_gen=False):
     """One index of the workload and `steps` decode steps (each followed by a dense comparator step
-    if asked), nothing timed."""
-    k, v = kvsynth.kv_cache(w)
-    kd = torch.from_numpy(k.view(np.int16)).to(dev)
-    vd = torch.from_numpy(v.view(np.int16)).to(dev)
+    if asked), nothing timed: the small case of the ncu captures."""
+    if device_gen:
+        g = kvsynth.DeviceGen(w, device=dev)
+        kd, vd = g.kv_cache()
+        qs = [g.queries(s) for s in range(steps)]
+    else:
+        k, v = kvsynth.kv_cache(w)
+        kd = torch.from_numpy(k.view(np.int16)).to(dev)
+        vd = torch.from_numpy(v.view(np.int16)).to(dev)
+        qs = [torch.from_numpy(kvsynth.queries(w, step=s).view(np.int16)).to(dev) for s in range(steps)]
     ix = wi.WaveIndex.build(wi.config_from_workload(w), kd, vd)
     for s in range(steps):
-        q = torch.from_numpy(kvsynth.queries(w, step=s).view(np.int16)).to(dev)
-        ix.decode(q)
+        ix.decode(qs[s])
         if dense:
-            ix.dense_decode(q)
+            ix.dense_decode(qs[s])
     torch.cuda.synchronize()
     ix.check()
     ix.free()
     print(json.dumps({"profile_steps": steps, "workload": w.name}), flush=True)
 
 
+class Timer:
+    """CUDA-graph replays timed with CUDA events on one stream (the stream the library launches on)."""
+
+    def __init__(self, torch, stream):
+        self.torch, self.stream = torch, stream
+
+    def graph(self, fn, n):
+        g = self.torch.cuda.CUDAGraph()
+        with self.torch.cuda.graph(g, stream=self.stream):
+            for s in range(n):
+                fn(s)
+        return g
+
+    def replay(self, graphs):
+        """Replay `graphs` in order between two events; milliseconds."""
+        torch = self.torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            for g in graphs:
+                g.replay()
+            e1.record(self.stream)
+        self.stream.synchronize()
+        return e0.elapsed_time(e1)
+
+    def steps_plan(self, fn, steps, chunk):
+        """Graphs covering exactly `steps` calls of fn (chunks of `chunk`), each replayed once untimed."""
+        full, rest = divmod(steps, chunk)
+        g_full = self.graph(fn, chunk) if full else None
+        g_rest = self.graph(lambda s: fn(full * chunk + s), rest) if rest else None
+        for g in (g_full, g_rest):
+            if g is not None:
+                self.replay([g])
+        return [g_full] * full + ([g_rest] if g_rest is not None else [])
+
+
+def algorithmic_bytes(w, vs_bytes, exact_rows_per_step, union_fraction):
+    """Algorithmic bytes per launch of each decode kernel (index and K/V bytes the method must read;
+    scratch traffic excluded), and per step (plus queries in and outputs out)."""
+    cand = {"scores": w.units * w.clusters * (128 * 2 + 4),                  # mean keys + counts
+            "select_estimate": w.units * w.clusters * (128 * vs_bytes + 4),   # value sums + counts
+            "exact_merge": exact_rows_per_step * union_fraction * ROW_BYTES}   # GQA union of the rows
+    step = sum(cand.values()) + w.units * w.group * 128 * (2 + 4)
+    return cand, step
+
+
+def union_fraction(replicas, w):
+    """Rows in the union over each kv head's query heads / rows the heads select one by one
+    (last step of every replica; steady rows counted once per head in both)."""
+    loaded = union = 0
+    steady = w.n_sink + w.local_window
+    for ix in replicas:
+        ids, _ = ix.selection()
+        counts = np.empty((ix.units, ix.clusters), np.int32)
+        import clustered_sparse_kv_gb300 as wi
+        wi.wi_index_export(ix.handle, counts=counts)
+        ids = ids.cpu().numpy()
+        for uu in range(w.units):
+            per_head = [ids[uu, hh][ids[uu, hh] >= 0] for hh in range(w.group)]
+            loaded += sum(int(counts[uu][sel].sum()) + steady for sel in per_head)
+            union += int(counts[uu][np.unique(np.concatenate(per_head))].sum()) + steady
+    return union / max(loaded, 1)
+
+
+def measure_decode(wi, torch, timer, w, replicas, qs, outs, steps, chunk, vs_bytes, iso_replays=3):
+    """Decode steps over rotating replicas, and each decode kernel alone.  Returns a dict of
+    timings and algorithmic bytes; the graphs of the timed region are returned to be replayed
+    again (clock sampling) by the caller."""
+    R, L = len(replicas), len(qs)
+    stream = timer.stream
+
+    def step(s):
+        replicas[s % R].decode(qs[s % L], out=outs[s % R], stream=stream)
+
+    graphs = timer.steps_plan(step, steps, chunk)
+    rows1 = sum(wi.wi_profile_read(ix.handle, times=False)[2] for ix in replicas)   # warm replays counted
+    ms = timer.replay(graphs)
+    rows2 = sum(wi.wi_profile_read(ix.handle, times=False)[2] for ix in replicas)
+    for ix in replicas:
+        ix.check()
+    rows_per_step = (rows2 - rows1) / max(steps, 1)
+    # each kernel alone: a graph of `chunk` launches of that kernel over the same replicas (each repeats
+    # its part of the replica's last step)
+    iso = {}
+    for kid, name in enumerate(wi.DECODE_KERNELS):
+        g = timer.graph(lambda s: wi.wi_decode_kernel(replicas[s % R].handle, kid, qs[s % L], outs[s % R], stream),
+                        chunk)
+        timer.replay([g])
+        t = timer.replay([g] * iso_replays)
+        iso[name] = 1e3 * t / (iso_replays * chunk)
+    for ix in replicas:
+        ix.check()
+    uf = union_fraction(replicas, w)
+    cand, step_bytes = algorithmic_bytes(w, vs_bytes, rows_per_step, uf)
+    return {"ms": ms, "graphs": graphs, "kernels_us": iso, "rows_per_step": rows_per_step, "union": uf,
+            "bytes": cand, "step_bytes": step_bytes}
+
+
+def roofline_of(d, w, hbm, peak_kind):
+    """Roofline of the dominant decode kernel (the longest alone): algorithmic bytes per launch
+    over its average launch duration, against the measured HBM peak."""
+    iso = d["kernels_us"]
+    dom = max(iso, key=iso.get)
+    achieved = d["bytes"][dom] / (iso[dom] * 1e-6) / 1e9 if iso[dom] > 0 else 0.0
+    return {"bound": "hbm", "kernel": KERNEL_NAMES[dom], "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "peak_kind": peak_kind, "bytes_per_launch": d["bytes"][dom],
+            "duration_us": iso[dom], "duration": "the kernel alone: graph of its launches, CUDA events",
+            "traffic": ncu_traffic(KERNEL_NAMES[dom], w.name), "source": decode_source_hash()}
+
+
+def build_record(wi, ix, w, secs, tf_peak, peak_kind):
+    st_ = wi.wi_index_build_stats(ix.handle)
+    n_idx = w.n_ctx - w.n_sink - w.local_window
+    flops = 2.0 * w.iters * w.units * n_idx * w.clusters_per_seg * 128
+    assign_s = st_["assign_ms"] / 1e3
+    tf = flops / assign_s / 1e12
+    return {"seconds": secs, "segment_units_per_s": w.units * w.n_segments / secs, "assign_flop": flops,
+            "assign_seconds": assign_s, "assign_launches": st_["assign_launches"], "assign_tflops": tf,
+            "assign_roofline": {"bound": "tensor", "achieved": tf, "peak": tf_peak, "unit": "TFLOP/s",
+                                "frac": tf / tf_peak, "peak_kind": peak_kind},
+            "assign_tflops_over_build": flops / secs / 1e12,
+            "build_frac_of_tensor_peak": flops / secs / 1e12 / tf_peak}
+
+
+def timed_build(wi, torch, cfg, k, v, stream):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        ix = wi.WaveIndex.build(cfg, k, v, stream=stream)
+        e1.record(stream)
+    stream.synchronize()
+    ix.check()
+    return ix, e0.elapsed_time(e1) / 1e3
+
+
+def dense_record(wi, torch, timer, w, replicas, qs, outs, steps, chunk, hbm, peak_kind, wave_ms):
+    """The dense comparator (full attention over every cached token) on the same replicas and queries."""
+    R, L = len(replicas), len(qs)
+    stream = timer.stream
+    n = max(1, min(chunk, steps))
+    g = timer.graph(lambda s: replicas[s % R].dense_decode(qs[s % L], out=outs[s % R], stream=stream), n)
+    timer.replay([g])
+    reps = max(1, steps // n)
+    d_ms = timer.replay([g] * reps) / (reps * n)
+    for ix in replicas:
+        ix.check()
+    d_bytes = w.units * w.n_ctx * ROW_BYTES + w.units * w.group * 128 * (2 + 4)
+    d_gbs = d_bytes / (d_ms * 1e-3) / 1e9
+    return {"kernel": "k_dense_decode", "steps": reps * n, "ms_per_step": d_ms,
+            "value": w.batch * w.layers / (d_ms / 1e3), "unit": UNIT, "bytes_per_step": d_bytes,
+            "hbm_gbs": d_gbs, "peak": hbm, "frac": d_gbs / hbm, "peak_kind": peak_kind,
+            "wave_index_speedup": d_ms / wave_ms}
+
+
+def measure_config(wi, torch, timer, name, dev, hbm, tf_burst, peak_kind, steps, dense_steps):
+    """Full-size record of one more workload, generated on the device: build, decode steps, kernels
+    alone, dense comparator, and (append workloads) the decode steps that append a token."""
+    w = kvsynth.get_workload(name)
+    stream = timer.stream
+    t0 = time.perf_counter()
+    gen = kvsynth.DeviceGen(w, device=dev, stream=stream)
+    k, v = gen.kv_cache(stream=stream)
+    stream.synchronize()
+    gen_s = time.perf_counter() - t0
+    cfg = wi.config_from_workload(w)
+    ix, build_s = timed_build(wi, torch, cfg, k, v, stream)
+    build = build_record(wi, ix, w, build_s, tf_burst, peak_kind)
+    L = min(32, steps)
+    qs = [gen.queries(s, stream=stream) for s in range(L)]
+    out = torch.empty((w.batch, w.layers, w.n_q_heads, 128), dtype=torch.float32, device=dev)
+    for s in range(3):
+        ix.decode(qs[s], out=out, stream=stream)
+    stream.synchronize()
+    ix.check()
+    d = measure_decode(wi, torch, timer, w, [ix], qs, [out], steps, L, 4, iso_replays=2)
+    ms_per_step = d["ms"] / steps
+    rec = {"workload": w.name, "batch": w.batch, "layers": w.layers, "n_q_heads": w.n_q_heads,
+           "n_kv_heads": w.n_kv_heads, "n_ctx": w.n_ctx, "units": w.units, "clusters": w.clusters,
+           "k": ix.k_max, "steps": steps, "ms_per_step": ms_per_step, "steps_per_s": 1e3 / ms_per_step,
+           "value": w.batch * w.layers * 1e3 / ms_per_step, "unit": "steps/s (batch×layer)",
+           "step_bytes": d["step_bytes"], "step_hbm_gbs": d["step_bytes"] / (ms_per_step * 1e-3) / 1e9,
+           "kernels_us_alone": d["kernels_us"], "roofline": roofline_of(d, w, hbm, peak_kind),
+           "exact_rows_per_step": d["rows_per_step"], "exact_union_fraction": d["union"],
+           "decode_layout": wi.wi_decode_layout(ix.handle), "generate_s": gen_s,
+           "l2": f"one replica: {d['step_bytes'] / 1e9:.2f} GB per step, far above L2", "build": build}
+    rec["step_frac"] = rec["step_hbm_gbs"] / hbm
+    if dense_steps > 0:
+        rec["dense_comparator"] = dense_record(wi, torch, timer, w, [ix], qs, [out], dense_steps, 8, hbm,
+                                               peak_kind, ms_per_step)
+    ix.free()
+    if w.append and w.decode_steps > 0:
+        # the workload's decode on a fresh build: every step attends, then appends its token (not
+        # graph-replayable: the append slot advances), launched step by step, timed with events
+        T = w.decode_steps
+        ka, va = gen.kv_cache(p0=w.n_ctx, p1=w.n_ctx + T, stream=stream)
+        kn = [ka[:, :, :, t].contiguous() for t in range(T)]
+        vn = [va[:, :, :, t].contiguous() for t in range(T)]
+        qa = [gen.queries(t, stream=stream) for t in range(T)]
+        gen.kv_cache(out_k=k, out_v=v, stream=stream)   # the unpermuted cache again
+        ix2, _ = timed_build(wi, torch, cfg, k, v, stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for t in range(T):
+                ix2.decode(qa[t], kn[t], vn[t], out=out, stream=stream)
+            e1.record(stream)
+        stream.synchronize()
+        ix2.check()
+        a_ms = e0.elapsed_time(e1) / T
+        rec["append"] = {"steps": T, "ms_per_step": a_ms, "steps_per_s": 1e3 / a_ms,
+                         "value": w.batch * w.layers * 1e3 / a_ms,
+                         "timing": f"{T} steps launched one by one (each appends its token), CUDA events"}
+        ix2.free()
+    del k, v, gen
+    torch.cuda.empty_cache()
+    return rec
+
+
+def variant_accuracy(wi, torch, w, k_dev, v_dev, qs, dev, stream):
+    """Relative L2 of the wave-index output against full attention (the dense comparator, itself
+    checked against the float64 definition by the tests) per (unit, query head), for the default
+    index and its two variants: information only."""
+    res = {}
+    for name, vsb, grp in (("default", 0, 0), ("valsum_bf16", 1, 0), ("group_topk", 0, 1)):
+        cfg = wi.config_from_workload(w)
+        cfg.valsum_bf16, cfg.group_topk = vsb, grp
+        ix = wi.WaveIndex.build(cfg, k_dev.clone(), v_dev.clone(), stream=stream)
+        errs = []
+        for q in qs:
+            o = ix.decode(q, stream=stream)
+            r = ix.dense_decode(q, stream=stream)
+            stream.synchronize()
+            o64 = o.double().reshape(-1, 128)
+            r64 = r.double().reshape(-1, 128)
+            errs.append((torch.linalg.norm(o64 - r64, dim=1) / torch.linalg.norm(r64, dim=1)).cpu().numpy())
+        ix.check()
+        ix.free()
+        e = np.concatenate(errs)
+        res[name] = {"rel_l2_mean": float(e.mean()), "rel_l2_max": float(e.max()), "samples": int(e.size)}
+    return res
+
+
+def spawn_ranks(n):
+    """--gpus N without a launcher: run this script under torch.distributed.run with N ranks."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
@@ -263,13 +557,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-build-timing", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=2000)
-    ap.add_argument("--no-kernel-events", action="store_true",
-                    help="do not record per-kernel events inside the timed region (value only)")
+    ap.add_argument("--configs", default=",".join(EXTRA_CONFIGS),
+                    help="comma-separated further workloads measured at full size (empty: none)")
+    ap.add_argument("--config-steps", type=int, default=256, help="decode steps timed per further workload")
+    ap.add_argument("--no-accuracy", action="store_true", help="skip the variant accuracy record")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="profiling run: build one index of the workload, run this many decode steps, "
                          "print nothing else (a small case for ncu captures)")
     ap.add_argument("--profile-dense", action="store_true",
                     help="with --profile-steps: also run the dense comparator after every decode step")
+    ap.add_argument("--profile-device-gen", action="store_true",
+                    help="with --profile-steps: generate the workload on the device")
     ap.add_argument("--valsum-bf16", action="store_true",
                     help="the index variant whose decode reads a bf16 copy of the value sums")
     ap.add_argument("--group-topk", action="store_true",
@@ -278,9 +576,13 @@ def main():
                     help="dense comparator steps timed after the wave-index region (0: skip)")
     args = ap.parse_args()
 
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(spawn_ranks(args.gpus))
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}")
     w = kvsynth.get_workload(args.workload)
 
     if args.impl == "reference":
@@ -304,8 +606,10 @@ def main():
 
     seed = rank_seed(w, rank)
     if args.profile_steps > 0:
-        profile_run(wi, torch, w, dev, args.profile_steps, dense=args.profile_dense)
+        profile_run(wi, torch, w, dev, args.profile_steps, dense=args.profile_dense,
+                    device_gen=args.profile_device_gen)
         return
+    hbm, tf_burst, tf_sust, peak_kind = peaks()
     k, v = kvsynth.kv_cache(w, seed=seed)
     k_dev = torch.from_numpy(k.view(np.int16)).to(dev)
     v_dev = torch.from_numpy(v.view(np.int16)).to(dev)
@@ -315,134 +619,46 @@ def main():
     vs_bytes = 2 if args.valsum_bf16 else 4
     R = args.replicas
     stream = torch.cuda.Stream(device=dev)
+    timer = Timer(torch, stream)
     replicas = []
     build = None
-    with torch.cuda.stream(stream):
-        for r in range(R):
-            kr, vr = k_dev.clone(), v_dev.clone()
-            stream.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            ix = wi.WaveIndex.build(cfg, kr, vr, stream=stream)
-            e1.record(stream)
-            stream.synchronize()
-            ix.check()
-            if r == 1 and not args.no_build_timing:   # replica 0 is the warm-up build
-                secs = e0.elapsed_time(e1) / 1e3
-                st_ = wi.wi_index_build_stats(ix.handle)
-                n_idx = w.n_ctx - w.n_sink - w.local_window
-                flops = 2.0 * w.iters * w.units * n_idx * w.clusters_per_seg * 128
-                assign_s = st_["assign_ms"] / 1e3
-                tf = flops / assign_s / 1e12
-                build = {"seconds": secs, "segment_units_per_s": w.units * w.n_segments / secs,
-                         "assign_flop": flops, "assign_seconds": assign_s,
-                         "assign_launches": st_["assign_launches"], "assign_tflops": tf,
-                         "assign_roofline": {"bound": "tensor", "achieved": tf, "peak": peaks()[1],
-                                             "unit": "TFLOP/s", "frac": tf / peaks()[1],
-                                             "peak_kind": peaks()[3]},
-                         "assign_tflops_over_build": flops / secs / 1e12}
-            replicas.append(ix)
-    del k_dev, v_dev
+    for r in range(R):
+        ix, secs = timed_build(wi, torch, cfg, k_dev.clone(), v_dev.clone(), stream)
+        if r == 1 and not args.no_build_timing:   # replica 0 is the warm-up build
+            build = build_record(wi, ix, w, secs, tf_burst, peak_kind)
+        replicas.append(ix)
 
     # queries: one per step of a chunk, resident on the device before timing
     L = args.chunk
     qs = [torch.from_numpy(kvsynth.queries(w, step=s, seed=seed).view(np.int16)).to(dev) for s in range(L)]
     outs = [torch.empty((w.batch, w.layers, w.n_q_heads, 128), dtype=torch.float32, device=dev) for _ in range(R)]
-
     with torch.cuda.stream(stream):
         for s in range(max(args.warmup, 3)):
             replicas[s % R].decode(qs[s % L], out=outs[s % R], stream=stream)
         stream.synchronize()
-        for ix in replicas:
-            ix.check()
-
-    K = args.steps
-    full, rest = divmod(K, L)
-
-    def capture(nsteps):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for s in range(nsteps):
-                replicas[s % R].decode(qs[s], out=outs[s % R], stream=stream)
-        return g
-
-    def run_region(g_full, g_rest):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(full):
-                g_full.replay()
-            if g_rest is not None:
-                g_rest.replay()
-            e1.record(stream)
-        stream.synchronize()
-        return e0.elapsed_time(e1)
-
-    # graphs without per-kernel events: the timed region of `value`
-    g_full = capture(L) if full else None
-    g_rest = capture(rest) if rest else None
-    # graphs with per-kernel events recorded by the library: kernel durations (a second region)
-    gk_full = gk_rest = None
-    if not args.no_kernel_events:
-        for ix in replicas:
-            wi.wi_profile_begin(ix.handle, max(1, math.ceil(L / R)))
-        gk_full = capture(L) if full else None
-        gk_rest = capture(rest) if rest else None
-    stream.synchronize()
-    rows0 = [wi.wi_profile_read(ix.handle, times=False)[2] for ix in replicas]
-
-    barrier()
-    with ClockSampler(local) as clocks:
-        ms = run_region(g_full, g_rest)
-    barrier()
-    ms = max_over_ranks(ms, dist, dev)
     for ix in replicas:
         ix.check()
-    ms_events = None
-    if gk_full is not None or gk_rest is not None:
-        rows0 = [wi.wi_profile_read(ix.handle, times=False)[2] for ix in replicas]
-        ms_events = run_region(gk_full, gk_rest)
 
-    # per-kernel durations (events recorded by the library in the timed region)
-    kern_ms = {n: 0.0 for n in wi.DECODE_KERNELS}
-    kern_steps = 0
-    rows = 0
-    for ix, r0 in zip(replicas, rows0):
-        d, st, rr = wi.wi_profile_read(ix.handle)
-        for n in kern_ms:
-            kern_ms[n] += d[n]
-        kern_steps += st
-        rows += rr - r0
-    mean_us = {n: 1e3 * kern_ms[n] / max(kern_steps, 1) for n in kern_ms}
-    rows_per_step = rows / max(K, 1)          # rows loaded by exact attention, per query head
-    # the algorithmic exact-zone bytes count each row once per kv head (union over the group's heads);
-    # measure the union / per-head ratio on each replica's last step
-    loaded = union = 0
-    for ix in replicas:
-        ids, _ = ix.selection()
-        counts = ix.export()["counts"]
-        ids, counts = ids.cpu().numpy(), counts.cpu().numpy()
-        steady = w.n_sink + w.local_window
-        for uu in range(w.units):
-            per_head = [ids[uu, hh][ids[uu, hh] >= 0] for hh in range(w.group)]
-            loaded += sum(int(counts[uu][sel].sum()) + steady for sel in per_head)
-            union += int(counts[uu][np.unique(np.concatenate(per_head))].sum()) + steady
-    dedup = union / max(loaded, 1)
-    hbm, tf_burst, tf_sust, peak_kind = peaks()
-    bytes_d1 = w.units * w.clusters * (INDEX_BYTES_PER_CLUSTER - 128 * (4 - vs_bytes))
-    bytes_d3 = rows_per_step * dedup * ROW_BYTES
-    cand = {"scores": w.units * w.clusters * (128 * 2 + 4),              # mu + count
-            "select_estimate": w.units * w.clusters * (128 * vs_bytes + 4),  # value sums + count
-            "exact_merge": bytes_d3}
-    dom = max(cand, key=lambda n: mean_us[n])
-    achieved = cand[dom] / (mean_us[dom] * 1e-6) / 1e9 if mean_us[dom] > 0 else 0.0
-    step_bytes = bytes_d1 + bytes_d3 + w.units * w.group * 128 * (2 + 4)
+    K = args.steps
+    barrier()
+    d = measure_decode(wi, torch, timer, w, replicas, qs, outs, K, L, vs_bytes)
+    barrier()
+    ms = max_over_ranks(d["ms"], dist, dev)
+    # clocks under the same load: the timed graphs replayed for ~1.6 s (another thread) while the
+    # sampler runs inside that window
+    import threading
+    soak = max(1, int(math.ceil(1.6 / max(d["ms"] / 1e3, 1e-6))))
+    th = threading.Thread(target=timer.replay, args=(d["graphs"] * soak,))
+    th.start()
+    time.sleep(0.05)
+    with ClockSampler(local) as clocks:
+        time.sleep(0.8)
+    th.join()
     ms_per_step = ms / K
     value = job_value(world, K, w.batch, w.layers, ms / 1e3)
+    step_bytes = d["step_bytes"]
 
     # e2e: host buffers through the C ABI, copies inside the timed region
-    for ix in replicas:
-        wi.wi_profile_begin(ix.handle, 0)
     qh = [torch.from_numpy(kvsynth.queries(w, step=L + s, seed=seed).view(np.int16)).pin_memory()
           for s in range(8)]
     oh = torch.empty((w.batch, w.layers, w.n_q_heads, 128), dtype=torch.float32).pin_memory()
@@ -463,77 +679,75 @@ def main():
     for ix in replicas:
         ix.check()
 
-    # the dense comparator (full attention over every cached token) on the same replicas and queries:
-    # graphs of L steps, CUDA events on the launching stream, after the wave-index regions
     dense = None
     if args.dense_steps > 0:
-        with torch.cuda.stream(stream):
-            for s in range(3):
-                replicas[s % R].dense_decode(qs[s % L], out=outs[s % R], stream=stream)
-            stream.synchronize()
-            gd = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gd, stream=stream):
-                for s in range(L):
-                    replicas[s % R].dense_decode(qs[s], out=outs[s % R], stream=stream)
-            nd = max(1, args.dense_steps // L)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(nd):
-                gd.replay()
-            e1.record(stream)
-        stream.synchronize()
-        for ix in replicas:
-            ix.check()
-        d_ms = max_over_ranks(e0.elapsed_time(e1) / (nd * L), dist, dev)
-        d_bytes = w.units * w.n_ctx * ROW_BYTES + w.units * w.group * 128 * (2 + 4)
-        d_gbs = d_bytes / (d_ms * 1e-3) / 1e9
-        dense = {"kernel": "k_dense_decode", "steps": nd * L, "ms_per_step": d_ms,
-                 "value": job_value(world, 1, w.batch, w.layers, d_ms / 1e3), "unit": UNIT,
-                 "bytes_per_step": d_bytes, "hbm_gbs": d_gbs, "peak": hbm, "frac": d_gbs / hbm,
-                 "peak_kind": peak_kind, "wave_index_speedup": d_ms / ms_per_step}
+        dense = dense_record(wi, torch, timer, w, replicas, qs, outs, args.dense_steps, L, hbm, peak_kind,
+                             ms_per_step)
+
+    accuracy = None
+    if rank == 0 and world == 1 and not args.no_accuracy:
+        accuracy = variant_accuracy(wi, torch, w, k_dev, v_dev, qs[:4], dev, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, k, v)
 
+    line_cfg = {"workload": w.name, "batch": w.batch, "layers": w.layers, "n_q_heads": w.n_q_heads,
+                "n_kv_heads": w.n_kv_heads, "head_dim": 128, "n_ctx": w.n_ctx, "seg_len": w.seg_len,
+                "clusters_per_seg": w.clusters_per_seg, "clusters": w.clusters,
+                "k": replicas[0].k_max, "steady": w.n_sink + w.local_window,
+                "l2": f"inputs larger than L2: {R} rotating index+KV replicas "
+                      f"({R * (w.units * w.n_ctx * 512 + d['bytes']['scores'] + d['bytes']['select_estimate']) / 1e9:.1f} GB)",
+                "timing": f"CUDA graphs of {L} steps replayed (each once untimed first); events on the "
+                          f"launching stream",
+                "decode_layout": wi.wi_decode_layout(replicas[0].handle),
+                "valsum": "bf16" if args.valsum_bf16 else "fp32",
+                "retrieval": "per kv head (summed scores)" if args.group_topk else "per query head"}
+    for ix in replicas:
+        ix.free()
+    replicas = []
+    del k_dev, v_dev
+    torch.cuda.empty_cache()
+
+    configs = []
+    names = [c for c in args.configs.split(",") if c] if world == 1 else []
+    for name in names:
+        if name == w.name:
+            continue
+        steps_c = args.config_steps if name != "llama3-8b-1m-32l" else max(8, args.config_steps // 8)
+        configs.append(measure_config(wi, torch, timer, name, dev, hbm, tf_burst, peak_kind, steps_c,
+                                      dense_steps=16 if args.dense_steps > 0 else 0))
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-            "ms_per_step": ms_per_step, "ms_per_step_with_kernel_events": (ms_events / K if ms_events else None),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "accumulate": "fp32", "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch, "layers": w.layers, "n_q_heads": w.n_q_heads,
-                       "n_kv_heads": w.n_kv_heads, "head_dim": 128, "n_ctx": w.n_ctx, "seg_len": w.seg_len,
-                       "clusters_per_seg": w.clusters_per_seg, "clusters": w.clusters,
-                       "k": replicas[0].k_max, "steady": w.n_sink + w.local_window,
-                       "l2": f"inputs larger than L2: {R} rotating index+KV replicas "
-                             f"({R * (w.units * w.n_ctx * 512 + bytes_d1) / 1e9:.1f} GB)",
-                       "timing": f"CUDA graphs of {L} steps replayed; events on the launching stream",
-                       "decode_layout": wi.wi_decode_layout(replicas[0].handle),
-                       "valsum": "bf16" if args.valsum_bf16 else "fp32",
-                       "retrieval": "per kv head (summed scores)" if args.group_topk else "per query head"},
-            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "peak_kind": peak_kind,
-                         "bytes_per_launch": cand[dom], "traffic": NCU_TRAFFIC.get((w.name, dom))},
+            "config": line_cfg,
+            "roofline": roofline_of(d, w, hbm, peak_kind),
             "step_hbm_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
+            "step_frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / hbm,
             "step_bytes": step_bytes,
-            "exact_rows_per_step": rows_per_step,
-            "exact_union_fraction": dedup,
-            "kernels_us": mean_us,
+            "exact_rows_per_step": d["rows_per_step"],
+            "exact_union_fraction": d["union"],
+            "kernels_us_alone": d["kernels_us"],
             "gpu_launches": K * wi.WI_NUM_DECODE_KERNELS,
             "e2e": {"value": e2e_val, "unit": UNIT, "steps": E,
                     "h2d_bytes_per_step": w.units * w.group * 128 * 2,
                     "d2h_bytes_per_step": w.units * w.group * 128 * 4},
             "cpu_baseline": cpu,
-            "clocks": clocks.summary(),
+            "clocks": dict(clocks.summary(), window="nvidia-smi every 100 ms while the timed graphs are "
+                                                    "replayed for ~1.6 s right after the timed region"),
         }
         if build is not None:
             line["build"] = build
         if dense is not None:
             line["dense_comparator"] = dense
+        if accuracy is not None:
+            line["variant_accuracy"] = accuracy
+        if configs:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
-    for ix in replicas:
-        ix.free()
     if dist is not None:
         dist.destroy_process_group()
 

@@ -57,6 +57,7 @@ _SIGS = {
     "wi_decode_step": [_vp, _vp, _vp, _vp, _vp, _vp],
     "wi_decode_step_host": [_vp, _vp, _vp, _vp, _vp, _vp],
     "wi_dense_decode": [_vp, _vp, _vp, _vp],
+    "wi_decode_kernel": [_vp, ctypes.c_int, _vp, _vp, _vp],
     "wi_last_selection": [_vp, _vp, _vp, _vp],
     "wi_index_shape": [_vp, _ip, _ip, _ip, _ip, _ip],
     "wi_decode_layout": [_vp, _ip, _ip, _ip],
@@ -153,6 +154,11 @@ def wi_decode_step(ix: int, q, out, k_new=None, v_new=None, stream=None):
 
 def wi_dense_decode(ix: int, q, out, stream=None):
     _check(lib.wi_dense_decode(ix, _ptr(q), _ptr(out), _stream(stream)))
+
+
+def wi_decode_kernel(ix: int, kernel: int, q, out, stream=None):
+    """One decode kernel alone (0 scores, 1 top-k + estimation, 2 exact + merge), for timing."""
+    _check(lib.wi_decode_kernel(ix, kernel, _ptr(q), _ptr(out), _stream(stream)))
 
 
 def wi_decode_step_host(ix: int, q_host, out_host, k_new_host=None, v_new_host=None, stream=None):

@@ -60,6 +60,7 @@ struct wi_index {
   void* appV = nullptr;
   int* app_count = nullptr;
   int appended = 0;
+  long long steps_run = 0;  // decode steps enqueued (host-side count)
   // decode scratch
   WiDecodeBufs b{};
   int* err = nullptr;
@@ -517,11 +518,26 @@ int wi_decode_step(wi_index* ix, const void* q, const void* k_new, const void* v
   }
   cudaError_t e = wi_launch_decode(ix->g, ix->b, q, out, st, ev);
   if (e != cudaSuccess) return fail(WI_ECUDA, "decode launch: %s", cudaGetErrorString(e));
+  ix->steps_run++;
   if (k_new) {
     e = wi_launch_append(ix->g, ix->b, k_new, v_new, ix->appended, st);
     if (e != cudaSuccess) return fail(WI_ECUDA, "append launch: %s", cudaGetErrorString(e));
     ix->appended++;
   }
+  return WI_OK;
+}
+
+int wi_decode_kernel(wi_index* ix, int kernel, const void* q, float* out, void* stream) {
+  g_err[0] = 0;
+  if (!ix || !q || !out) return fail(WI_EINVAL, "index, q and out must be non-NULL");
+  if (kernel < 0 || kernel >= WI_DECODE_KERNELS) return fail(WI_EINVAL, "kernel must be in [0, %d)", WI_DECODE_KERNELS);
+  if (reinterpret_cast<uintptr_t>(q) & 15) return fail(WI_EINVAL, "q must be 16-byte aligned");
+  if (ix->steps_run == 0)
+    return fail(WI_EINVAL, "run one whole decode step on this index first");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ix->last_stream = st;
+  cudaError_t e = wi_launch_decode(ix->g, ix->b, q, out, st, nullptr, 1u << kernel);
+  if (e != cudaSuccess) return fail(WI_ECUDA, "decode kernel launch: %s", cudaGetErrorString(e));
   return WI_OK;
 }
 

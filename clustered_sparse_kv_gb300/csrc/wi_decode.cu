@@ -492,8 +492,11 @@ __device__ void estimate_role(unsigned char* raw, const VT* __restrict__ valsum,
 // Every pass over the clusters is a short rolled loop with the CTA's stride:
 // the role runs once per CTA per step and its instructions mostly miss the
 // instruction cache, so the code executed once is kept small (the rare paths
-// are out of line).  The keys are cached in shared memory when C <= kSelKeysMax, else
-// recomputed from the (L2-resident) scores and counts at every pass.
+// are out of line).  The keys are cached in shared memory when C <= kSelKeysMax;
+// above it (up to 65536 clusters) the first pass streams them from global
+// memory with 16-byte loads and keeps each key's distance bin (16 bits) in
+// shared memory, which the later passes read; only the threshold bin's keys
+// and the selected keys are read again.
 constexpr int kSelThreads = 512;  // ranking capacity: candidates in the threshold bin
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kBinsPerLane = kTopkBins / kSelThreads;  // 4
@@ -563,8 +566,9 @@ __host__ __device__ inline size_t sel_base_bytes(int C, int kmax) {
 __host__ __device__ inline bool sel_rows_async(int C, int kmax) {
   return C <= kSelKeysMax && sel_base_bytes(C, kmax) + (size_t)C * 12 <= 200 * 1024;
 }
+// Above kSelKeysMax the keys do not fit: each key's logarithmic distance bin (16 bits) is kept instead.
 __host__ __device__ inline size_t sel_keys_bytes(int C, int kmax) {
-  return C <= kSelKeysMax ? (size_t)C * (sel_rows_async(C, kmax) ? 12 : 4) : 0;
+  return C <= kSelKeysMax ? (size_t)C * (sel_rows_async(C, kmax) ? 12 : 4) : ((size_t)C * 2 + 15) / 16 * 16;
 }
 __host__ __device__ inline size_t sel_smem_bytes(int C, int kmax) {
   return sel_base_bytes(C, kmax) + sel_keys_bytes(C, kmax);
@@ -718,6 +722,8 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
     }
   };
   const KeySrc key_of{cached ? ks : nullptr, s};
+  uint16_t* kbin = reinterpret_cast<uint16_t*>(ks);  // [C] distance bins (0xFFFF: empty cluster) if !cached
+  constexpr uint32_t kFarBin = 64 * 30;               // log_bin(2^30): the far keys' bins start here
   int kk = min(kmax, a.nonempty[u]);
   // the first keys' loads are in flight across the K0 reduction and the barrier below
   const int n4 = C / 4;
@@ -729,7 +735,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
       f[r] = i < n4 ? __ldcg(reinterpret_cast<const uint4*>(s) + i) : make_uint4(0u, 0u, 0u, 0u);
     }
   };
-  if (cached) load4(tid);
+  load4(tid);
   // K0 = the largest key of a non-empty cluster, from k_scores' per-CTA maxima of the same
   // scores (every warp reduces them itself: no barrier)
   uint32_t K0 = 0u;
@@ -767,9 +773,25 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
       }
     }
   } else {
-    __syncthreads();
-    if (kk > 0)
-      for (int j = tid; j < C; j += kSThreads) count_key(key_of(j), false);
+    __syncthreads();  // the histogram and the masks are zero
+    auto bin_of = [&](uint32_t k) -> uint32_t { return k == 0u ? 0xFFFFu : (uint32_t)log_bin(K0 - k); };
+    for (int i0 = tid; i0 < n4; i0 += 4 * kSThreads) {
+      if (i0 != tid) load4(i0);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int i = i0 + r * kSThreads;
+        if (i < n4) {
+          const uint32_t b0 = bin_of(f[r].x), b1 = bin_of(f[r].y), b2 = bin_of(f[r].z), b3 = bin_of(f[r].w);
+          reinterpret_cast<uint2*>(kbin)[i] = make_uint2(b0 | (b1 << 16), b2 | (b3 << 16));
+          if (kk > 0) {
+            if (b0 < kFarBin) atomicAdd(&sm.hist[0][b0], 1);
+            if (b1 < kFarBin) atomicAdd(&sm.hist[0][b1], 1);
+            if (b2 < kFarBin) atomicAdd(&sm.hist[0][b2], 1);
+            if (b3 < kFarBin) atomicAdd(&sm.hist[0][b3], 1);
+          }
+        }
+      }
+    }
   }
   __syncthreads();
   bool found = kk == 0;
@@ -778,7 +800,14 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
     int above = 0;
     found = find_bin(sm.hist[0], kk, sm, &bstar, &above);
     if (!found) {  // uniform: the k-th key is a far one; add the far keys and search again
-      for (int j = tid; j < C; j += kSThreads) count_key(key_of(j), true);
+      if (cached) {
+        for (int j = tid; j < C; j += kSThreads) count_key(key_of(j), true);
+      } else {
+        for (int j = tid; j < C; j += kSThreads) {
+          const uint32_t b = kbin[j];
+          if (b != 0xFFFFu && b >= kFarBin) atomicAdd(&sm.hist[0][b], 1);
+        }
+      }
       __syncthreads();
       found = find_bin(sm.hist[0], kk, sm, &bstar, &above);
     }
@@ -811,10 +840,24 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
                               classify(k4.w, j + 3);
         if (bits) atomicOr(&tmask[j >> 5], bits);
       }
-    } else {
-      for (int j = tid; j < C; j += kSThreads) {
-        const uint32_t bits = classify(key_of(j), j);
-        if (bits) atomicOr(&tmask[j >> 5], bits);
+    } else {  // four bins per load; the threshold bin's keys are read again from global memory
+      for (int i = tid; i < C / 4; i += kSThreads) {
+        const uint2 b2 = reinterpret_cast<const uint2*>(kbin)[i];
+        const uint32_t bq[4] = {b2.x & 0xFFFFu, b2.x >> 16, b2.y & 0xFFFFu, b2.y >> 16};
+        uint32_t bits = 0u;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int j = 4 * i + q;
+          if (bq[q] == 0xFFFFu || (int)bq[q] > bstar) continue;
+          if ((int)bq[q] < bstar) {
+            bits |= 1u << (j & 31);
+          } else {
+            const uint32_t k = __ldcg(s + j);
+            const int slot = atomicAdd(&sm.s_ncand, 1);
+            if (slot < kSelThreads) { sm.ckey[slot] = k; sm.cid[slot] = j; }
+          }
+        }
+        if (bits) atomicOr(&tmask[(4 * i) >> 5], bits);
       }
     }
   }
@@ -1611,13 +1654,13 @@ cudaError_t launch_select(const WiGeom& g, const WiDecodeBufs& b, const TopkArgs
 
 template <int G>
 cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, float* out, cudaStream_t st,
-                     const cudaEvent_t* ev) {
+                     const cudaEvent_t* ev, unsigned mask) {
   const bf16* q = static_cast<const bf16*>(qv);
   const float lam = 1.0f / sqrtf((float)WI_D);
   cudaError_t e = mark(ev, 0, st);
   if (e != cudaSuccess) return e;
   // scores
-  e = g.grp ? launch_scores<G, true>(g, b, q, st) : launch_scores<G, false>(g, b, q, st);
+  if (mask & 1u) e = g.grp ? launch_scores<G, true>(g, b, q, st) : launch_scores<G, false>(g, b, q, st);
   if (e != cudaSuccess || (e = mark(ev, 1, st)) != cudaSuccess) return e;
   TopkArgs t;
   t.scores = reinterpret_cast<const uint32_t*>(b.scores);
@@ -1645,7 +1688,7 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   t.PE = b.p_es;
   t.lam = lam;
   t.n_sink = g.n_sink;
-  e = launch_select<G>(g, b, t, st);
+  if (mask & 2u) e = launch_select<G>(g, b, t, st);
   if (e != cudaSuccess || (e = mark(ev, 2, st)) != cudaSuccess) return e;
   ExactArgs a;
   a.q = q;
@@ -1678,7 +1721,7 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   a.W = g.W;
   a.max_append = g.max_append;
   a.lam = lam;
-  e = b.valsum16 ? launch_exact<bf16>(g, b, a, st) : launch_exact<float>(g, b, a, st);
+  if (mask & 4u) e = b.valsum16 ? launch_exact<bf16>(g, b, a, st) : launch_exact<float>(g, b, a, st);
   if (e != cudaSuccess) return e;
   return mark(ev, 3, st);
 }
@@ -1686,16 +1729,16 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
 }  // namespace
 
 cudaError_t wi_launch_decode(const WiGeom& g, const WiDecodeBufs& b, const void* q, float* out, cudaStream_t st,
-                             const cudaEvent_t* ev) {
+                             const cudaEvent_t* ev, unsigned mask) {
   switch (g.G) {
-    case 1: return launch_g<1>(g, b, q, out, st, ev);
-    case 2: return launch_g<2>(g, b, q, out, st, ev);
-    case 3: return launch_g<3>(g, b, q, out, st, ev);
-    case 4: return launch_g<4>(g, b, q, out, st, ev);
-    case 5: return launch_g<5>(g, b, q, out, st, ev);
-    case 6: return launch_g<6>(g, b, q, out, st, ev);
-    case 7: return launch_g<7>(g, b, q, out, st, ev);
-    case 8: return launch_g<8>(g, b, q, out, st, ev);
+    case 1: return launch_g<1>(g, b, q, out, st, ev, mask);
+    case 2: return launch_g<2>(g, b, q, out, st, ev, mask);
+    case 3: return launch_g<3>(g, b, q, out, st, ev, mask);
+    case 4: return launch_g<4>(g, b, q, out, st, ev, mask);
+    case 5: return launch_g<5>(g, b, q, out, st, ev, mask);
+    case 6: return launch_g<6>(g, b, q, out, st, ev, mask);
+    case 7: return launch_g<7>(g, b, q, out, st, ev, mask);
+    case 8: return launch_g<8>(g, b, q, out, st, ev, mask);
     default: return cudaErrorInvalidValue;
   }
 }

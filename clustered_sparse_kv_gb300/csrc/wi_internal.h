@@ -94,8 +94,9 @@ struct WiDecodeBufs {
 // Full attention over every cached and appended token (the dense comparator).
 cudaError_t wi_launch_dense(const WiGeom& g, const WiDecodeBufs& b, const void* q, float* out, cudaStream_t st);
 int wi_dense_ctas_per_sm(int G);
+// mask: bit i launches decode kernel i (1 scores, 2 select/estimate, 4 exact/merge); 7 = a whole step
 cudaError_t wi_launch_decode(const WiGeom& g, const WiDecodeBufs& b, const void* q, float* out, cudaStream_t st,
-                             const cudaEvent_t* ev);
+                             const cudaEvent_t* ev, unsigned mask = 7u);
 // bytes (a multiple of 16) from src to dst, 16-byte aligned; either may be mapped host memory.
 cudaError_t wi_launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t st);
 cudaError_t wi_launch_append(const WiGeom& g, const WiDecodeBufs& b, const void* k_new, const void* v_new, int t,

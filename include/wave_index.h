@@ -174,6 +174,18 @@ int wi_last_selection(const wi_index* ix, int32_t* ids, int32_t* counts, void* s
  */
 int wi_dense_decode(wi_index* ix, const void* q, float* out, void* stream);
 
+/*
+ * One kernel of the decode step alone (benchmarking aid: the duration of one
+ * kernel in isolation, without events between kernels).  kernel 0: centroid
+ * scores; 1: top-k with the estimation over all clusters; 2: exact attention
+ * with the final merge.  Each kernel reads what the previous one wrote in the
+ * last decode step of this index, so it repeats that step's work for its
+ * part; q and out as in wi_decode_step (kernel 2 rewrites out).  Returns
+ * WI_EINVAL before the index's first wi_decode_step.  Stream-ordered, no
+ * allocation, graph-capturable.
+ */
+int wi_decode_kernel(wi_index* ix, int kernel, const void* q, float* out, void* stream);
+
 /* Sizes of an index: units, clusters per unit, k_max (the budget), group g,
  * tokens appended so far (host-side count).  Any output pointer may be NULL. */
 int wi_index_shape(const wi_index* ix, int* units, int* clusters, int* k_max, int* group, int* appended);

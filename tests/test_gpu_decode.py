@@ -162,6 +162,25 @@ def test_topk_half_tied(wi):
     assert run_case(wi, w, idx=idx, strict_ids=True) < 1e-4
 
 
+@pytest.mark.parametrize("n_ctx,budget", [(131072, 0), (81920, 37)])
+def test_topk_large_cluster_count(wi, n_ctx, budget):
+    """Above 32768 clusters per kv head the top-k keeps 16-bit distance bins in shared memory
+    instead of the keys: C = 65536 (k = 1180, the million-token budget) and C = 40960."""
+    w = small(n_ctx=n_ctx, seg_len=1024, clusters_per_seg=512, iters=1, n_q_heads=4, budget_k=budget,
+              budget_frac=0.018, seed=34)
+    assert w.clusters > 32768
+    assert run_case(wi, w, strict_ids=False) < 1e-4
+
+
+def test_topk_large_cluster_count_ties(wi):
+    """Every score tied at C = 65536 (more ties than ranking threads: the radix path over keys read
+    from global memory) and two score levels at C = 40960; the selection must equal the oracle's."""
+    w = small(n_ctx=131072, seg_len=1024, clusters_per_seg=512, iters=1, n_q_heads=4, budget_k=100, seed=35)
+    assert run_case(wi, w, idx=tied_index(w, lambda j: 0), strict_ids=True) < 1e-4
+    w = small(n_ctx=81920, seg_len=1024, clusters_per_seg=512, iters=1, n_q_heads=4, budget_k=300, seed=36)
+    assert run_case(wi, w, idx=tied_index(w, lambda j: (j * 7) % 3 == 0), strict_ids=True) < 1e-4
+
+
 def test_decode_large_budget(wi):
     # k above the top-k's list capacity (512): the selection goes through per-chunk bit masks
     w = small(n_ctx=16384, seg_len=1024, clusters_per_seg=128, iters=2, n_q_heads=4, budget_k=700, seed=33)
@@ -248,6 +267,28 @@ def test_graph_replay_matches_direct(wi):
         assert torch.equal(got, direct)
     ix.free()
 
+
+
+def test_single_kernel_launches_repeat_the_step(wi):
+    """wi_decode_kernel (the benchmark's kernel-alone timing) launches one kernel of the step; run
+    after a whole step, each kernel repeats its part, so the output is bit-identical."""
+    w = small(n_ctx=8192, seg_len=2048, clusters_per_seg=128, iters=2, n_q_heads=8, n_kv_heads=2, budget_k=9,
+              seed=62)
+    k, v, q, K, V, Q = gen(w)
+    ix = wi.WaveIndex.build(wi.config_from_workload(w), dev16(k), dev16(v))
+    qd = dev16(q)
+    with pytest.raises(wi.WiError):
+        wi.wi_decode_kernel(ix.handle, 2, qd, torch.empty(1, device=DEV))  # no whole step yet
+    ref = ix.decode(qd)
+    torch.cuda.synchronize()
+    for order in ([2], [1, 2], [0, 1, 2], [2, 2]):
+        out = torch.full_like(ref, float("nan"))
+        for kid in order:
+            wi.wi_decode_kernel(ix.handle, kid, qd, out)
+        torch.cuda.synchronize()
+        ix.check()
+        assert torch.equal(out, ref), order
+    ix.free()
 
 
 @pytest.mark.parametrize("splits", [1, 5, 12])
