@@ -262,9 +262,16 @@ class WaveIndex:
         wi_dense_decode(self.handle, q, out, stream)
         return out
 
+    @property
+    def perm_slots(self) -> int:
+        """Slots per unit in perm: the build's clustered tokens plus room for the segments that
+        appends may grow (max_append // seg_len of seg_len tokens)."""
+        c = self.cfg
+        return c.n_ctx - c.n_sink - c.local_window + (c.max_append // c.seg_len) * c.seg_len
+
     def export(self, stream=None) -> dict:
         U, C = self.units, self.clusters
-        n_idx = self.cfg.n_ctx - self.cfg.n_sink - self.cfg.local_window
+        n_idx = self.perm_slots
         dev = self.k.device
         r = {
             "counts": torch.empty((U, C), dtype=torch.int32, device=dev),

@@ -2,6 +2,7 @@
 // allocation and the order of the kernels of a build and of a decode step.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -60,6 +61,13 @@ struct wi_index {
   void* appV = nullptr;
   int* app_count = nullptr;
   int appended = 0;
+  // decode-time growth (only when max_append >= seg_len): the grown segments' rows and counters
+  void* grownK = nullptr;
+  void* grownV = nullptr;
+  int* grown = nullptr;
+  int* kcur = nullptr;
+  int grown_host = 0;
+  WiGrowBufs gw{};
   long long steps_run = 0;  // decode steps enqueued (host-side count)
   // decode scratch
   WiDecodeBufs b{};
@@ -87,6 +95,10 @@ struct wi_index {
   int prof_slots = 0;
   long long prof_steps = 0;
 };
+
+int wi_budget(const WiGeom& g, int C) {
+  return g.budget_k > 0 ? g.budget_k : (int)std::ceil(g.budget_frac * (double)C);
+}
 
 int wi_geom_from_config(const wi_config* c, WiGeom* g, char* msg, size_t msglen) {
 #define BAD(...)                          \
@@ -122,17 +134,24 @@ int wi_geom_from_config(const wi_config* c, WiGeom* g, char* msg, size_t msglen)
   g->S = c->seg_len;
   g->Cs = c->clusters_per_seg;
   g->nseg = (int)(c->n_ctx / c->seg_len);
-  if ((long long)g->nseg * g->Cs >= (1LL << 30)) BAD("too many clusters per unit");
-  g->C = g->nseg * g->Cs;
+  // decode-time growth: one more segment per seg_len appended tokens
+  g->Gmax = c->max_append / c->seg_len;
+  if (((long long)g->nseg + g->Gmax) * g->Cs >= (1LL << 30)) BAD("too many clusters per unit");
+  g->Cb = g->nseg * g->Cs;
+  g->C = g->Cb + g->Gmax * g->Cs;
   g->n = c->n_ctx;
   g->n_sink = c->n_sink;
   g->W = c->local_window;
   g->n_idx = (int)(c->n_ctx - c->n_sink - c->local_window);
+  g->perm_stride = g->n_idx + g->Gmax * g->S;
   g->iters = c->iters;
   g->max_append = c->max_append;
-  long long k = c->budget_k > 0 ? c->budget_k : (long long)std::ceil(c->budget_frac * (double)g->C);
-  if (k < 1 || k > g->C) BAD("retrieval budget k = %lld must be in [1, C = %d]", k, g->C);
-  g->kmax = (int)k;
+  g->budget_frac = c->budget_frac;
+  g->budget_k = c->budget_k;
+  const long long k = wi_budget(*g, g->Cb);
+  if (k < 1 || k > g->Cb) BAD("retrieval budget k = %lld must be in [1, C = %d]", k, g->Cb);
+  g->kbuild = (int)k;
+  g->kmax = wi_budget(*g, g->C);
   if (g->G > 8) {
     snprintf(msg, msglen, "query heads per kv head must be <= 8 (got %d)", g->G);
     return WI_EUNSUPPORTED;
@@ -142,7 +161,7 @@ int wi_geom_from_config(const wi_config* c, WiGeom* g, char* msg, size_t msglen)
     return WI_EUNSUPPORTED;
   }
   if (g->C > 65536) {
-    snprintf(msg, msglen, "at most 65536 clusters per kv head (got %d)", g->C);
+    snprintf(msg, msglen, "at most 65536 clusters per kv head, grown segments included (got %d)", g->C);
     return WI_EUNSUPPORTED;
   }
   if (g->S > 16384) {
@@ -194,19 +213,48 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   if (g.vs16) A(ix->valsum16, U * C * 128 * 2);
   A(ix->cnt, U * C * 4);
   A(ix->off, U * (C + 1) * 4);
-  A(ix->perm, U * (size_t)g.n_idx * 4);
+  A(ix->perm, U * (size_t)g.perm_stride * 4);
   A(ix->nonempty, U * 4);
   const size_t app = (size_t)(g.max_append > 0 ? g.max_append : 1);
   A(ix->appK, U * app * 128 * 2);
   A(ix->appV, U * app * 128 * 2);
   A(ix->app_count, 4);
   A(ix->err, 4);
+  A(ix->grown, 4);
+  A(ix->kcur, 4);
+  if (g.Gmax > 0) {
+    // room for the segments that appends may add; their clusters stay empty until grown
+    const size_t S = g.S, Cs = g.Cs, rows = (size_t)g.Gmax * U * S;
+    A(ix->grownK, rows * 128 * 2);
+    A(ix->grownV, rows * 128 * 2);
+    WiGrowBufs& w = ix->gw;
+    A(w.chat, U * Cs * 128 * 2);
+    A(w.assign, U * S * 4);
+    A(w.seg_counts, U * Cs * 4);
+    A(w.seg_offsets, U * (Cs + 1) * 4);
+    A(w.slots, U * S * 4);
+    A(w.mu, U * Cs * 128 * 2);
+    A(w.valsum, U * Cs * 128 * 4);
+    A(w.cnt, U * Cs * 4);
+    A(w.off, U * (Cs + 1) * 4);
+    A(w.perm, U * S * 4);
+    A(w.nonempty, U * 4);
+    A(w.tK, U * S * 128 * 2);
+    A(w.tV, U * S * 128 * 2);
+    WI_CUDA(cudaMemsetAsync(ix->mu, 0, U * C * 128 * 2, st));
+    WI_CUDA(cudaMemsetAsync(ix->valsum, 0, U * C * 128 * 4, st));
+    WI_CUDA(cudaMemsetAsync(ix->cnt, 0, U * C * 4, st));
+    WI_CUDA(cudaMemsetAsync(ix->off, 0, U * (C + 1) * 4, st));
+    WI_CUDA(cudaMemsetAsync(ix->perm, 0xFF, U * (size_t)g.perm_stride * 4, st));
+  }
   WiDecodeBufs& b = ix->b;
   int sms = 0;
   WI_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ix->device));
   const int tiles = (int)((C + 15) / 16);  // score_estimate splits a unit's clusters on multiples of 16
+  // scores: at most one wave of one CTA per SM (a partial second wave of a few CTAs would double
+  // the kernel's time)
   int p1 = env_int("WI_D1_CTAS_PER_UNIT", 0);
-  if (p1 <= 0) p1 = (int)((sms + U - 1) / U);
+  if (p1 <= 0) p1 = (int)(sms / U);
   if (p1 > tiles) p1 = tiles;
   if (p1 > 256) p1 = 256;
   if (p1 < 1) p1 = 1;
@@ -218,9 +266,12 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   if (pe > 256) pe = 256;
   if (pe < 1) pe = 1;
   b.p_es = pe;
-  // exact attention: (splits + 1 steady CTA) per head, sized to fill two CTAs per SM in one wave
+  // exact attention: (splits + 1 steady CTA) per head.  Few heads: fill two CTAs per SM in one wave
+  // (the step is a latency chain); many heads: about two waves of split CTAs, so that the heads'
+  // unequal row counts balance across the SMs
   int ns = env_int("WI_D3_SPLITS", 0);
-  if (ns <= 0) ns = (int)((2 * (size_t)sms) / (U * G)) - 1;
+  const size_t heads = U * G, slots = 2 * (size_t)sms;
+  if (ns <= 0) ns = heads * 2 <= slots ? (int)(slots / heads) - 1 : (int)((2 * slots + heads - 1) / heads);
   if (ns > 64) ns = 64;
   if (ns < 1) ns = 1;
   b.nsplit = ns;
@@ -263,8 +314,14 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   b.appK = ix->appK;
   b.appV = ix->appV;
   b.app_count = ix->app_count;
+  b.grownK = ix->grownK;
+  b.grownV = ix->grownV;
+  b.grown = ix->grown;
+  b.kcur = ix->kcur;
   b.err = ix->err;
   WI_CUDA(cudaMemsetAsync(ix->app_count, 0, 4, st));
+  WI_CUDA(cudaMemsetAsync(ix->grown, 0, 4, st));
+  WI_CUDA(wi_launch_set_int(ix->kcur, g.kbuild, st));
   WI_CUDA(cudaMemsetAsync(ix->err, 0, 4, st));
   WI_CUDA(cudaMemsetAsync(b.selcnt, 0, U * G * 4, st));
   WI_CUDA(cudaMemsetAsync(b.ticket, 0, U * G * 4, st));
@@ -294,22 +351,31 @@ int new_index(const wi_config* cfg, void* k, void* v, wi_index** out, wi_index**
   return WI_OK;
 }
 
+// Scratch rows of the in-place permutation: whole units, at most 1 GiB each for K and V.
+int perm_scratch(const WiGeom& g, void** tK, void** tV, int* nb, cudaStream_t st) {
+  const size_t per_unit = (size_t)(g.n_idx > 0 ? g.n_idx : 1) * 128 * 2;
+  const size_t cap = (size_t)1 << 30;
+  *nb = (int)(cap / per_unit);
+  if (*nb < 1) *nb = 1;
+  if (*nb > g.U) *nb = g.U;
+  *tK = *tV = nullptr;
+  if (cudaMallocAsync(tK, per_unit * *nb, st) != cudaSuccess || cudaMallocAsync(tV, per_unit * *nb, st) != cudaSuccess) {
+    cudaGetLastError();
+    if (*tK) cudaFreeAsync(*tK, st);
+    *tK = nullptr;
+    return fail(WI_ENOMEM, "permutation scratch (%zu bytes) allocation failed", 2 * per_unit * *nb);
+  }
+  return WI_OK;
+}
+
 // Permute the clustered rows of K, V by ix->perm, through bounded scratch.
 int permute_kv(wi_index* ix, cudaStream_t st) {
   const WiGeom& g = ix->g;
   if (g.n_idx == 0) return WI_OK;
-  const size_t per_unit = (size_t)g.n_idx * 128 * 2;
-  const size_t cap = (size_t)1 << 30;
-  int nb = (int)(cap / per_unit);
-  if (nb < 1) nb = 1;
-  if (nb > g.U) nb = g.U;
   void *tK = nullptr, *tV = nullptr;
-  if (cudaMallocAsync(&tK, per_unit * nb, st) != cudaSuccess ||
-      cudaMallocAsync(&tV, per_unit * nb, st) != cudaSuccess) {
-    cudaGetLastError();
-    if (tK) cudaFreeAsync(tK, st);
-    return fail(WI_ENOMEM, "permutation scratch (%zu bytes) allocation failed", 2 * per_unit * nb);
-  }
+  int nb = 0;
+  int rc = perm_scratch(g, &tK, &tV, &nb, st);
+  if (rc != WI_OK) return rc;
   cudaError_t e = cudaSuccess;
   for (int u0 = 0; u0 < g.U && e == cudaSuccess; u0 += nb) {
     const int nu = (g.U - u0) < nb ? (g.U - u0) : nb;
@@ -324,7 +390,6 @@ int permute_kv(wi_index* ix, cudaStream_t st) {
 struct BuildScratch {
   void* chat = nullptr;
   int32_t* assign = nullptr;
-  float* invnorm = nullptr;
   int* seg_counts = nullptr;
   int* seg_offsets = nullptr;
   int* slots = nullptr;
@@ -336,7 +401,6 @@ int scratch_alloc(const WiGeom& g, BuildScratch* s, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   e = cudaMallocAsync(&s->chat, SU * g.Cs * 128 * 2, st);
   if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&s->assign), rows * 4, st);
-  if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&s->invnorm), rows * 4, st);
   if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&s->seg_counts), SU * g.Cs * 4, st);
   if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&s->seg_offsets), SU * (g.Cs + 1) * 4, st);
   if (e == cudaSuccess) e = cudaMallocAsync(reinterpret_cast<void**>(&s->slots), SU * g.S * 4, st);
@@ -348,7 +412,7 @@ int scratch_alloc(const WiGeom& g, BuildScratch* s, cudaStream_t st) {
 }
 
 void scratch_free(BuildScratch* s, cudaStream_t st) {
-  void* ps[] = {s->chat, s->assign, s->invnorm, s->seg_counts, s->seg_offsets, s->slots};
+  void* ps[] = {s->chat, s->assign, s->seg_counts, s->seg_offsets, s->slots};
   for (void* p : ps)
     if (p) cudaFreeAsync(p, st);
 }
@@ -381,6 +445,8 @@ int wi_build_index(const wi_config* cfg, void* k, void* v, const void* init_cent
   ix->last_stream = st;
   const WiGeom& g = ix->g;
   BuildScratch s;
+  void *tK = nullptr, *tV = nullptr;
+  int nb = 0;
   if ((rc = alloc_index(ix, st)) != WI_OK || (rc = scratch_alloc(g, &s, st)) != WI_OK) {
     scratch_free(&s, st);
     destroy(ix);
@@ -392,7 +458,6 @@ int wi_build_index(const wi_config* cfg, void* k, void* v, const void* init_cent
     ix->build_ev.push_back(e);
   }
   WI_LAUNCH(cudaEventRecord(ix->build_ev[0], st));
-  WI_LAUNCH(wi_launch_invnorm(k, s.invnorm, (long long)g.U * g.n, st));
   if (init_centroids)
     WI_LAUNCH(cudaMemcpyAsync(s.chat, init_centroids, (size_t)g.U * g.nseg * g.Cs * 128 * 2, cudaMemcpyDefault, st));
   else
@@ -403,18 +468,24 @@ int wi_build_index(const wi_config* cfg, void* k, void* v, const void* init_cent
     WI_LAUNCH(cudaEventRecord(ix->build_ev[3 + 2 * t], st));
     WI_LAUNCH(wi_launch_segment_sort(g, s.assign, s.seg_counts, s.seg_offsets, s.slots, ix->err, st));
     if (t + 1 < g.iters)
-      WI_LAUNCH(wi_launch_centroid_update(g, k, s.invnorm, s.seg_counts, s.seg_offsets, s.slots, s.chat, st));
+      WI_LAUNCH(wi_launch_centroid_update(g, k, s.seg_counts, s.seg_offsets, s.slots, s.chat, st));
   }
-  WI_LAUNCH(wi_launch_final_reduce(g, k, v, s.seg_counts, s.seg_offsets, s.slots, ix->mu, ix->valsum, ix->cnt,
-                                   ix->off, ix->perm, ix->nonempty, st));
+  // the final index and the in-place permutation, one pass over K and V for both
+  if ((rc = perm_scratch(g, &tK, &tV, &nb, st)) != WI_OK) goto done;
+  WI_LAUNCH(wi_launch_reduce_permute(g, k, v, s.seg_counts, s.seg_offsets, s.slots, ix->mu, ix->valsum, ix->cnt,
+                                     ix->off, ix->perm, ix->nonempty, tK, tV, nb, st));
   if (g.vs16) WI_LAUNCH(wi_launch_to_bf16(ix->valsum, ix->valsum16, (long long)g.U * g.C * 128, st));
+  cudaFreeAsync(tK, st);
+  cudaFreeAsync(tV, st);
+  tK = tV = nullptr;
   scratch_free(&s, st);
   s = BuildScratch();
-  if ((rc = permute_kv(ix, st)) != WI_OK) goto done;
   WI_LAUNCH(cudaEventRecord(ix->build_ev[1], st));
   *out = ix;
   return WI_OK;
 done:
+  if (tK) cudaFreeAsync(tK, st);
+  if (tV) cudaFreeAsync(tV, st);
   scratch_free(&s, st);
   cudaStreamSynchronize(st);
   destroy(ix);
@@ -434,8 +505,10 @@ int wi_index_import(const wi_config* cfg, void* k, void* v, const int32_t* count
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   ix->last_stream = st;
   const WiGeom& g = ix->g;
-  const size_t U = g.U, C = g.C;
-  std::vector<int32_t> hc(U * C), hp(U * (size_t)g.n_idx), hoff(U * (C + 1)), hne(U, 0);
+  // the caller's arrays hold the build's Cb clusters; the index's rows have room for C (grown segments)
+  const size_t U = g.U, Cb = g.Cb, C = g.C, PS = g.perm_stride;
+  std::vector<int32_t> hc(U * Cb), hp(U * (size_t)g.n_idx), hoff(U * (C + 1), (int)(g.n - g.W)), hne(U, 0);
+  std::vector<int32_t> hcC(U * C, 0), hpP(U * PS, -1);
   std::vector<unsigned char> seen;
   if (cudaMemcpy(hc.data(), counts, hc.size() * 4, cudaMemcpyDefault) != cudaSuccess ||
       cudaMemcpy(hp.data(), perm, hp.size() * 4, cudaMemcpyDefault) != cudaSuccess) {
@@ -446,9 +519,10 @@ int wi_index_import(const wi_config* cfg, void* k, void* v, const int32_t* count
   for (size_t u = 0; u < U; ++u) {
     long long run = g.n_sink;
     seen.assign((size_t)g.n, 0);
-    for (size_t c = 0; c < C; ++c) {
-      const int m = hc[u * C + c];
+    for (size_t c = 0; c < Cb; ++c) {
+      const int m = hc[u * Cb + c];
       if (m < 0) { destroy(ix); return fail(WI_EINVAL, "negative count (unit %zu, cluster %zu)", u, c); }
+      hcC[u * C + c] = m;
       hoff[u * (C + 1) + c] = (int)run;
       const int s = (int)(c / g.Cs);
       for (int t = 0; t < m; ++t) {
@@ -465,15 +539,16 @@ int wi_index_import(const wi_config* cfg, void* k, void* v, const int32_t* count
       if (m > 0) hne[u]++;
     }
     if (run != g.n - g.W) { destroy(ix); return fail(WI_EINVAL, "counts of unit %zu do not cover the clustered tokens", u); }
-    hoff[u * (C + 1) + C] = (int)run;
+    std::copy(hp.begin() + u * g.n_idx, hp.begin() + (u + 1) * g.n_idx, hpP.begin() + u * PS);
   }
   if ((rc = alloc_index(ix, st)) != WI_OK) { destroy(ix); return rc; }
-  WI_LAUNCH(cudaMemcpyAsync(ix->cnt, hc.data(), hc.size() * 4, cudaMemcpyHostToDevice, st));
-  WI_LAUNCH(cudaMemcpyAsync(ix->perm, hp.data(), hp.size() * 4, cudaMemcpyHostToDevice, st));
+  WI_LAUNCH(cudaMemcpyAsync(ix->cnt, hcC.data(), hcC.size() * 4, cudaMemcpyHostToDevice, st));
+  WI_LAUNCH(cudaMemcpyAsync(ix->perm, hpP.data(), hpP.size() * 4, cudaMemcpyHostToDevice, st));
   WI_LAUNCH(cudaMemcpyAsync(ix->off, hoff.data(), hoff.size() * 4, cudaMemcpyHostToDevice, st));
   WI_LAUNCH(cudaMemcpyAsync(ix->nonempty, hne.data(), hne.size() * 4, cudaMemcpyHostToDevice, st));
-  WI_LAUNCH(cudaMemcpyAsync(ix->mu, mu, U * C * 128 * 2, cudaMemcpyDefault, st));
-  WI_LAUNCH(cudaMemcpyAsync(ix->valsum, valsum, U * C * 128 * 4, cudaMemcpyDefault, st));
+  WI_LAUNCH(cudaMemcpy2DAsync(ix->mu, C * 128 * 2, mu, Cb * 128 * 2, Cb * 128 * 2, U, cudaMemcpyDefault, st));
+  WI_LAUNCH(cudaMemcpy2DAsync(ix->valsum, C * 128 * 4, valsum, Cb * 128 * 4, Cb * 128 * 4, U, cudaMemcpyDefault,
+                              st));
   if (g.vs16) WI_LAUNCH(wi_launch_to_bf16(ix->valsum, ix->valsum16, (long long)U * C * 128, st));
   if ((rc = permute_kv(ix, st)) != WI_OK) goto done;
   // the host vectors above are pageable: finish the copies before they go away
@@ -495,7 +570,7 @@ int wi_index_export(const wi_index* ix, int32_t* counts, int32_t* offsets, int32
   const size_t U = g.U, C = g.C;
   if (counts) WI_CUDA(cudaMemcpyAsync(counts, ix->cnt, U * C * 4, cudaMemcpyDefault, st));
   if (offsets) WI_CUDA(cudaMemcpyAsync(offsets, ix->off, U * (C + 1) * 4, cudaMemcpyDefault, st));
-  if (perm) WI_CUDA(cudaMemcpyAsync(perm, ix->perm, U * (size_t)g.n_idx * 4, cudaMemcpyDefault, st));
+  if (perm) WI_CUDA(cudaMemcpyAsync(perm, ix->perm, U * (size_t)g.perm_stride * 4, cudaMemcpyDefault, st));
   if (mu) WI_CUDA(cudaMemcpyAsync(mu, ix->mu, U * C * 128 * 2, cudaMemcpyDefault, st));
   if (valsum) WI_CUDA(cudaMemcpyAsync(valsum, ix->valsum, U * C * 128 * 4, cudaMemcpyDefault, st));
   return WI_OK;
@@ -520,9 +595,19 @@ int wi_decode_step(wi_index* ix, const void* q, const void* k_new, const void* v
   if (e != cudaSuccess) return fail(WI_ECUDA, "decode launch: %s", cudaGetErrorString(e));
   ix->steps_run++;
   if (k_new) {
-    e = wi_launch_append(ix->g, ix->b, k_new, v_new, ix->appended, st);
+    const WiGeom& g = ix->g;
+    e = wi_launch_append(g, ix->b, k_new, v_new, ix->appended, st);
     if (e != cudaSuccess) return fail(WI_ECUDA, "append launch: %s", cudaGetErrorString(e));
     ix->appended++;
+    // decode-time index maintenance: once the local window holds W + seg_len rows, its oldest
+    // seg_len rows become one more segment (every seg_len appended tokens)
+    if (ix->grown_host < g.Gmax && ix->appended == (ix->grown_host + 1) * g.S) {
+      const int gi = ix->grown_host;
+      e = wi_launch_grow(g, ix->b, ix->gw, ix->mu, ix->valsum, ix->valsum16, ix->cnt, ix->off, ix->perm,
+                         ix->nonempty, gi, wi_budget(g, g.Cb + (gi + 1) * g.Cs), ix->err, st);
+      if (e != cudaSuccess) return fail(WI_ECUDA, "index growth launch: %s", cudaGetErrorString(e));
+      ix->grown_host++;
+    }
   }
   return WI_OK;
 }
@@ -687,11 +772,10 @@ int wi_kmeans_step(const wi_config* cfg, const void* k, const void* centroids, i
   }
   const size_t cb = (size_t)g.U * g.nseg * g.Cs * 128 * 2;
   WI_LAUNCH(cudaMemsetAsync(err, 0, 4, st));
-  WI_LAUNCH(wi_launch_invnorm(k, s.invnorm, (long long)g.U * g.n, st));
   WI_LAUNCH(cudaMemcpyAsync(s.chat, centroids, cb, cudaMemcpyDeviceToDevice, st));
   WI_LAUNCH(wi_launch_assign(g, k, s.chat, assign, err, st));
   WI_LAUNCH(wi_launch_segment_sort(g, assign, s.seg_counts, s.seg_offsets, s.slots, err, st));
-  WI_LAUNCH(wi_launch_centroid_update(g, k, s.invnorm, s.seg_counts, s.seg_offsets, s.slots, s.chat, st));
+  WI_LAUNCH(wi_launch_centroid_update(g, k, s.seg_counts, s.seg_offsets, s.slots, s.chat, st));
   WI_LAUNCH(cudaMemcpyAsync(new_centroids, s.chat, cb, cudaMemcpyDeviceToDevice, st));
   {
     int herr = 0;

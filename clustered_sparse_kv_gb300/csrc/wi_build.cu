@@ -5,13 +5,14 @@
 // into segments that are clustered independently; fr 2.A.2 names spherical
 // k-means; zh 2.A names the precomputed per-cluster value sum that the
 // estimation zone reads.  Kernels here:
-//   invnorm          1/|K_i| per token (fp32)
 //   init_centroids   c_j = bf16(K_p / |K_p|), p = segment start + stride * j
 //   assign (SIMT)    a_i = argmax_j K_i . c_j, ties to the lowest j
 //   segment_sort     counting sort of a segment's tokens by (cluster, position)
 //   centroid_update  c_j = bf16(u_j / |u_j|), u_j = sum of member K_i / |K_i|
-//   final_reduce     counts, row offsets, perm, mu_j = bf16(mean K), valsum_j
-//   permute          in-place cluster-contiguous reorder of K and V rows
+//   reduce_gather    counts, row offsets, perm, mu_j = bf16(mean K), valsum_j,
+//                    and the members' K / V rows gathered cluster by cluster
+//   scatter_back     the gathered rows written back: K and V cluster-contiguous
+//   gather_rows      the gather alone, by a given perm (an imported index)
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -39,16 +40,6 @@ __global__ void k_to_bf16(const float4* __restrict__ in, uint2* __restrict__ out
   const float4 x = in[i];
   const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
   out[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
-}
-
-__global__ void k_invnorm(const bf16* __restrict__ K, float* __restrict__ invnorm, long long rows) {
-  const int lane = threadIdx.x & 31;
-  const long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (r >= rows) return;
-  float x[4];
-  load_bf16x4(K + r * WI_D + 4 * lane, x);
-  const float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
-  if (lane == 0) invnorm[r] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
 }
 
 __global__ void k_init_centroids(const bf16* __restrict__ K, bf16* __restrict__ chat, int total, int nseg, int S,
@@ -201,11 +192,13 @@ __global__ void __launch_bounds__(512) k_segment_sort(const int32_t* __restrict_
 }
 
 // One warp per cluster: c_j = bf16(u_j / |u_j|), u_j = sum over members (in
-// position order) of K_i * (1/|K_i|).  Empty clusters keep c_j.
-__global__ void k_centroid_update(const bf16* __restrict__ K, const float* __restrict__ invnorm,
-                                  const int* __restrict__ seg_counts, const int* __restrict__ seg_offsets,
-                                  const int* __restrict__ slots, bf16* __restrict__ chat, int total, int S, int Cs,
-                                  int nseg, long long n) {
+// position order) of K_i * (1/|K_i|), the norm taken in fp32 from the row
+// itself.  Eight member rows in flight per warp.  Empty clusters keep c_j.
+constexpr int kUpdRows = 8;
+__global__ void __launch_bounds__(256) k_centroid_update(const bf16* __restrict__ K, const int* __restrict__ seg_counts,
+                                                         const int* __restrict__ seg_offsets,
+                                                         const int* __restrict__ slots, bf16* __restrict__ chat,
+                                                         int total, int S, int Cs, int nseg, long long n) {
   const int lane = threadIdx.x & 31;
   const int gid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (gid >= total) return;
@@ -214,35 +207,24 @@ __global__ void k_centroid_update(const bf16* __restrict__ K, const float* __res
   if (m == 0) return;
   const int b = seg_offsets[(long long)su * (Cs + 1) + cl];
   const int* sl = slots + (long long)su * S + b;
-  const long long rowbase = (long long)u * n + (long long)s * S;
+  const bf16* Kb = K + ((long long)u * n + (long long)s * S) * WI_D + 4 * lane;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  int t = 0;
-  for (; t + 4 <= m; t += 4) {
-    long long r[4];
-    uint2 w[4];
-    float iv[4];
+  for (int t0 = 0; t0 < m; t0 += kUpdRows) {
+    uint2 w[kUpdRows];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) r[i] = rowbase + sl[t + i];
+    for (int i = 0; i < kUpdRows; ++i)
+      w[i] = t0 + i < m ? ldg_u2(Kb + (long long)sl[t0 + i] * WI_D) : make_uint2(0u, 0u);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      w[i] = ldg_u2(K + r[i] * WI_D + 4 * lane);
-      iv[i] = __ldg(invnorm + r[i]);
+    for (int i = 0; i < kUpdRows; ++i) {
+      if (t0 + i < m) {  // warp-uniform
+        float x[4];
+        unpack_bf16x4(w[i], x);
+        const float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
+        const float iv = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] = fmaf(x[e], iv, acc[e]);
+      }
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float x[4];
-      unpack_bf16x4(w[i], x);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[e] = fmaf(x[e], iv[i], acc[e]);
-    }
-  }
-  for (; t < m; ++t) {
-    const long long r = rowbase + sl[t];
-    float x[4];
-    load_bf16x4(K + r * WI_D + 4 * lane, x);
-    const float iv = __ldg(invnorm + r);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[e] = fmaf(x[e], iv, acc[e]);
   }
   const float nrm = sqrtf(warp_sum(acc[0] * acc[0] + acc[1] * acc[1] + acc[2] * acc[2] + acc[3] * acc[3]));
   bf16* o = chat + (size_t)gid * WI_D + 4 * lane;
@@ -250,76 +232,78 @@ __global__ void k_centroid_update(const bf16* __restrict__ K, const float* __res
   for (int e = 0; e < 4; ++e) o[e] = __float2bfloat16_rn(nrm > 0.f ? acc[e] / nrm : 0.f);
 }
 
-// One warp per cluster of the final assignment: count, row offset, perm,
-// mu = bf16(sum K / count), valsum = sum V (fp32), in position order.
-__global__ void k_final_reduce(const bf16* __restrict__ K, const bf16* __restrict__ V,
-                               const int* __restrict__ seg_counts, const int* __restrict__ seg_offsets,
-                               const int* __restrict__ slots, bf16* __restrict__ mu, float* __restrict__ valsum,
-                               int* __restrict__ cnt, int* __restrict__ off, int* __restrict__ perm,
-                               int* __restrict__ nonempty, int U, int C, int S, int Cs, int nseg, long long n,
-                               int n_sink, int W, int n_idx) {
+// One warp per cluster of the final assignment, for the units [u0, u0 + nu):
+// count, row offset, perm, mu = bf16(sum K / count), valsum = sum V (fp32),
+// summed in position order, and the member rows copied in that order to the
+// cluster's slots in the scratch rows tK / tV of the batch (the gather half
+// of the in-place permutation).  The C clusters of each unit land in arrays
+// of row stride Cst (offsets Cst + 1), perm in rows of pst slots.
+__global__ void __launch_bounds__(256) k_reduce_gather(
+    const bf16* __restrict__ K, const bf16* __restrict__ V, const int* __restrict__ seg_counts,
+    const int* __restrict__ seg_offsets, const int* __restrict__ slots, bf16* __restrict__ mu,
+    float* __restrict__ valsum, int* __restrict__ cnt, int* __restrict__ off, int* __restrict__ perm,
+    int* __restrict__ nonempty, bf16* __restrict__ tK, bf16* __restrict__ tV, int u0, int nu, int C, int Cst, int S,
+    int Cs, int nseg, long long n, int n_sink, int W, int pst, int n_idx) {
   const int lane = threadIdx.x & 31;
   const long long gid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (gid >= (long long)U * C) return;
-  const int u = (int)(gid / C), c = (int)(gid % C), s = c / Cs, cl = c % Cs;
+  if (gid >= (long long)nu * C) return;
+  const int ub = (int)(gid / C), u = u0 + ub, c = (int)(gid % C), s = c / Cs, cl = c % Cs;
+  const long long dst = (long long)u * Cst + c;
   const long long su = (long long)u * nseg + s;
   const int m = seg_counts[su * Cs + cl];
   const int b = seg_offsets[su * (Cs + 1) + cl];
   const long long slot0 = seg_slot_base(s, S, n, n_sink, W) + b;
   if (lane == 0) {
-    off[(long long)u * (C + 1) + c] = (int)slot0;
-    if (c == C - 1) off[(long long)u * (C + 1) + C] = (int)(n - W);
-    cnt[gid] = m;
+    off[(long long)u * (Cst + 1) + c] = (int)slot0;
+    if (c == C - 1) off[(long long)u * (Cst + 1) + C] = (int)(n - W);
+    cnt[dst] = m;
     if (m > 0) atomicAdd(&nonempty[u], 1);
   }
   const int* sl = slots + su * S + b;
-  const long long rowbase = (long long)u * n;
-  for (int t = lane; t < m; t += 32) perm[(long long)u * n_idx + (slot0 - n_sink) + t] = s * S + sl[t];
+  for (int t = lane; t < m; t += 32) perm[(long long)u * pst + (slot0 - n_sink) + t] = s * S + sl[t];
+  const long long rowbase = (long long)u * n + (long long)s * S;
+  const long long trow = (long long)ub * n_idx + (slot0 - n_sink);  // the cluster's first scratch row
   float ak[4] = {0.f, 0.f, 0.f, 0.f}, av[4] = {0.f, 0.f, 0.f, 0.f};
-  int t = 0;
-  for (; t + 4 <= m; t += 4) {
-    uint2 wk[4], wv[4];
+  constexpr int R = 8;
+  for (int t0 = 0; t0 < m; t0 += R) {
+    uint2 wk[R], wv[R];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const long long r = rowbase + (long long)s * S + sl[t + i];
-      wk[i] = ldg_u2(K + r * WI_D + 4 * lane);
-      wv[i] = ldg_u2(V + r * WI_D + 4 * lane);
+    for (int i = 0; i < R; ++i) {
+      const long long r = rowbase + (t0 + i < m ? sl[t0 + i] : 0);
+      wk[i] = t0 + i < m ? ldg_u2(K + r * WI_D + 4 * lane) : make_uint2(0u, 0u);
+      wv[i] = t0 + i < m ? ldg_u2(V + r * WI_D + 4 * lane) : make_uint2(0u, 0u);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float xk[4], xv[4];
-      unpack_bf16x4(wk[i], xk);
-      unpack_bf16x4(wv[i], xv);
+    for (int i = 0; i < R; ++i) {
+      if (t0 + i < m) {  // warp-uniform
+        reinterpret_cast<uint2*>(tK + (trow + t0 + i) * WI_D)[lane] = wk[i];
+        reinterpret_cast<uint2*>(tV + (trow + t0 + i) * WI_D)[lane] = wv[i];
+        float xk[4], xv[4];
+        unpack_bf16x4(wk[i], xk);
+        unpack_bf16x4(wv[i], xv);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) { ak[e] += xk[e]; av[e] += xv[e]; }
+        for (int e = 0; e < 4; ++e) { ak[e] += xk[e]; av[e] += xv[e]; }
+      }
     }
   }
-  for (; t < m; ++t) {
-    const long long r = rowbase + (long long)s * S + sl[t];
-    float xk[4], xv[4];
-    load_bf16x4(K + r * WI_D + 4 * lane, xk);
-    load_bf16x4(V + r * WI_D + 4 * lane, xv);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) { ak[e] += xk[e]; av[e] += xv[e]; }
-  }
-  bf16* mo = mu + gid * WI_D + 4 * lane;
+  bf16* mo = mu + dst * WI_D + 4 * lane;
   float4 vo;
   const float fm = (float)m;
 #pragma unroll
   for (int e = 0; e < 4; ++e) mo[e] = __float2bfloat16_rn(m > 0 ? ak[e] / fm : 0.f);
   vo.x = av[0]; vo.y = av[1]; vo.z = av[2]; vo.w = av[3];
-  *reinterpret_cast<float4*>(valsum + gid * WI_D + 4 * lane) = vo;
+  *reinterpret_cast<float4*>(valsum + dst * WI_D + 4 * lane) = vo;
 }
 
 // Cluster-contiguous reorder, through a scratch copy of units [u0, u0+nu):
 // tmp[r] = rows[perm[r]] for every clustered slot r, then copied back.
 __global__ void k_gather_rows(const bf16* __restrict__ K, const bf16* __restrict__ V, const int* __restrict__ perm,
-                              bf16* __restrict__ tK, bf16* __restrict__ tV, int u0, long long n, int n_idx) {
+                              bf16* __restrict__ tK, bf16* __restrict__ tV, int u0, long long n, int n_idx, int pst) {
   const int lane = threadIdx.x & 31;
   const long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int u = u0 + blockIdx.y;
   if (r >= n_idx) return;
-  const long long src = (long long)u * n + perm[(long long)u * n_idx + r];
+  const long long src = (long long)u * n + perm[(long long)u * pst + r];
   const long long dst = (long long)blockIdx.y * n_idx + r;
   reinterpret_cast<uint2*>(tK + dst * WI_D)[lane] = ldg_u2(K + src * WI_D + 4 * lane);
   reinterpret_cast<uint2*>(tV + dst * WI_D)[lane] = ldg_u2(V + src * WI_D + 4 * lane);
@@ -346,12 +330,6 @@ cudaError_t wi_launch_to_bf16(const float* in, void* out, long long n, cudaStrea
   if (n4 <= 0) return cudaSuccess;
   k_to_bf16<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(reinterpret_cast<const float4*>(in),
                                                            static_cast<uint2*>(out), n4);
-  return cudaGetLastError();
-}
-
-cudaError_t wi_launch_invnorm(const void* K, float* invnorm, long long rows, cudaStream_t st) {
-  const long long blocks = (rows + 7) / 8;
-  k_invnorm<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const bf16*>(K), invnorm, rows);
   return cudaGetLastError();
 }
 
@@ -390,26 +368,36 @@ cudaError_t wi_launch_segment_sort(const WiGeom& g, const int32_t* assign, int* 
   return cudaGetLastError();
 }
 
-cudaError_t wi_launch_centroid_update(const WiGeom& g, const void* K, const float* invnorm, const int* seg_counts,
-                                      const int* seg_offsets, const int* slots, void* chat, cudaStream_t st) {
+cudaError_t wi_launch_centroid_update(const WiGeom& g, const void* K, const int* seg_counts, const int* seg_offsets,
+                                      const int* slots, void* chat, cudaStream_t st) {
   const int total = g.U * g.nseg * g.Cs;
-  k_centroid_update<<<(total + 7) / 8, 256, 0, st>>>(static_cast<const bf16*>(K), invnorm, seg_counts, seg_offsets,
-                                                      slots, static_cast<bf16*>(chat), total, g.S, g.Cs, g.nseg,
-                                                      g.n);
+  k_centroid_update<<<(total + 7) / 8, 256, 0, st>>>(static_cast<const bf16*>(K), seg_counts, seg_offsets, slots,
+                                                      static_cast<bf16*>(chat), total, g.S, g.Cs, g.nseg, g.n);
   return cudaGetLastError();
 }
 
-cudaError_t wi_launch_final_reduce(const WiGeom& g, const void* K, const void* V, const int* seg_counts,
-                                   const int* seg_offsets, const int* slots, void* mu, float* valsum, int* cnt,
-                                   int* off, int* perm, int* nonempty, cudaStream_t st) {
+cudaError_t wi_launch_reduce_permute(const WiGeom& g, void* K, void* V, const int* seg_counts, const int* seg_offsets,
+                                     const int* slots, void* mu, float* valsum, int* cnt, int* off, int* perm,
+                                     int* nonempty, void* tmpK, void* tmpV, int batch_units, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(nonempty, 0, sizeof(int) * g.U, st);
   if (e != cudaSuccess) return e;
-  const long long total = (long long)g.U * g.C;
-  k_final_reduce<<<(unsigned)((total + 7) / 8), 256, 0, st>>>(
-      static_cast<const bf16*>(K), static_cast<const bf16*>(V), seg_counts, seg_offsets, slots,
-      static_cast<bf16*>(mu), valsum, cnt, off, perm, nonempty, g.U, g.C, g.S, g.Cs, g.nseg, g.n, g.n_sink, g.W,
-      g.n_idx);
-  return cudaGetLastError();
+  if (batch_units < 1) return cudaErrorInvalidValue;
+  for (int u0 = 0; u0 < g.U; u0 += batch_units) {
+    const int nu = g.U - u0 < batch_units ? g.U - u0 : batch_units;
+    const long long warps = (long long)nu * g.Cb;
+    k_reduce_gather<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(
+        static_cast<const bf16*>(K), static_cast<const bf16*>(V), seg_counts, seg_offsets, slots,
+        static_cast<bf16*>(mu), valsum, cnt, off, perm, nonempty, static_cast<bf16*>(tmpK),
+        static_cast<bf16*>(tmpV), u0, nu, g.Cb, g.C, g.S, g.Cs, g.nseg, g.n, g.n_sink, g.W, g.perm_stride, g.n_idx);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (g.n_idx == 0) continue;
+    const long long words = (long long)g.n_idx * WI_D / 8;
+    dim3 g2((unsigned)((words + 255) / 256), nu);
+    k_scatter_back<<<g2, 256, 0, st>>>(static_cast<bf16*>(K), static_cast<bf16*>(V), static_cast<const bf16*>(tmpK),
+                                       static_cast<const bf16*>(tmpV), u0, g.n, g.n_sink, g.n_idx);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t wi_launch_permute(const WiGeom& g, void* K, void* V, const int* perm, void* tmpK, void* tmpV, int u0,
@@ -417,7 +405,8 @@ cudaError_t wi_launch_permute(const WiGeom& g, void* K, void* V, const int* perm
   if (g.n_idx == 0 || nu == 0) return cudaSuccess;
   dim3 g1((unsigned)((g.n_idx + 7) / 8), nu);
   k_gather_rows<<<g1, 256, 0, st>>>(static_cast<const bf16*>(K), static_cast<const bf16*>(V), perm,
-                                    static_cast<bf16*>(tmpK), static_cast<bf16*>(tmpV), u0, g.n, g.n_idx);
+                                    static_cast<bf16*>(tmpK), static_cast<bf16*>(tmpV), u0, g.n, g.n_idx,
+                                    g.perm_stride);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long words = (long long)g.n_idx * WI_D / 8;

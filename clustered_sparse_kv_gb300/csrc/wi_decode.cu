@@ -535,10 +535,12 @@ struct TopkArgs {
   int4* splits;  // [U][G][NS+2]  (position, row inside that cluster, split's first selected row, 0)
   int4* sruns;   // [U][G][NS+1][32] runs of positions splits[b].x .. +31 (one read for the split's CTA)
   const int* app_count;
+  const int* kcur;   // budget of the clusters held so far (grows with the index)
+  const int* grown;  // segments grown during decode: their seg_len rows each left the local window
   float* part1;  // estimation partials [U][G][PE]
   const unsigned* kmaxp;  // [U][P1][G] largest key over the non-empty clusters of each k_scores CTA
   int* err;
-  int U, G, C, kmax, NS, PE, n_sink, W, P1;
+  int U, G, C, kmax, NS, PE, n_sink, W, P1, seg_len;
   float lam;
 };
 
@@ -724,7 +726,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   const KeySrc key_of{cached ? ks : nullptr, s};
   uint16_t* kbin = reinterpret_cast<uint16_t*>(ks);  // [C] distance bins (0xFFFF: empty cluster) if !cached
   constexpr uint32_t kFarBin = 64 * 30;               // log_bin(2^30): the far keys' bins start here
-  int kk = min(kmax, a.nonempty[u]);
+  int kk = min(min(*a.kcur, kmax), a.nonempty[u]);
   // the first keys' loads are in flight across the K0 reduction and the barrier below
   const int n4 = C / 4;
   uint4 f[4];
@@ -932,7 +934,8 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
     int4* sruns = a.sruns + uh * NSP * 32;
     if (tid < NSP) {
       int4 sp = make_int4(0, 0, 0, 0);
-      const long long S = (long long)a.n_sink + a.W + max(*a.app_count, 0), T = S + R;
+      const long long S = (long long)a.n_sink + a.W + max(*a.app_count, 0) - (long long)*a.grown * a.seg_len,
+                      T = S + R;
       const int rb = (int)max(0LL, (T * tid) / NSP - S);
       if (R > 0 && rb < R) {
         int lo = 0, hi = kk - 1;  // largest position whose first row is <= rb
@@ -987,7 +990,8 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
     const int NSP = a.NS + 1;
     int4 sp = make_int4(kk, 0, R, 0);
     if (tid < NSP) {
-      const long long S = (long long)a.n_sink + a.W + max(*a.app_count, 0), T = S + R;
+      const long long S = (long long)a.n_sink + a.W + max(*a.app_count, 0) - (long long)*a.grown * a.seg_len,
+                      T = S + R;
       const int rb = (int)max(0LL, (T * tid) / NSP - S);
       if (R > 0 && rb < R) {
         int lo = 0, hi = kk - 1;  // largest position whose first row is <= rb
@@ -1120,6 +1124,10 @@ struct ExactArgs {
   const bf16* appK;
   const bf16* appV;
   const int* app_count;
+  const bf16* grownK;  // [gmax][U][seg_len][128]: rows of the segments grown during decode
+  const bf16* grownV;
+  const int* grown;    // segments grown so far
+  int gmax, seg_len, U;
   const int* selcnt;
   const int4* runs;
   const int4* splits;
@@ -1255,15 +1263,29 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
     StagePacker pk{st, full, empty, nrows, a.err};
     const int amax = a.max_append > 0 ? a.max_append : 1;
     if (split == 0) {
-      // ---- steady rows first: sinks and local window are fixed since the build (copied before
-      // the wait), appended rows after it
+      // ---- steady rows first: the sinks and (in an index that cannot grow) the build's local window
+      // are fixed since the build (copied before the wait), the rest of the window after it
       const size_t w0 = (size_t)(a.n - a.W) * WI_D;
-      pk.push(lane == 0 ? Ku : Ku + w0, lane == 0 ? Vu : Vu + w0, lane == 0 ? a.n_sink : (lane == 1 ? a.W : 0));
+      const int wl = a.gmax == 0 ? a.W : 0;
+      pk.push(lane == 0 ? Ku : Ku + w0, lane == 0 ? Vu : Vu + w0, lane == 0 ? a.n_sink : (lane == 1 ? wl : 0));
     }
     pdl_wait();
+    const int ngrown = a.gmax > 0 ? min(*a.grown, a.gmax) : 0;
     if (split == 0) {
       const int na = *a.app_count;
-      pk.push(a.appK + (size_t)u * amax * WI_D, a.appV + (size_t)u * amax * WI_D, lane == 0 ? na : 0);
+      const bf16* Ka = a.appK + (size_t)u * amax * WI_D;
+      const bf16* Va = a.appV + (size_t)u * amax * WI_D;
+      if (a.gmax == 0) {
+        pk.push(Ka, Va, lane == 0 ? na : 0);
+      } else {
+        // the window starts past the grown segments: the build's window rows not grown yet, then the
+        // appended rows not grown yet
+        const int gs = ngrown * a.seg_len;
+        const int wrem = max(a.W - gs, 0), a0 = min(max(gs - a.W, 0), na);
+        const size_t wr = (size_t)(a.n - wrem) * WI_D;
+        pk.push(lane == 0 ? Ku + wr : Ka + (size_t)a0 * WI_D, lane == 0 ? Vu + wr : Va + (size_t)a0 * WI_D,
+                lane == 0 ? wrem : (lane == 1 ? na - a0 : 0));
+      }
     }
     // ---- selected clusters: rows [b_s, b_{s+1}) of the head's row-balanced split, 32 runs per
     // batch; one round trip gives the split bounds and the copies of its first 32 runs
@@ -1278,8 +1300,14 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
       const int4 rr = (pos + lane < kk) ? (pos == sa.x ? r0 : runs[pos + lane]) : make_int4(0, 0, 0, 0);
       const int i_in = lane == 0 ? in : 0;
       const bool valid = pos + lane < kk;
-      // a run must lie inside the clustered rows; anything else is reported, never copied
-      const bool sane = !valid || (i_in >= 0 && i_in <= rr.y && rr.x >= a.n_sink && (long long)rr.x + rr.y <= a.n - a.W);
+      // a run must lie inside the build's clustered rows or (rows n.. : a grown segment's slots, seg_len
+      // per segment) inside one grown segment; anything else is reported, never copied
+      const bool in_grown = valid && (long long)rr.x >= a.n;
+      const int gr = in_grown ? (int)((long long)rr.x - a.n) : 0;
+      const int gseg = in_grown ? gr / a.seg_len : 0, goff = in_grown ? gr % a.seg_len : 0;
+      const bool sane = !valid || (i_in >= 0 && i_in <= rr.y &&
+                                   (in_grown ? (gseg < ngrown && goff + rr.y <= a.seg_len)
+                                             : (rr.x >= a.n_sink && (long long)rr.x + rr.y <= a.n - a.W)));
       if (__any_sync(0xffffffffu, !sane)) {
         if (lane == 0) atomicOr(a.err, WI_DEVERR_BAD_ROW);
         break;
@@ -1287,8 +1315,9 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
       const int len = valid ? rr.y - i_in : 0;
       const int before = warp_inclusive_scan(len) - len;
       const int take = max(0, min(len, rows_left - before));
-      const size_t r = (size_t)(rr.x + i_in) * WI_D;
-      pk.push(Ku + r, Vu + r, take);
+      const size_t o = in_grown ? (((size_t)gseg * a.U + u) * a.seg_len + goff + i_in) * WI_D
+                                : (size_t)(rr.x + i_in) * WI_D;
+      pk.push((in_grown ? a.grownK : Ku) + o, (in_grown ? a.grownV : Vu) + o, take);  // whole warp
       rows_left -= __shfl_sync(0xffffffffu, warp_inclusive_scan(take), 31);
       in = 0;
       pos += 32;
@@ -1675,6 +1704,9 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   t.splits = b.splits;
   t.kmaxp = b.kmaxp;
   t.app_count = b.app_count;
+  t.kcur = b.kcur;
+  t.grown = b.grown;
+  t.seg_len = g.S;
   t.W = g.W;
   t.P1 = b.p1;
   t.sruns = b.sruns;
@@ -1697,6 +1729,12 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   a.appK = static_cast<const bf16*>(b.appK);
   a.appV = static_cast<const bf16*>(b.appV);
   a.app_count = b.app_count;
+  a.grownK = static_cast<const bf16*>(b.grownK);
+  a.grownV = static_cast<const bf16*>(b.grownV);
+  a.grown = b.grown;
+  a.gmax = g.Gmax;
+  a.seg_len = g.S;
+  a.U = g.U;
   a.selcnt = b.selcnt;
   a.runs = b.runs;
   a.splits = b.splits;

@@ -11,17 +11,27 @@ struct WiGeom {
   int U;          // units = batch * layers * n_kv_heads
   int G;          // query heads per kv head
   int S, Cs;      // segment length, clusters per segment
-  int nseg;       // segments per unit
-  int C;          // clusters per unit
+  int nseg;       // segments per unit at build
+  int Cb;         // clusters per unit of the build's segments = nseg * Cs
+  int Gmax;       // segments that decode-time growth may add: max_append / S
+  int C;          // clusters per unit the index holds room for = Cb + Gmax * Cs (row stride of every
+                  // per-cluster array; clusters of segments not grown yet are empty)
   long long n;    // built tokens per unit
   int n_sink, W;  // steady zone
-  int n_idx;      // clustered tokens per unit = n - n_sink - W
+  int n_idx;      // clustered tokens per unit at build = n - n_sink - W
+  int perm_stride;  // slots per unit in perm = n_idx + Gmax * S
   int iters;
-  int kmax;       // retrieval budget
+  int kbuild;     // retrieval budget over the build's clusters
+  int kmax;       // retrieval budget over all C clusters (the largest it can grow to)
   int max_append;
   int vs16;       // decode reads the bf16 copy of the value sums
   int grp;        // group-shared retrieval: one top-k per kv head from the heads' summed scores
+  double budget_frac;
+  int budget_k;
 };
+
+// Retrieval budget for C clusters: budget_k if set, else ceil(budget_frac * C).
+int wi_budget(const WiGeom& g, int C);
 
 int wi_geom_from_config(const wi_config* cfg, WiGeom* g, char* msg, size_t msglen);
 void wi_set_error(const char* msg);  // sets the thread-local message of wi_last_error()
@@ -29,17 +39,20 @@ void wi_set_error(const char* msg);  // sets the thread-local message of wi_last
 // ---- build kernels (wi_build.cu); all enqueue on `st` and return the launch status
 // out[i] = bf16(in[i]), round to nearest even.
 cudaError_t wi_launch_to_bf16(const float* in, void* out, long long n, cudaStream_t st);
-cudaError_t wi_launch_invnorm(const void* K, float* invnorm, long long rows, cudaStream_t st);
 cudaError_t wi_launch_init_centroids(const WiGeom& g, const void* K, void* chat, cudaStream_t st);
 cudaError_t wi_launch_assign(const WiGeom& g, const void* K, const void* chat, int32_t* assign, int* err,
                              cudaStream_t st);
 cudaError_t wi_launch_segment_sort(const WiGeom& g, const int32_t* assign, int* seg_counts, int* seg_offsets,
                                    int* slots, int* err, cudaStream_t st);
-cudaError_t wi_launch_centroid_update(const WiGeom& g, const void* K, const float* invnorm, const int* seg_counts,
-                                      const int* seg_offsets, const int* slots, void* chat, cudaStream_t st);
-cudaError_t wi_launch_final_reduce(const WiGeom& g, const void* K, const void* V, const int* seg_counts,
-                                   const int* seg_offsets, const int* slots, void* mu, float* valsum, int* cnt,
-                                   int* off, int* perm, int* nonempty, cudaStream_t st);
+cudaError_t wi_launch_centroid_update(const WiGeom& g, const void* K, const int* seg_counts, const int* seg_offsets,
+                                      const int* slots, void* chat, cudaStream_t st);
+// B4 + B5: the final index of the g.Cb build clusters of every unit (arrays of row stride g.C, offsets
+// g.C + 1, perm g.perm_stride; nonempty cleared first) and the in-place cluster-contiguous permutation
+// of K and V, batch_units units at a time through the scratch rows tmpK / tmpV (batch_units * n_idx
+// rows each).
+cudaError_t wi_launch_reduce_permute(const WiGeom& g, void* K, void* V, const int* seg_counts, const int* seg_offsets,
+                                     const int* slots, void* mu, float* valsum, int* cnt, int* off, int* perm,
+                                     int* nonempty, void* tmpK, void* tmpV, int batch_units, cudaStream_t st);
 cudaError_t wi_launch_permute(const WiGeom& g, void* K, void* V, const int* perm, void* tmpK, void* tmpV,
                               int u0, int nu, cudaStream_t st);
 size_t wi_assign_smem_bytes(const WiGeom& g);
@@ -65,6 +78,10 @@ struct WiDecodeBufs {
   void* appK;
   void* appV;
   int* app_count;
+  const void* grownK;     // [Gmax][U][S][128] rows of the segments grown during decode, cluster-contiguous
+  const void* grownV;
+  int* grown;             // segments grown so far (device)
+  int* kcur;              // retrieval budget of the clusters held so far (device)
   float* scores;          // [U][G][C] order-preserving score keys (uint32; 0 = empty cluster)
   float* part1;           // [U][G][p_es][WI_PART]  estimation partials
   int* sel;               // [U][G][kmax]
@@ -101,4 +118,27 @@ cudaError_t wi_launch_decode(const WiGeom& g, const WiDecodeBufs& b, const void*
 cudaError_t wi_launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t st);
 cudaError_t wi_launch_append(const WiGeom& g, const WiDecodeBufs& b, const void* k_new, const void* v_new, int t,
                              cudaStream_t st);
+
+// ---- decode-time index maintenance (wi_grow.cu): the oldest S rows of the local window become
+// segment `gi` of the grown part (B1-B5 on that one segment), merged into the index.
+struct WiGrowBufs {
+  // one segment of every unit: [U][S] tokens, [U][Cs] clusters
+  void* chat;
+  int32_t* assign;
+  int* seg_counts;
+  int* seg_offsets;
+  int* slots;
+  void* mu;
+  float* valsum;
+  int* cnt;
+  int* off;
+  int* perm;
+  int* nonempty;
+  void* tK;   // permutation scratch [U][S][128]
+  void* tV;
+};
+cudaError_t wi_launch_set_int(int* p, int v, cudaStream_t st);
+cudaError_t wi_launch_grow(const WiGeom& g, const WiDecodeBufs& b, const WiGrowBufs& w, void* mu, float* valsum,
+                           void* valsum16, int* cnt, int* off, int* perm, int* nonempty, int gi, int k_after,
+                           int* err, cudaStream_t st);
 

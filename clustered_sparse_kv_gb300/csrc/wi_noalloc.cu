@@ -58,10 +58,9 @@ extern "C" int wi_kmeans_step_noalloc(const wi_config* cfg, const void* k, const
   if (!k || !centroids || !assign || !new_centroids)
     return nfail(WI_EINVAL, "k, centroids, assign and new_centroids must be non-NULL");
   // scratch layout inside the static array
-  const size_t SU = (size_t)g.U * g.nseg, rows = (size_t)g.U * g.n;
+  const size_t SU = (size_t)g.U * g.nseg;
   const size_t o_err = 0;
-  const size_t o_inv = align256(o_err + 4);
-  const size_t o_cnt = align256(o_inv + rows * 4);
+  const size_t o_cnt = align256(o_err + 4);
   const size_t o_off = align256(o_cnt + SU * g.Cs * 4);
   const size_t o_slot = align256(o_off + SU * (g.Cs + 1) * 4);
   const size_t o_chat = align256(o_slot + SU * g.S * 4);
@@ -69,7 +68,7 @@ extern "C" int wi_kmeans_step_noalloc(const wi_config* cfg, const void* k, const
   if (need > kWiNoallocScratchBytes) {
     snprintf(msg, sizeof(msg),
              "problem needs %zu bytes of scratch; the no-allocation round is limited to %zu bytes "
-             "(about 340K tokens at 512 clusters per 8192-token segment): use wi_kmeans_step",
+             "(about 400K tokens at 512 clusters per 8192-token segment): use wi_kmeans_step",
              need, kWiNoallocScratchBytes);
     return nfail(WI_EINVAL, msg);
   }
@@ -79,7 +78,6 @@ extern "C" int wi_kmeans_step_noalloc(const wi_config* cfg, const void* k, const
   if (e != cudaSuccess || !sym) return nfail(WI_ECUDA, "cudaGetSymbolAddress(no-allocation scratch)", e);
   unsigned char* base = static_cast<unsigned char*>(sym);
   int* err = reinterpret_cast<int*>(base + o_err);
-  float* invnorm = reinterpret_cast<float*>(base + o_inv);
   int* seg_counts = reinterpret_cast<int*>(base + o_cnt);
   int* seg_offsets = reinterpret_cast<int*>(base + o_off);
   int* slots = reinterpret_cast<int*>(base + o_slot);
@@ -87,13 +85,12 @@ extern "C" int wi_kmeans_step_noalloc(const wi_config* cfg, const void* k, const
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t cb = SU * g.Cs * 128 * 2;
   if ((e = cudaMemsetAsync(err, 0, 4, st)) != cudaSuccess) return nfail(WI_ECUDA, "clear error word", e);
-  if ((e = wi_launch_invnorm(k, invnorm, (long long)rows, st)) != cudaSuccess) return nfail(WI_ECUDA, "invnorm", e);
   if ((e = cudaMemcpyAsync(chat, centroids, cb, cudaMemcpyDeviceToDevice, st)) != cudaSuccess)
     return nfail(WI_ECUDA, "copy centroids", e);
   if ((e = wi_launch_assign(g, k, chat, assign, err, st)) != cudaSuccess) return nfail(WI_ECUDA, "assign", e);
   if ((e = wi_launch_segment_sort(g, assign, seg_counts, seg_offsets, slots, err, st)) != cudaSuccess)
     return nfail(WI_ECUDA, "segment sort", e);
-  if ((e = wi_launch_centroid_update(g, k, invnorm, seg_counts, seg_offsets, slots, chat, st)) != cudaSuccess)
+  if ((e = wi_launch_centroid_update(g, k, seg_counts, seg_offsets, slots, chat, st)) != cudaSuccess)
     return nfail(WI_ECUDA, "centroid update", e);
   if ((e = cudaMemcpyAsync(new_centroids, chat, cb, cudaMemcpyDeviceToDevice, st)) != cudaSuccess)
     return nfail(WI_ECUDA, "copy centroids out", e);

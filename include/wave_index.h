@@ -59,8 +59,12 @@ typedef struct wi_index wi_index; /* opaque, library-owned */
  * k-means (summary fr 2.A.2).  Retrieval budget (summary zh section 3):
  * k = budget_k if > 0, else ceil(budget_frac * C), C = all clusters of a unit;
  * capped at the unit's non-empty clusters at decode time.
+ * Decode-time growth (an extension: the pages describe the index at prefill):
+ * the index holds room for C = (n_ctx / seg_len + max_append / seg_len) *
+ * clusters_per_seg clusters per unit; those of segments not grown yet are
+ * empty, and the budget k counts only the clusters held so far.
  * Limits of this build (WI_EUNSUPPORTED beyond them): n_q_heads / n_kv_heads
- * <= 8, k <= 4096, seg_len <= 16384, C <= 65536.
+ * <= 8, k <= 4096, seg_len <= 16384, C <= 65536 (room for growth included).
  */
 typedef struct {
   int batch, layers, n_q_heads, n_kv_heads, head_dim; /* head_dim == 128 */
@@ -69,7 +73,8 @@ typedef struct {
   int clusters_per_seg;   /* multiple of 16 in [16, 512] dividing seg_len */
   int iters;              /* k-means rounds (assignments), >= 1 */
   int n_sink, local_window;
-  int max_append;         /* capacity of the decode-time append buffer, >= 0 */
+  int max_append;         /* capacity of the decode-time append buffer, >= 0; with max_append >=
+                             seg_len the index also grows during decode (wi_decode_step) */
   double budget_frac;
   int budget_k;
   int valsum_bf16;        /* 0: decode reads the fp32 value sums; 1: it reads a bf16 copy made at
@@ -100,11 +105,12 @@ int wi_build_index(const wi_config* cfg, void* k, void* v, const void* init_cent
 
 /*
  * Adopt an index computed elsewhere instead of clustering (e.g. by a CPU
- * reference).  counts: [units][C] int32; perm: [units][n_ctx - n_sink -
+ * reference).  counts: [units][Cb] int32, Cb = (n_ctx / seg_len) *
+ * clusters_per_seg (the build's clusters); perm: [units][n_ctx - n_sink -
  * local_window] int32, the original position of every clustered slot in
  * cluster-contiguous order (slots of cluster j follow those of cluster j-1;
- * slot numbering starts at row n_sink); mu: bf16 [units][C][128] mean keys;
- * valsum: fp32 [units][C][128] value sums.  All four are "any" pointers and
+ * slot numbering starts at row n_sink); mu: bf16 [units][Cb][128] mean keys;
+ * valsum: fp32 [units][Cb][128] value sums.  All four are "any" pointers and
  * are copied.  k, v as in wi_build_index (permuted in place by perm).
  * Returns WI_EINVAL if perm is not a bijection on the clustered positions
  * consistent with counts and segments (checked on the host).
@@ -113,10 +119,15 @@ int wi_index_import(const wi_config* cfg, void* k, void* v, const int32_t* count
                     const uint16_t* mu, const float* valsum, void* stream, wi_index** out);
 
 /*
- * Copy the index out ("any" pointers; any of them may be NULL to skip it).
+ * Copy the index out ("any" pointers; any of them may be NULL to skip it),
+ * C = the clusters per unit from wi_index_shape (room for growth included).
  * counts [units][C], offsets [units][C+1] (row of the first slot of each
- * cluster; offsets[C] = n_ctx - local_window), perm as in wi_index_import,
- * mu bf16 [units][C][128], valsum fp32 [units][C][128].  Asynchronous.
+ * cluster; offsets[Cb] = n_ctx - local_window; a grown segment g's slots are
+ * rows n_ctx + g*seg_len + slot), perm [units][n_ctx - n_sink - local_window
+ * + (max_append / seg_len) * seg_len] (as in wi_index_import, then every grown
+ * segment's seg_len slots; -1 where nothing has grown yet), mu bf16
+ * [units][C][128], valsum fp32 [units][C][128].  Clusters not grown yet have
+ * count 0 and zero mean key and value sum.  Asynchronous.
  */
 int wi_index_export(const wi_index* ix, int32_t* counts, int32_t* offsets, int32_t* perm, uint16_t* mu,
                     float* valsum, void* stream);
@@ -132,8 +143,17 @@ int wi_index_export(const wi_index* ix, int32_t* counts, int32_t* offsets, int32
  * far.  If k_new and v_new (device bf16 [batch][layers][n_kv_heads][128]) are
  * non-NULL, that token is appended AFTER this step's attention; returns
  * WI_EFULL (nothing enqueued) when max_append tokens are already appended.
+ * Appended tokens join the local window.  When an append leaves the window
+ * holding local_window + seg_len rows (every seg_len appended tokens), the
+ * step also grows the index: the window's oldest seg_len rows become one more
+ * segment, clustered like a build segment (same seeds rule, iters rounds,
+ * counts / mean keys / value sums; its rows copied, cluster-contiguous, into
+ * library memory), its clusters take the next free ids and the budget is
+ * recomputed for the clusters held.
  * Uses only library-owned scratch: no allocation and no host synchronisation.
- * Steps without append replay correctly from a captured CUDA graph.
+ * Steps without append replay correctly from a captured CUDA graph (a graph
+ * captured before a growth keeps attending over the grown index correctly:
+ * the growth state lives in device memory).
  */
 int wi_decode_step(wi_index* ix, const void* q, const void* k_new, const void* v_new, float* out, void* stream);
 
@@ -186,8 +206,10 @@ int wi_dense_decode(wi_index* ix, const void* q, float* out, void* stream);
  */
 int wi_decode_kernel(wi_index* ix, int kernel, const void* q, float* out, void* stream);
 
-/* Sizes of an index: units, clusters per unit, k_max (the budget), group g,
- * tokens appended so far (host-side count).  Any output pointer may be NULL. */
+/* Sizes of an index: units, clusters per unit C (room for decode-time growth
+ * included), k_max (the budget for C clusters, the largest it can grow to),
+ * group g, tokens appended so far (host-side count).  Any output pointer may
+ * be NULL. */
 int wi_index_shape(const wi_index* ix, int* units, int* clusters, int* k_max, int* group, int* appended);
 
 /*
@@ -255,7 +277,7 @@ int wi_profile_read(wi_index* ix, double* kernel_ms, int* steps, unsigned long l
  * such callers cannot let a clustering round call cudaMalloc.  Same
  * arguments, same results as wi_kmeans_step; its scratch is a fixed 8 MiB
  * device array that every GPU loading this library holds until the process
- * exits.  Problems that need more scratch (about 340K tokens in total at 512
+ * exits.  Problems that need more scratch (about 400K tokens in total at 512
  * clusters per 8192-token segment) return WI_EINVAL with a message.
  * All calls share the array: calls whose work overlaps on the GPU race on it
  * (order them on one stream).  Every call looks up the array's device

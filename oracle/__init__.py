@@ -21,6 +21,10 @@ Parity status per function (what pins it is in ``tests/test_oracle_pins.py``):
                               the default; brute-force summed-score top-k;
                               all clusters = full attention)
   lse_merge           pinned (associativity against the single sum)
+  grow_unit_index     pinned (a grown segment equals build_unit_index of
+                              that segment alone; all clusters after growth
+                              = textbook softmax; singleton grown clusters
+                              make the estimate exact)
   full_attention      pinned (equals decode_unit with every cluster
                               retrieved; one row gives its value row;
                               identical keys give the mean value row;
@@ -33,7 +37,10 @@ from .bf16 import bf16_round, bf16_from_bits, bf16_to_bits, fp32_round  # noqa: 
 from .wave_index import (  # noqa: F401
     IndexParams,
     steady_positions,
+    window_start,
     indexed_positions,
+    grown_segments,
+    grow_unit_index,
     budget_k,
     init_centroids,
     assign,

@@ -67,6 +67,11 @@ def steady_positions(n: int, p: IndexParams) -> np.ndarray:
     return np.concatenate([lo, hi])
 
 
+def window_start(n: int, p: IndexParams) -> int:
+    """First position of the build's local window (the steady zone's tail)."""
+    return max(n - p.local_window, min(p.n_sink, n))
+
+
 def indexed_positions(n: int, p: IndexParams) -> np.ndarray:
     """Positions that are clustered: the complement of the steady zone."""
     mask = np.ones(n, bool)
@@ -192,6 +197,65 @@ def build_unit_index(K: np.ndarray, V: np.ndarray, p: IndexParams, c_init: list 
     }
 
 
+def grown_segments(n_appended: int, p: IndexParams) -> int:
+    """Segments added during decode after n_appended appended tokens.
+
+    READING (decode-time index maintenance; the pages describe the index at
+    prefill only): appended tokens join the local window; once a step's append
+    leaves the window holding local_window + seg_len rows, its oldest seg_len
+    rows become one more segment, so the window is back to local_window rows.
+    That happens after every seg_len appended tokens.
+    """
+    return n_appended // p.seg_len
+
+
+def grow_unit_index(index: dict, K_all: np.ndarray, V_all: np.ndarray, n: int, p: IndexParams) -> dict:
+    """The index of one unit after decode-time growth (see grown_segments).
+
+    K_all, V_all hold the n built rows followed by every appended row.
+    Grown segment g covers positions [w0 + g*S, w0 + (g+1)*S), w0 = the
+    build's window start; it is clustered on its own like a build segment
+    (segmented clustering, de/fr/zh 2.A: the seeds, the spherical rounds and
+    the per-cluster count, mean key and value sum), every position of it
+    clustered, and its clusters are numbered after all existing ones.  Its
+    slots are numbered from row n + g*S (the build's slots end below row n).
+    """
+    S, Cs = p.seg_len, p.clusters_per_seg
+    grown = grown_segments(K_all.shape[0] - n, p)
+    w0 = window_start(n, p)
+    C0 = index["counts"].shape[0]
+    d = K_all.shape[1]
+    counts = [index["counts"]]
+    mus, vss, perms, offs = [index["mu"]], [index["valsum"]], [index["perm"]], [index["offsets"][:-1]]
+    assignment = np.full(K_all.shape[0], -1, np.int64)
+    assignment[:n] = index["assignment"][:n]
+    for g in range(grown):
+        pos = w0 + g * S + np.arange(S)
+        a, _ = spherical_kmeans(K_all[pos], np.arange(S), p)
+        ids = C0 + g * Cs + a
+        assignment[pos] = ids
+        cnt = np.bincount(a, minlength=Cs).astype(np.int64)
+        order = np.argsort(a, kind="stable")        # by cluster, by position inside a cluster
+        ksum = np.zeros((Cs, d))
+        vsum = np.zeros((Cs, d))
+        np.add.at(ksum, a, K_all[pos])
+        np.add.at(vsum, a, V_all[pos])
+        mu = np.zeros((Cs, d))
+        ne = cnt > 0
+        mu[ne] = bf16_round(ksum[ne] / cnt[ne, None])
+        counts.append(cnt)
+        mus.append(mu)
+        vss.append(fp32_round(vsum))
+        perms.append(pos[order])
+        offs.append(n + g * S + np.concatenate([[0], np.cumsum(cnt)[:-1]]))
+    out = dict(index)
+    out.update({"counts": np.concatenate(counts), "mu": np.concatenate(mus), "valsum": np.concatenate(vss),
+                "perm": np.concatenate(perms), "assignment": assignment, "grown": grown})
+    offsets = np.concatenate(offs)
+    out["offsets"] = np.concatenate([offsets, [offsets[-1] + out["counts"][-1]]])
+    return out
+
+
 def build_index(K: np.ndarray, V: np.ndarray, p: IndexParams, **kw) -> list:
     """Index of every unit; K, V shaped [units][n][d] (float64)."""
     return [build_unit_index(K[u], V[u], p, **kw) for u in range(K.shape[0])]
@@ -249,12 +313,17 @@ def decode_unit(q_heads: np.ndarray, K: np.ndarray, V: np.ndarray, index: dict, 
     C = counts.shape[0]
     nonempty = counts > 0
     k = budget_k(C, p)
-    steady = steady_positions(n, p)
+    if k_app is not None and k_app.shape[0] > 0:
+        K = np.concatenate([K, k_app])
+        V = np.concatenate([V, v_app])
+    if a.shape[0] < K.shape[0]:      # appended positions not clustered (yet)
+        a = np.concatenate([a, np.full(K.shape[0] - a.shape[0], -1)])
+    # steady zone: the sinks, and the local window from its start (past any grown segment) to the
+    # last appended token
+    w = window_start(n, p) + index.get("grown", 0) * p.seg_len
+    steady = np.concatenate([np.arange(min(p.n_sink, n)), np.arange(w, K.shape[0])])
     ks = K[steady]
     vsd = V[steady]
-    if k_app is not None and k_app.shape[0] > 0:
-        ks = np.concatenate([ks, k_app])
-        vsd = np.concatenate([vsd, v_app])
     out = np.zeros((q_heads.shape[0], d))
     info = []
     R_group = select_topk(mu @ q_heads.sum(axis=0), nonempty, k) if group_topk else None

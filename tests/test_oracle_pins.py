@@ -492,3 +492,79 @@ def test_group_topk_variant_pins():
     wa = tiny_workload(n=1024, S=256, Cs=16, g=4, budget_k=10 ** 6, seed=17)
     np.testing.assert_allclose(oracle.decode(Q, K, V, idx, params_of(wa), 4, group_topk=True),
                                oracle.full_attention(Q, K, V), rtol=0, atol=1e-12)
+
+
+# ------------------------------------------- decode-time index maintenance ----
+
+def grown_case(n=2048, S=256, Cs=16, W=8, n_sink=4, appended=600, iters=3, seed=12, budget_k=3):
+    w = tiny_workload(n=n, S=S, Cs=Cs, g=2, iters=iters, n_sink=n_sink, window=W, budget_k=budget_k, seed=seed)
+    K, V, Q = gen_unit(w)
+    ka, va = kvsynth.kv_cache(w, p0=n, p1=n + appended)
+    KA = oracle.bf16_from_bits(ka).reshape(appended, D)
+    VA = oracle.bf16_from_bits(va).reshape(appended, D)
+    p = params_of(w)
+    idx = oracle.build_unit_index(K[0], V[0], p)
+    K_all, V_all = np.concatenate([K[0], KA]), np.concatenate([V[0], VA])
+    return w, p, K[0], V[0], Q[0], KA, VA, K_all, V_all, idx
+
+
+def test_grown_segment_equals_build_of_that_segment_alone():
+    """A segment added during decode is clustered exactly like a build segment of its own
+    (segments are independent, de/fr/zh 2.A): its counts, mean keys, value sums, member order
+    and assignment equal build_unit_index run on those seg_len rows alone (no steady zone)."""
+    w, p, K, V, Q, KA, VA, K_all, V_all, idx = grown_case()
+    n, S, Cs = w.n_ctx, p.seg_len, p.clusters_per_seg
+    assert oracle.grown_segments(600, p) == 2
+    gi = oracle.grow_unit_index(idx, K_all, V_all, n, p)
+    C0 = idx["counts"].shape[0]
+    assert gi["counts"].shape[0] == C0 + 2 * Cs and gi["grown"] == 2
+    w0 = n - p.local_window
+    p_alone = IndexParams(seg_len=S, clusters_per_seg=Cs, iters=p.iters, n_sink=0, local_window=0)
+    n_idx = idx["perm"].size
+    for g in range(2):
+        pos = w0 + g * S + np.arange(S)
+        ref = oracle.build_unit_index(K_all[pos], V_all[pos], p_alone)
+        sl = slice(C0 + g * Cs, C0 + (g + 1) * Cs)
+        np.testing.assert_array_equal(gi["counts"][sl], ref["counts"])
+        np.testing.assert_array_equal(gi["mu"][sl], ref["mu"])
+        np.testing.assert_array_equal(gi["valsum"][sl], ref["valsum"])
+        np.testing.assert_array_equal(gi["assignment"][pos], C0 + g * Cs + ref["assignment"])
+        np.testing.assert_array_equal(gi["perm"][n_idx + g * S:n_idx + (g + 1) * S], pos[ref["perm"]])
+        np.testing.assert_array_equal(gi["offsets"][sl], n + g * S + ref["offsets"][:-1])
+    # the build's part is untouched; the window past the grown segments is not clustered
+    np.testing.assert_array_equal(gi["counts"][:C0], idx["counts"])
+    np.testing.assert_array_equal(gi["assignment"][:w0], idx["assignment"][:w0])
+    assert np.all(gi["assignment"][w0 + 2 * S:] == -1)
+    assert gi["counts"].sum() == idx["counts"].sum() + 2 * S
+
+
+def test_all_clusters_after_growth_is_full_attention():
+    """Every cluster retrieved after growth: the zones partition the n + appended tokens, so the
+    output is textbook softmax attention over all of them (1e-12)."""
+    w, p, K, V, Q, KA, VA, K_all, V_all, idx = grown_case(budget_k=10 ** 6)
+    gi = oracle.grow_unit_index(idx, K_all, V_all, w.n_ctx, p)
+    o = oracle.decode_unit(Q, K, V, gi, p, KA, VA)
+    for h in range(Q.shape[0]):
+        np.testing.assert_allclose(o[h], textbook_attention(Q[h], K_all, V_all), rtol=1e-12, atol=1e-14)
+
+
+def test_singleton_grown_clusters_make_estimation_exact():
+    """clusters_per_seg = seg_len: every cluster, grown ones included, holds one token, so the
+    estimate is exact for any budget and the output is full attention."""
+    w, p, K, V, Q, KA, VA, K_all, V_all, idx = grown_case(n=1024, S=128, Cs=128, appended=300, budget_k=2)
+    gi = oracle.grow_unit_index(idx, K_all, V_all, w.n_ctx, p)
+    assert gi["grown"] == 2 and gi["counts"].max() == 1
+    o = oracle.decode_unit(Q, K, V, gi, p, KA, VA)
+    for h in range(Q.shape[0]):
+        np.testing.assert_allclose(o[h], textbook_attention(Q[h], K_all, V_all), rtol=1e-10, atol=1e-12)
+
+
+def test_budget_counts_grown_clusters():
+    """k = ceil(budget_frac * C) counts the grown segments' clusters too."""
+    w, p, K, V, Q, KA, VA, K_all, V_all, idx = grown_case(budget_k=0)
+    p = IndexParams(seg_len=p.seg_len, clusters_per_seg=p.clusters_per_seg, iters=p.iters, n_sink=p.n_sink,
+                    local_window=p.local_window, budget_frac=0.05)
+    gi = oracle.grow_unit_index(idx, K_all, V_all, w.n_ctx, p)
+    _, info = oracle.decode_unit(Q, K, V, gi, p, KA, VA, details=True)
+    C = gi["counts"].shape[0]
+    assert len(info[0]["selected"]) == math.ceil(0.05 * C) == math.ceil(0.05 * (128 + 32))
