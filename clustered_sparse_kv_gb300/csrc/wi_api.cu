@@ -275,10 +275,19 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   if (ns > 64) ns = 64;
   if (ns < 1) ns = 1;
   b.nsplit = ns;
-  // dense comparator: row ranges per unit so that all CTAs fill the SMs once
-  int ds = (int)((wi_dense_ctas_per_sm(G) * (size_t)sms + U - 1) / U);
-  if (ds > 256) ds = 256;
-  if (ds < 1) ds = 1;
+  // dense comparator: row ranges per unit such that the U * ranges CTAs come closest to whole waves
+  // (a partial last wave idles SMs), at least 1024 rows each; the fewest ranges among equals
+  int ds = 1;
+  {
+    const long long slots = (long long)wi_dense_ctas_per_sm(G) * sms;
+    double best = -1.0;
+    for (int d = 1; d <= 256; ++d) {
+      if (d > 1 && g.n / d < 1024) break;
+      const long long ctas = (long long)U * d, waves = (ctas + slots - 1) / slots;
+      const double eff = (double)ctas / (double)(waves * slots);
+      if (eff > best + 1e-9) { best = eff; ds = d; }
+    }
+  }
   b.dsplits = ds;
   A(b.dpart, U * G * (size_t)ds * WI_PART * 4);
   A(b.dticket, U * 4);
@@ -447,7 +456,9 @@ int wi_build_index(const wi_config* cfg, void* k, void* v, const void* init_cent
   BuildScratch s;
   void *tK = nullptr, *tV = nullptr;
   int nb = 0;
-  if ((rc = alloc_index(ix, st)) != WI_OK || (rc = scratch_alloc(g, &s, st)) != WI_OK) {
+  // every allocation of the build first: the build's kernels then run back to back
+  if ((rc = alloc_index(ix, st)) != WI_OK || (rc = scratch_alloc(g, &s, st)) != WI_OK ||
+      (rc = perm_scratch(g, &tK, &tV, &nb, st)) != WI_OK) {
     scratch_free(&s, st);
     destroy(ix);
     return rc;
@@ -471,7 +482,6 @@ int wi_build_index(const wi_config* cfg, void* k, void* v, const void* init_cent
       WI_LAUNCH(wi_launch_centroid_update(g, k, s.seg_counts, s.seg_offsets, s.slots, s.chat, st));
   }
   // the final index and the in-place permutation, one pass over K and V for both
-  if ((rc = perm_scratch(g, &tK, &tV, &nb, st)) != WI_OK) goto done;
   WI_LAUNCH(wi_launch_reduce_permute(g, k, v, s.seg_counts, s.seg_offsets, s.slots, ix->mu, ix->valsum, ix->cnt,
                                      ix->off, ix->perm, ix->nonempty, tK, tV, nb, st));
   if (g.vs16) WI_LAUNCH(wi_launch_to_bf16(ix->valsum, ix->valsum16, (long long)g.U * g.C * 128, st));

@@ -19,6 +19,7 @@
 
 #include "wi_common.cuh"
 #include "wi_internal.h"
+#include "wi_pipe.cuh"
 
 namespace {
 
@@ -214,15 +215,21 @@ __global__ void __launch_bounds__(256) k_centroid_update(const bf16* __restrict_
 #pragma unroll
     for (int i = 0; i < kUpdRows; ++i)
       w[i] = t0 + i < m ? ldg_u2(Kb + (long long)sl[t0 + i] * WI_D) : make_uint2(0u, 0u);
+    // the eight rows' squared norms in one warp transpose-reduction (lanes 4i..4i+3 end with row i's)
+    float x[kUpdRows][4], ss[kUpdRows];
 #pragma unroll
     for (int i = 0; i < kUpdRows; ++i) {
-      if (t0 + i < m) {  // warp-uniform
-        float x[4];
-        unpack_bf16x4(w[i], x);
-        const float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
-        const float iv = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+      unpack_bf16x4(w[i], x[i]);
+      ss[i] = x[i][0] * x[i][0] + x[i][1] * x[i][1] + x[i][2] * x[i][2] + x[i][3] * x[i][3];
+    }
+    const float sq = transpose_reduce<kUpdRows>(ss);
+    const float ivl = sq > 0.f ? 1.0f / sqrtf(sq) : 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] = fmaf(x[e], iv, acc[e]);
+    for (int i = 0; i < kUpdRows; ++i) {
+      const float iv = __shfl_sync(0xffffffffu, ivl, 4 * i);
+      if (t0 + i < m) {  // warp-uniform
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] = fmaf(x[i][e], iv, acc[e]);
       }
     }
   }
