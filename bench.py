@@ -447,7 +447,9 @@ def dense_record(wi, torch, timer, w, replicas, qs, outs, steps, chunk, hbm, pea
     return {"kernel": "k_dense_decode", "steps": reps * n, "ms_per_step": d_ms,
             "value": w.batch * w.layers / (d_ms / 1e3), "unit": UNIT, "bytes_per_step": d_bytes,
             "hbm_gbs": d_gbs, "peak": hbm, "frac": d_gbs / hbm, "peak_kind": peak_kind,
-            "wave_index_speedup": d_ms / wave_ms}
+            "wave_index_speedup": d_ms / wave_ms,
+            # against a full-attention pass that would stream its bytes at the measured copy peak
+            "wave_index_speedup_vs_dense_at_peak": d_bytes / (hbm * 1e9) / (wave_ms * 1e-3)}
 
 
 def measure_config(wi, torch, timer, name, dev, hbm, tf_burst, peak_kind, steps, dense_steps):

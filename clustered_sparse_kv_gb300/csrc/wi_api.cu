@@ -261,11 +261,16 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   b.p1 = p1;
   // the estimation CTAs share a launch with the U*G top-k CTAs (one CTA per SM each)
   int pe = env_int("WI_ESTIMATE_CTAS_PER_UNIT", 0);
-  if (pe <= 0) pe = (size_t)U * G < (size_t)sms ? (int)((sms - U * G) / U) : p1;
+  // with many heads the top-k CTAs fill the SMs beside the estimation CTAs, which need about 0.6 of
+  // the SMs to keep HBM streaming: round(0.6 * SMs / U) per unit
+  if (pe <= 0) pe = (size_t)U * G < (size_t)sms ? (int)((sms - U * G) / U) : (int)((6 * (size_t)sms + 5 * U) / (10 * U));
   if (pe > tiles) pe = tiles;
   if (pe > 256) pe = 256;
   if (pe < 1) pe = 1;
   b.p_es = pe;
+  // estimation CTAs that fit in one wave go first, so their stream overlaps the top-k CTAs
+  const int ef = env_int("WI_ESTIMATE_FIRST", -1);
+  b.est_first = ef >= 0 ? (ef != 0) : ((size_t)U * pe < (size_t)sms);
   // exact attention: (splits + 1 steady CTA) per head.  Few heads: fill two CTAs per SM in one wave
   // (the step is a latency chain); many heads: about two waves of split CTAs, so that the heads'
   // unequal row counts balance across the SMs

@@ -541,6 +541,7 @@ struct TopkArgs {
   const unsigned* kmaxp;  // [U][P1][G] largest key over the non-empty clusters of each k_scores CTA
   int* err;
   int U, G, C, kmax, NS, PE, n_sink, W, P1, seg_len;
+  int est_first;  // the estimation CTAs take the first block indices (they start before the top-k CTAs)
   float lam;
 };
 
@@ -1083,13 +1084,18 @@ template <int G, typename VT, bool GRP>
 __global__ void __launch_bounds__(kSThreads, 1) k_select_estimate(TopkArgs a) {
   extern __shared__ __align__(128) unsigned char se_raw[];
   pdl_trigger();
-  const int nsel = GRP ? a.U : a.U * a.G;
-  if ((int)blockIdx.x < nsel) {
+  const int nsel = GRP ? a.U : a.U * a.G, nest = a.U * a.PE;
+  // block order: the top-k CTAs first, or (when the estimation CTAs fit in one wave beside them) the
+  // estimation CTAs first, so that their HBM stream overlaps the top-k instead of following it
+  const int bi = blockIdx.x;
+  const bool sel = a.est_first ? bi >= nest : bi < nsel;
+  if (sel) {
+    const int si = a.est_first ? bi - nest : bi;
     pdl_wait();
     // a query head's row, or with group-shared retrieval the unit's summed-score row G
-    select_role<G, GRP>(se_raw, a, GRP ? (int)blockIdx.x : (int)blockIdx.x / a.G, GRP ? a.G : (int)blockIdx.x % a.G);
+    select_role<G, GRP>(se_raw, a, GRP ? si : si / a.G, GRP ? a.G : si % a.G);
   } else {
-    const int e = blockIdx.x - nsel;
+    const int e = a.est_first ? bi : bi - nsel;
     estimate_role<G, VT, G + (GRP ? 1 : 0)>(se_raw, static_cast<const VT*>(a.valsum), a.cnt, a.scores, a.part1,
                                             a.C, e / a.PE, e % a.PE, a.PE, a.lam, a.err);
   }
@@ -1720,6 +1726,7 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   t.PE = b.p_es;
   t.lam = lam;
   t.n_sink = g.n_sink;
+  t.est_first = b.est_first;
   if (mask & 2u) e = launch_select<G>(g, b, t, st);
   if (e != cudaSuccess || (e = mark(ev, 2, st)) != cudaSuccess) return e;
   ExactArgs a;

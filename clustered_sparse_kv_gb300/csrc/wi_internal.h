@@ -98,6 +98,7 @@ struct WiDecodeBufs {
   int* err;
   int p1;                 // k_scores CTAs per unit
   int p_es;               // estimation CTAs per unit (= estimation partials per head)
+  int est_first;          // the select/estimate launch starts its estimation CTAs first
   int nsplit;             // exact_merge CTAs per head over the selected rows (plus one for steady rows)
   // dense comparator (full attention)
   float* dpart;           // [U][G][dsplits][WI_PART]  row-range partials

@@ -217,8 +217,10 @@ int wi_index_shape(const wi_index* ix, int* units, int* clusters, int* k_max, in
  * from the device's SM count: scores CTAs per unit, estimation CTAs per unit,
  * and exact-attention splits per head over the selected rows (one more CTA
  * takes the steady rows).  The environment variables WI_D1_CTAS_PER_UNIT,
- * WI_ESTIMATE_CTAS_PER_UNIT and WI_D3_SPLITS (positive integers), read when
- * the index is made, override the defaults.  Results do not depend on the
+ * WI_ESTIMATE_CTAS_PER_UNIT and WI_D3_SPLITS (positive integers), and
+ * WI_ESTIMATE_FIRST (0 or 1: the estimation CTAs before the top-k CTAs in
+ * their shared launch; default: when they fit in one wave), read when the
+ * index is made, override the defaults.  Results do not depend on the
  * layout beyond float rounding order.  Any output pointer may be NULL.
  */
 int wi_decode_layout(const wi_index* ix, int* score_ctas, int* estimate_ctas, int* exact_splits);

@@ -145,3 +145,67 @@ def test_one_million_tokens_one_kv_head(wi):
         got = out.cpu().numpy().reshape(w.units, w.group, 128).astype(np.float64)
         check_step(w, [0], k, v, exp, qb, got, ids.cpu().numpy(), cnt.cpu().numpy())
     ix.free()
+
+
+def test_one_million_tokens_32_layers_full_size(wi):
+    """The million-token, 32-layer workload at full size (256 units, 137 GB generated on the
+    device), built by the library and decoded in the launch configuration the benchmark times;
+    two sampled units (layer 0 kv head 0, layer 31 kv head 7) checked against the oracle given the
+    exported index, on two steps.  The build permutes the cache in place, so the sampled units'
+    original rows are kept aside first."""
+    w = kvsynth.get_workload("llama3-8b-1m-32l")
+    assert (w.units, w.clusters) == (256, 65536)
+    gen = kvsynth.DeviceGen(w)
+    kt, vt = gen.kv_cache()
+    sample = [0, 255]
+    k_orig = [kt.view(w.units, w.n_ctx, 128)[u].cpu().numpy().view(np.uint16) for u in sample]
+    v_orig = [vt.view(w.units, w.n_ctx, 128)[u].cpu().numpy().view(np.uint16) for u in sample]
+    ix = wi.WaveIndex.build(wi.config_from_workload(w), kt, vt)
+    torch.cuda.synchronize()
+    ix.check()
+    layout = wi.wi_decode_layout(ix.handle)
+    assert layout == {"score_ctas": 1, "estimate_ctas": 1, "exact_splits": 1}
+    p = params_of(w)
+    kk = oracle.budget_k(w.clusters, p)
+    I = oracle.indexed_positions(w.n_ctx, p)
+    # the sampled units' index, exported one array at a time (full-size device copies, then sliced)
+    exp = {}
+    for name, shape, dt in (("counts", (w.units, w.clusters), torch.int32),
+                            ("perm", (w.units, w.n_ctx - w.n_sink - w.local_window), torch.int32),
+                            ("mu", (w.units, w.clusters, 128), torch.int16),
+                            ("valsum", (w.units, w.clusters, 128), torch.float32)):
+        t = torch.empty(shape, dtype=dt, device="cuda")
+        wi.wi_index_export(ix.handle, **{name: t})
+        torch.cuda.synchronize()
+        exp[name] = [t[u].cpu().numpy() for u in sample]
+        del t
+        torch.cuda.empty_cache()
+    idx = []
+    for i in range(len(sample)):
+        counts, perm_u = exp["counts"][i], exp["perm"][i]
+        assert counts.sum() == I.size
+        np.testing.assert_array_equal(np.sort(perm_u), I)
+        idx.append({"counts": counts.astype(np.int64), "valsum": exp["valsum"][i].astype(np.float64),
+                    "mu": oracle.bf16_from_bits(exp["mu"][i].view(np.uint16)).reshape(w.clusters, 128),
+                    "assignment": assignment_from_index(counts, perm_u, w.n_ctx, p.n_sink)})
+    KV = [(oracle.bf16_from_bits(k_orig[i]), oracle.bf16_from_bits(v_orig[i])) for i in range(len(sample))]
+    for step in range(2):
+        qd = gen.queries(step)
+        out = ix.decode(qd)
+        ids, cnt = ix.selection()
+        torch.cuda.synchronize()
+        ix.check()
+        got = out.cpu().numpy().reshape(w.units, w.group, 128).astype(np.float64)
+        assert np.isfinite(got).all()
+        Q = oracle.bf16_from_bits(qd.cpu().numpy().view(np.uint16)).reshape(w.units, w.group, 128)
+        ids, cnt = ids.cpu().numpy(), cnt.cpu().numpy()
+        for i, u in enumerate(sample):
+            ref, info = oracle.decode_unit(Q[u], KV[i][0], KV[i][1], idx[i], p, details=True)
+            err = rel_l2(got[u], ref)
+            assert err.max() <= OUT_REL_L2, (step, u, err.max())
+            ne = idx[i]["counts"] > 0
+            for h in range(w.group):
+                check_topk(ids[u, h], cnt[u, h], info[h]["scores"], ne, kk)
+    ix.free()
+    del kt, vt
+    torch.cuda.empty_cache()

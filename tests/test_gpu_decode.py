@@ -314,6 +314,30 @@ def test_exact_split_counts(wi, monkeypatch, splits):
     ix.free()
 
 
+@pytest.mark.parametrize("est_first,pe", [(0, 3), (1, 3), (1, 1)])
+def test_select_estimate_block_orders(wi, monkeypatch, est_first, pe):
+    """The top-k / estimation launch with either role first in block order, and 1 or 3 estimation
+    CTAs per unit, gives the oracle's output."""
+    w = small(batch=2, n_q_heads=8, n_kv_heads=2, n_ctx=4096, seg_len=1024, clusters_per_seg=64, iters=2,
+              budget_k=12, seed=6)
+    k, v, q, K, V, Q = gen(w)
+    p = params_of(w)
+    idx = oracle.build_index(K, V, p)
+    monkeypatch.setenv("WI_ESTIMATE_FIRST", str(est_first))
+    monkeypatch.setenv("WI_ESTIMATE_CTAS_PER_UNIT", str(pe))
+    ix = wi.WaveIndex.adopt(wi.config_from_workload(w), dev16(k), dev16(v), *index_arrays(idx))
+    assert wi.wi_decode_layout(ix.handle)["estimate_ctas"] == pe
+    for t in range(2):
+        qb = kvsynth.queries(w, step=t)
+        out = ix.decode(dev16(qb)).cpu().numpy()
+        ix.check()
+        Qt = oracle.bf16_from_bits(qb).reshape(w.units, w.group, 128)
+        ref = oracle.decode(Qt, K, V, idx, p, w.group)
+        err = rel_l2(out.reshape(w.units, w.group, 128).astype(np.float64), ref)
+        assert err.max() <= OUT_REL_L2, (t, err.max())
+    ix.free()
+
+
 def _bf16_valsum_index(idx):
     """The bf16 value-sum variant's definition: the stored fp32 value sums rounded to bf16."""
     return [{**d, "valsum": oracle.bf16_round(oracle.fp32_round(d["valsum"]))} for d in idx]
