@@ -193,11 +193,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_assign_tc(const __grid_constant
     const int cols = P.N / 2;           // columns per group per half (multiple of 32)
     bool ok = true;                     // after one timed-out wait the warp stops waiting but keeps
                                         // meeting the epilogue barriers, so no warp is left behind
+    // the row's running argmax as kChains independent chains over interleaved columns (column i goes
+    // to chain i % kChains, each chain keeps its first maximum), so that the compares do not form one
+    // dependent chain; combined at the end with ties to the lowest column
+    constexpr int kChains = 8;
     for (int t = t0; t < t1; ++t) {
       const int it = t - t0;
       const int su = t / tiles_per_seg, mt = t % tiles_per_seg;
-      float bv = -INFINITY;
-      int bj = 0x7fffffff;
+      float cv[kChains];
+      int cj[kChains];
+#pragma unroll
+      for (int c = 0; c < kChains; ++c) { cv[c] = -INFINITY; cj[c] = 0x7fffffff; }
       for (int h = 0; h < P.halves && ok; ++h) {
         if (!mbar_wait(&sm.tmem_full[h], it & 1, P.err)) { ok = false; sm.abort_flag = 1; break; }
         tc_fence_after();
@@ -212,13 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_assign_tc(const __grid_constant
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float v = __uint_as_float(r0[i]);
-            if (v > bv) { bv = v; bj = col + i; }
+            if (v > cv[i % kChains]) { cv[i % kChains] = v; cj[i % kChains] = col + i; }
           }
           if (c0 + 32 < cols) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float v = __uint_as_float(r1[i]);
-              if (v > bv) { bv = v; bj = col + 32 + i; }
+              if (v > cv[i % kChains]) { cv[i % kChains] = v; cj[i % kChains] = col + 32 + i; }
             }
           }
         }
@@ -226,6 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_assign_tc(const __grid_constant
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.tmem_empty[h]);
       }
+      float bv = cv[0];
+      int bj = cj[0];
+#pragma unroll
+      for (int c = 1; c < kChains; ++c)
+        if (cv[c] > bv || (cv[c] == bv && cj[c] < bj)) { bv = cv[c]; bj = cj[c]; }
       sm.best_v[cgroup][row] = bv;
       sm.best_j[cgroup][row] = bj;
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");

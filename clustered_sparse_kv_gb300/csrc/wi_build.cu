@@ -128,62 +128,86 @@ __global__ void __launch_bounds__(256) k_assign_simt(const bf16* __restrict__ K,
   }
 }
 
-// Counting sort of one segment's clustered tokens by (cluster, position).
-// Outputs per segment-unit: counts [Cs], offsets [Cs+1] (local slots),
-// slots [S] (position relative to the segment start, in slot order).
-__global__ void __launch_bounds__(512) k_segment_sort(const int32_t* __restrict__ assign,
-                                                      int* __restrict__ seg_counts, int* __restrict__ seg_offsets,
-                                                      int* __restrict__ slots, int S, int Cs, int nseg, long long n,
-                                                      int* err) {
+// Counting sort of one segment's clustered tokens by (cluster, position),
+// stable and in O(S): each of the 16 warps takes a contiguous chunk of the
+// segment's positions; pass 1 counts per (warp, cluster) (match_any groups the
+// lanes of one cluster, whose leader adds the group's size); a scan turns the
+// counts into each warp's first slot per cluster (clusters in order, warps in
+// position order inside a cluster); pass 2 walks every chunk again in position
+// order and gives each lane its slot = that start + its rank among the lanes
+// of its cluster.  Outputs per segment-unit: counts [Cs], offsets [Cs+1]
+// (local slots), slots [S] (position relative to the segment start, in slot
+// order).
+constexpr int kSortWarps = 16;
+__global__ void __launch_bounds__(32 * kSortWarps) k_segment_sort(const int32_t* __restrict__ assign,
+                                                                  int* __restrict__ seg_counts,
+                                                                  int* __restrict__ seg_offsets,
+                                                                  int* __restrict__ slots, int S, int Cs, int nseg,
+                                                                  long long n, int* err) {
   extern __shared__ __align__(16) int ss_raw[];
-  int* cnt = ss_raw;          // [Cs]
-  int* off = cnt + Cs;        // [Cs + 1]
-  int* cur = off + Cs + 1;    // [Cs]
-  int* tmp = cur + Cs;        // [32]
-  int* sa = tmp + 32;         // [S]
-  int* sb = sa + S;           // [S]
+  int* wc = ss_raw;                   // [kSortWarps][Cs] counts, then first slots
+  int* cnt = wc + kSortWarps * Cs;    // [Cs]
+  int* off = cnt + Cs;                // [Cs + 1]
+  int* tmp = off + Cs + 1;            // [32]
+  int* sb = tmp + 32;                 // [S] sorted positions
   const int su = blockIdx.x, u = su / nseg, s = su % nseg;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t* a = assign + (long long)u * n + (long long)s * S;
-  for (int j = tid; j < Cs; j += blockDim.x) { cnt[j] = 0; cur[j] = 0; }
+  const int chunk = (S + kSortWarps - 1) / kSortWarps;
+  const int p0 = warp * chunk, p1 = min(S, p0 + chunk);
+  for (int i = tid; i < kSortWarps * Cs; i += blockDim.x) wc[i] = 0;
   __syncthreads();
-  for (int i = tid; i < S; i += blockDim.x) {
-    const int c = a[i];
-    if (c >= 0) {
-      const int cl = c - s * Cs;
-      if (cl < 0 || cl >= Cs) atomicOr(err, WI_DEVERR_BAD_CLUSTER);
-      else atomicAdd(&cnt[cl], 1);
+  int* my = wc + warp * Cs;
+  const unsigned below = (1u << lane) - 1u;
+  // local cluster of position i, -1 for steady / outside the chunk
+  auto local = [&](int i) -> int {
+    if (i >= p1) return -1;
+    const int c = __ldg(a + i);
+    if (c < 0) return -1;
+    const int cl = c - s * Cs;
+    if (cl < 0 || cl >= Cs) {
+      atomicOr(err, WI_DEVERR_BAD_CLUSTER);
+      return -1;
     }
+    return cl;
+  };
+  for (int i0 = p0; i0 < p1; i0 += 32) {
+    const int cl = local(i0 + lane);
+    const unsigned peers = __match_any_sync(0xffffffffu, cl);
+    if (cl >= 0 && (peers & below) == 0u) my[cl] += __popc(peers);
   }
   __syncthreads();
+  // counts per cluster, offsets, and every warp's first slot per cluster
   int running = 0;
   for (int base = 0; base < Cs; base += blockDim.x) {
     const int j = base + tid;
-    const int v = j < Cs ? cnt[j] : 0;
+    int v = 0;
+    if (j < Cs)
+      for (int w = 0; w < kSortWarps; ++w) v += wc[w * Cs + j];
     int tot;
     const int ex = block_exclusive_scan(v, tmp, &tot);
-    if (j < Cs) off[j] = running + ex;
+    if (j < Cs) {
+      cnt[j] = v;
+      off[j] = running + ex;
+      int r = running + ex;
+      for (int w = 0; w < kSortWarps; ++w) {
+        const int c = wc[w * Cs + j];
+        wc[w * Cs + j] = r;
+        r += c;
+      }
+    }
     running += tot;
   }
   if (tid == 0) off[Cs] = running;
   __syncthreads();
-  for (int i = tid; i < S; i += blockDim.x) {
-    const int c = a[i];
-    if (c >= 0) {
-      const int cl = c - s * Cs;
-      if (cl >= 0 && cl < Cs) sa[off[cl] + atomicAdd(&cur[cl], 1)] = i;
-    }
-  }
-  __syncthreads();
-  // order each cluster's slots by position: rank of every member among its cluster
-  for (int cl = warp; cl < Cs; cl += nw) {
-    const int b = off[cl], m = cnt[cl];
-    for (int e = lane; e < m; e += 32) {
-      const int v = sa[b + e];
-      int r = 0;
-      for (int x = 0; x < m; ++x) r += sa[b + x] < v;
-      sb[b + r] = v;
-    }
+  for (int i0 = p0; i0 < p1; i0 += 32) {
+    const int cl = local(i0 + lane);
+    const unsigned peers = __match_any_sync(0xffffffffu, cl);
+    const int first = cl >= 0 ? my[cl] : 0;
+    if (cl >= 0) sb[first + __popc(peers & below)] = i0 + lane;
+    __syncwarp();
+    if (cl >= 0 && (peers & below) == 0u) my[cl] = first + __popc(peers);
+    __syncwarp();
   }
   __syncthreads();
   const int total = off[Cs];
@@ -366,12 +390,12 @@ cudaError_t wi_launch_assign(const WiGeom& g, const void* K, const void* chat, i
 
 cudaError_t wi_launch_segment_sort(const WiGeom& g, const int32_t* assign, int* seg_counts, int* seg_offsets,
                                    int* slots, int* err, cudaStream_t st) {
-  const size_t smem = sizeof(int) * ((size_t)3 * g.Cs + 1 + 32 + 2 * (size_t)g.S);
+  const size_t smem = sizeof(int) * ((size_t)(kSortWarps + 2) * g.Cs + 1 + 32 + (size_t)g.S);
   static int smem_set[kWiSmemDevices] = {};
   cudaError_t e = wi_ensure_smem(k_segment_sort, smem, smem_set);
   if (e != cudaSuccess) return e;
-  k_segment_sort<<<g.U * g.nseg, 512, smem, st>>>(assign, seg_counts, seg_offsets, slots, g.S, g.Cs, g.nseg, g.n,
-                                                   err);
+  k_segment_sort<<<g.U * g.nseg, 32 * kSortWarps, smem, st>>>(assign, seg_counts, seg_offsets, slots, g.S, g.Cs,
+                                                              g.nseg, g.n, err);
   return cudaGetLastError();
 }
 
