@@ -15,9 +15,10 @@
 //                (M = 128, N = min(Cs, 256), K = 16 per instruction) into one
 //                of two accumulator halves, so that the argmax of one half
 //                overlaps the products of the other;
-//   warps 2..9   epilogue: tcgen05.ld of the accumulator rows (warp w reads
+//   warps 2..17  epilogue: tcgen05.ld of the accumulator rows (warp w reads
 //                TMEM lanes 32*(w%4)..+31), running argmax over its column
-//                share, pairwise combine through shared memory, store.
+//                share (four column groups), combine through shared memory,
+//                store.
 // Every mbarrier wait is bounded (wi_pipe.cuh); on a timeout the kernel
 // records WI_DEVERR_MBAR_TIMEOUT, waits for its own copies and returns.
 #include <cuda.h>
@@ -36,7 +37,8 @@ namespace {
 
 constexpr int kTM = 128;                 // tokens per tile (MMA M)
 constexpr int kStagesA = 3;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;                  // four column groups of four warps (one per TMEM lane quarter)
+constexpr int kGroups = kEpiWarps / 4;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kATileBytes = kTM * WI_D * 2;  // 32 KB: two 16 KB halves of 64 columns
 constexpr int kMaxCs = 512;
@@ -44,14 +46,14 @@ constexpr int kBBytes = kMaxCs * WI_D * 2;   // 128 KB
 
 struct TcSmem {
   // small state first (3 KB), then the 1024-byte aligned tiles for the 128-byte swizzle
-  float best_v[2][kTM];                     // epilogue combine: column group x row
-  int best_j[2][kTM];
+  float best_v[kGroups - 1][kTM];           // epilogue combine: column groups 1.. x row
+  uint16_t best_j[kGroups - 1][kTM];
   uint64_t full_a[kStagesA], empty_a[kStagesA];
   uint64_t full_b, b_free;
   uint64_t tmem_full[2], tmem_empty[2];
   uint32_t tmem_base;
   int abort_flag;
-  unsigned char pad[3072 - 2 * kTM * 8 - (2 * kStagesA + 6) * 8 - 8];
+  unsigned char pad[3072 - (kGroups - 1) * kTM * 6 - (2 * kStagesA + 6) * 8 - 8];
   unsigned char b[kBBytes];                 // [k half][Cs rows][128 B]
   unsigned char a[kStagesA][kATileBytes];   // [k half][128 rows][128 B]
 };
@@ -185,12 +187,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_assign_tc(const __grid_constant
       if (!ok) sm.abort_flag = 1;
     }
   } else {
-    // ---------------- epilogue: warps 2..9
-    const int ew = warp - 2;            // 0..7
+    // ---------------- epilogue: warps 2..2+kEpiWarps-1
+    const int ew = warp - 2;
     const int quarter = warp & 3;       // TMEM lane quarter this warp may access
-    const int cgroup = ew >> 2;         // column group: 0 -> first half of each N block, 1 -> second
+    const int cgroup = ew >> 2;         // column group g takes columns [g*cols, (g+1)*cols) of each N block
     const int row = quarter * 32 + lane;
-    const int cols = P.N / 2;           // columns per group per half (multiple of 32)
+    const int groups = min(kGroups, P.N / 32);     // groups with columns (N = 64: two)
+    const int cols = P.N / groups;                 // columns per group per half (multiple of 32)
+    const int my_cols = cgroup < groups ? cols : 0;  // a group without columns still meets every barrier
     bool ok = true;                     // after one timed-out wait the warp stops waiting but keeps
                                         // meeting the epilogue barriers, so no warp is left behind
     // the row's running argmax as kChains independent chains over interleaved columns (column i goes
@@ -207,25 +211,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_assign_tc(const __grid_constant
       for (int h = 0; h < P.halves && ok; ++h) {
         if (!mbar_wait(&sm.tmem_full[h], it & 1, P.err)) { ok = false; sm.abort_flag = 1; break; }
         tc_fence_after();
-        for (int c0 = 0; c0 < cols; c0 += 64) {
-          // two 32-column loads in flight, then one wait
+        for (int c0 = 0; c0 < my_cols; c0 += 32) {  // 32 columns per load (the other warps hide its wait)
           const int col = h * P.N + cgroup * cols + c0;
           const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)col;
-          uint32_t r0[32], r1[32];
+          uint32_t r0[32];
           tmem_ld32_nowait(ta, r0);
-          if (c0 + 32 < cols) tmem_ld32_nowait(ta + 32, r1);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float v = __uint_as_float(r0[i]);
             if (v > cv[i % kChains]) { cv[i % kChains] = v; cj[i % kChains] = col + i; }
-          }
-          if (c0 + 32 < cols) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float v = __uint_as_float(r1[i]);
-              if (v > cv[i % kChains]) { cv[i % kChains] = v; cj[i % kChains] = col + 32 + i; }
-            }
           }
         }
         tc_fence_before();
@@ -237,13 +232,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_assign_tc(const __grid_constant
 #pragma unroll
       for (int c = 1; c < kChains; ++c)
         if (cv[c] > bv || (cv[c] == bv && cj[c] < bj)) { bv = cv[c]; bj = cj[c]; }
-      sm.best_v[cgroup][row] = bv;
-      sm.best_j[cgroup][row] = bj;
+      if (cgroup > 0) {
+        sm.best_v[cgroup - 1][row] = bv;
+        sm.best_j[cgroup - 1][row] = (uint16_t)min(bj, 0xFFFF);
+      }
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
       if (cgroup == 0) {
-        const float ov = sm.best_v[1][row];
-        const int oj = sm.best_j[1][row];
-        if (ov > bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
+        for (int g2 = 1; g2 < groups; ++g2) {
+          const float ov = sm.best_v[g2 - 1][row];
+          const int oj = sm.best_j[g2 - 1][row];
+          if (ov > bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
+        }
         const int u = su / P.nseg, sg = su % P.nseg;
         const long long p = (long long)sg * P.S + (long long)mt * kTM + row;
         int a = -1;

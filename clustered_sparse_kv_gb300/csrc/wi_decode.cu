@@ -549,6 +549,7 @@ struct alignas(16) SelSmem {
   int hist[2][kTopkBins];
   int s_wsum[32];
   int s_bin, s_above, s_ncand, s_pad;
+  uint64_t s_bar, s_pad2;  // completion of the keys' bulk copy (cached keys)
   int s_spos[68];  // first position of each split
   int s_wt[32];
   float s_wf[32];
@@ -738,7 +739,18 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
       f[r] = i < n4 ? __ldcg(reinterpret_cast<const uint4*>(s) + i) : make_uint4(0u, 0u, 0u, 0u);
     }
   };
-  load4(tid);
+  // cached keys: one bulk copy of the head's C keys into shared memory (the copy engine fetches them
+  // as one request instead of every thread's vector loads); above kSelKeysMax, vector loads
+  if (cached) {
+    if (tid == 0) {
+      mbar_init(&sm.s_bar, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      mbar_arrive_expect_tx(&sm.s_bar, (uint32_t)C * 4u);
+      bulk_g2s(ks, s, (uint32_t)C * 4u, &sm.s_bar);
+    }
+  } else {
+    load4(tid);
+  }
   // K0 = the largest key of a non-empty cluster, from k_scores' per-CTA maxima of the same
   // scores (every warp reduces them itself: no barrier)
   uint32_t K0 = 0u;
@@ -757,24 +769,21 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
     if (k != 0u && (K0 - k >= (1u << 30)) == far) atomicAdd(&sm.hist[0][log_bin(K0 - k)], 1);
   };
   if (cached) {
-    __syncthreads();  // the histogram and the masks are zero
-    for (int i0 = tid; i0 < n4; i0 += 4 * kSThreads) {
-      if (i0 != tid) load4(i0);
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int i = i0 + r * kSThreads;
-        const uint4 k4 = f[r];
-        if (i < n4) {
-          reinterpret_cast<uint4*>(ks)[i] = k4;
-          if (kk > 0) {
-            count_key(k4.x, false);
-            count_key(k4.y, false);
-            count_key(k4.z, false);
-            count_key(k4.w, false);
-          }
-        }
-      }
+    __syncthreads();  // the histogram and the masks are zero; the barrier's init is visible
+    // a timed-out wait is recorded; the CTA then selects nothing (uniformly), after waiting once more
+    // (bounded) for its copy so that none lands after the CTA left
+    if (__syncthreads_or(mbar_wait(&sm.s_bar, 0, a.err) ? 0 : 1)) {
+      if (tid == 0) mbar_wait(&sm.s_bar, 0, a.err);
+      kk = 0;
     }
+    if (kk > 0)
+      for (int i = tid; i < n4; i += kSThreads) {
+        const uint4 k4 = reinterpret_cast<const uint4*>(ks)[i];
+        count_key(k4.x, false);
+        count_key(k4.y, false);
+        count_key(k4.z, false);
+        count_key(k4.w, false);
+      }
   } else {
     __syncthreads();  // the histogram and the masks are zero
     auto bin_of = [&](uint32_t k) -> uint32_t { return k == 0u ? 0xFFFFu : (uint32_t)log_bin(K0 - k); };
