@@ -289,7 +289,7 @@ def profile_run(wi, torch, w, dev, steps, dense=False, device_gen=False):
     torch.cuda.synchronize()
     ix.check()
     ix.free()
-    print(json.dumps({"profile_steps": steps, "workload": w.name}), flush=True)
+    print(json.dumps({"profile_steps": steps, "workload": w.name, "units": w.units}), flush=True)
 
 
 class Timer:
@@ -574,6 +574,9 @@ def main():
                     help="with --profile-steps: also run the dense comparator after every decode step")
     ap.add_argument("--profile-device-gen", action="store_true",
                     help="with --profile-steps: generate the workload on the device")
+    ap.add_argument("--profile-units", default="",
+                    help="with --profile-steps: batch,layers,kv_heads of a smaller case of the workload "
+                         "(query heads per kv head kept), for captures whose traffic scales by units")
     ap.add_argument("--valsum-bf16", action="store_true",
                     help="the index variant whose decode reads a bf16 copy of the value sums")
     ap.add_argument("--group-topk", action="store_true",
@@ -612,6 +615,9 @@ def main():
 
     seed = rank_seed(w, rank)
     if args.profile_steps > 0:
+        if args.profile_units:
+            b, l, h = (int(x) for x in args.profile_units.split(","))
+            w = w.with_(batch=b, layers=l, n_kv_heads=h, n_q_heads=h * w.group)
         profile_run(wi, torch, w, dev, args.profile_steps, dense=args.profile_dense,
                     device_gen=args.profile_device_gen)
         return
