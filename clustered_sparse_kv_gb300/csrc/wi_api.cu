@@ -280,6 +280,9 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   if (ns > 64) ns = 64;
   if (ns < 1) ns = 1;
   b.nsplit = ns;
+  // exact stages: 32 rows when every exact CTA is resident at once (two per SM), else 64 rows
+  const int d3r = env_int("WI_D3_STAGE_ROWS", 0);
+  b.d3_rows = d3r == 32 || d3r == 64 ? d3r : (heads * (size_t)(ns + 1) <= slots ? 32 : 64);
   // dense comparator: row ranges per unit such that the U * ranges CTAs come closest to whole waves
   // (a partial last wave idles SMs), at least 1024 rows each; the fewest ranges among equals
   int ds = 1;

@@ -1115,22 +1115,33 @@ __global__ void __launch_bounds__(kSThreads, 1) k_select_estimate(TopkArgs a) {
 // local window, appended tokens) followed by its selected clusters' rows in
 // position order -- are cut into NS+1 row-balanced splits by the top-k; split
 // 0 starts with the steady rows (sinks and window copied before the
-// dependency wait).  A producer lane packs the row runs into 64-row stages
+// dependency wait).  A producer lane packs the row runs into ROWS-row stages
 // (K and V rows bulk-copied into shared memory; a stage with no rows ends the
-// stream); 8 consumer warps take 8 rows each per stage, flash-decode style.
-// The last CTA of the head (ticket counter) merges all partials into the
-// output row.
-constexpr int kD3Rows = 64;
-constexpr int kD3Stages = 3;
+// stream for the warps that take it); the 8 consumer warps form 8 / (ROWS /
+// 8) groups, group g taking stages g, g + groups, ..., each warp 8 rows of a
+// stage, flash-decode style.  The last CTA of the head (ticket counter) merges
+// all partials into the output row.  96 KB of stages either way: 64-row
+// stages take fewer bulk copies (a run is cut at every stage boundary), which
+// rules when the CTAs come in several waves; 32-row stages hand the first
+// rows to the consumers sooner, which rules a launch of one wave.
 constexpr int kD3Warps = 8;
 constexpr int kD3Threads = 32 * (kD3Warps + 1);
+constexpr int kD3StageBytes = 96 * 1024;
 
-struct D3Stage {
-  bf16 k[kD3Rows * WI_D];
-  bf16 v[kD3Rows * WI_D];
+template <int ROWS>
+struct D3Geo {
+  static constexpr int Rows = ROWS;
+  static constexpr int Stages = kD3StageBytes / (ROWS * WI_D * 4);
+  static constexpr int WPS = ROWS / 8;              // consumer warps per stage
+  static constexpr int Groups = kD3Warps / WPS;     // stages consumed at once
+  static_assert(ROWS % 8 == 0 && kD3Warps % WPS == 0 && Groups <= Stages, "stage geometry");
+  struct Stage {
+    bf16 k[ROWS * WI_D];
+    bf16 v[ROWS * WI_D];
+  };
+  static constexpr size_t SMEM = sizeof(Stage) * Stages + 2 * Stages * sizeof(uint64_t) + 4 * Stages * sizeof(int) +
+                                 sizeof(float) * kD3Warps * (WI_PART + WI_D) + 32;
 };
-constexpr size_t kD3Smem = sizeof(D3Stage) * kD3Stages + 2 * kD3Stages * sizeof(uint64_t) +
-                           4 * kD3Stages * sizeof(int) + sizeof(float) * kD3Warps * (WI_PART + WI_D) + 32;
 
 struct ExactArgs {
   const bf16* q;
@@ -1170,8 +1181,11 @@ struct ExactArgs {
 // falls in the stage (the copy engine takes ~60-100 cycles per copy, so the
 // copies of a stage are issued by several lanes at once); a stage is closed
 // once its 64 rows are placed.
+template <int ROWS>
 struct StagePacker {
-  D3Stage* st;
+  using Geo = D3Geo<ROWS>;
+  static constexpr int kD3Rows = Geo::Rows, kD3Stages = Geo::Stages, kD3Groups = Geo::Groups;
+  typename Geo::Stage* st;
   uint64_t* full;
   uint64_t* empty;
   int* nrows;
@@ -1214,19 +1228,22 @@ struct StagePacker {
     }
     if (ok) fpos = B;
   }
-  // Close the partial last stage and send the end marker (a stage with no rows); on failure,
-  // close what is open and wait for the copies in flight, so that none lands after the CTA left.
+  // Close the partial last stage and send the end markers (kD3Groups consecutive stages with no
+  // rows: one for every consumer group); on failure, close what is open and wait for the copies in
+  // flight, so that none lands after the CTA left.
   __device__ void finish(int* abort_flag) {
     const int lane = threadIdx.x & 31;
     if (lane != 0) return;
     int t = fpos / kD3Rows;
-    if (ok && fpos % kD3Rows != 0) {  // opened stage with rows: close it
+    bool closed = fpos % kD3Rows == 0;  // no stage is half filled
+    if (ok && !closed) {  // opened stage with rows: close it
       const int s = t % kD3Stages;
       nrows[s] = fpos % kD3Rows;
       mbar_arrive(&full[s]);
+      closed = true;
       ++t;
     }
-    if (ok) {  // the end marker
+    for (int e = 0; ok && e < kD3Groups; ++e, ++t) {  // the end markers
       const int s = t % kD3Stages, r = t / kD3Stages;
       if (t > opened && r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, err)) ok = false;
       if (ok) {
@@ -1236,7 +1253,7 @@ struct StagePacker {
     }
     if (!ok) {
       *abort_flag = 1;
-      if (fpos % kD3Rows != 0) {  // the stage being filled has rows in flight: let it complete
+      if (!closed) {  // the stage being filled has rows in flight: let it complete
         const int s = (fpos / kD3Rows) % kD3Stages;
         nrows[s] = fpos % kD3Rows;
         mbar_arrive(&full[s]);
@@ -1247,11 +1264,13 @@ struct StagePacker {
   }
 };
 
-template <typename VT>
+template <typename VT, int ROWS>
 __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
+  using Geo = D3Geo<ROWS>;
+  constexpr int kD3Stages = Geo::Stages, kD3WPS = Geo::WPS, kD3Groups = Geo::Groups;
   extern __shared__ __align__(128) unsigned char d3_raw[];
-  D3Stage* st = reinterpret_cast<D3Stage*>(d3_raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(d3_raw + sizeof(D3Stage) * kD3Stages);
+  typename Geo::Stage* st = reinterpret_cast<typename Geo::Stage*>(d3_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(d3_raw + sizeof(typename Geo::Stage) * kD3Stages);
   uint64_t* empty = full + kD3Stages;
   int* nrows = reinterpret_cast<int*>(empty + kD3Stages);        // [4 * stages]
   float* red = reinterpret_cast<float*>(nrows + 4 * kD3Stages);  // [warps][WI_PART]
@@ -1265,7 +1284,7 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
   if (tid == 0) {
     for (int s = 0; s < kD3Stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kD3Warps);
+      mbar_init(&empty[s], kD3WPS);
     }
     flags[0] = 0;
     flags[1] = 0;
@@ -1275,7 +1294,7 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
   if (warp == kD3Warps) {
     const bf16* Ku = a.K + (size_t)u * a.n * WI_D;
     const bf16* Vu = a.V + (size_t)u * a.n * WI_D;
-    StagePacker pk{st, full, empty, nrows, a.err};
+    StagePacker<ROWS> pk{st, full, empty, nrows, a.err};
     const int amax = a.max_append > 0 ? a.max_append : 1;
     if (split == 0) {
       // ---- steady rows first: the sinks and (in an index that cannot grow) the build's local window
@@ -1420,14 +1439,14 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
       }
     }
     const int ri = lane >> 2;  // the row (of the warp's 8) whose logit this lane ends with
-    for (int it = 0;; ++it) {
+    const int i0 = (warp % kD3WPS) * 8;  // the warp's rows of each stage its group takes
+    for (int it = warp / kD3WPS;; it += kD3Groups) {
       const int s = it % kD3Stages, r = it / kD3Stages;
       if (!mbar_wait(&full[s], r & 1, a.err)) { flags[0] = 1; break; }
       const int nr = nrows[s];
       if (nr == 0) break;
-      const int i0 = warp * 8;
       if (i0 < nr) {
-        const D3Stage& T = st[s];
+        const typename Geo::Stage& T = st[s];
         float v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -1681,12 +1700,18 @@ cudaError_t launch_scores(const WiGeom& g, const WiDecodeBufs& b, const bf16* q,
                     reinterpret_cast<uint32_t*>(b.scores), b.kmaxp, g.C, b.p1, b.err);
 }
 
+template <typename VT, int ROWS>
+cudaError_t launch_exact_rows(const WiGeom& g, const WiDecodeBufs& b, const ExactArgs& a, cudaStream_t st) {
+  static int smem_set[kWiSmemDevices] = {};
+  constexpr size_t smem = D3Geo<ROWS>::SMEM;
+  cudaError_t e = wi_ensure_smem(k_exact_merge<VT, ROWS>, smem, smem_set);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_exact_merge<VT, ROWS>, dim3(b.nsplit + 1, g.G, g.U), dim3(kD3Threads), smem, st, a);
+}
+
 template <typename VT>
 cudaError_t launch_exact(const WiGeom& g, const WiDecodeBufs& b, const ExactArgs& a, cudaStream_t st) {
-  static int smem_set[kWiSmemDevices] = {};
-  cudaError_t e = wi_ensure_smem(k_exact_merge<VT>, kD3Smem, smem_set);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(k_exact_merge<VT>, dim3(b.nsplit + 1, g.G, g.U), dim3(kD3Threads), kD3Smem, st, a);
+  return b.d3_rows == 32 ? launch_exact_rows<VT, 32>(g, b, a, st) : launch_exact_rows<VT, 64>(g, b, a, st);
 }
 
 template <int G>

@@ -100,6 +100,7 @@ struct WiDecodeBufs {
   int p_es;               // estimation CTAs per unit (= estimation partials per head)
   int est_first;          // the select/estimate launch starts its estimation CTAs first
   int nsplit;             // exact_merge CTAs per head over the selected rows (plus one for steady rows)
+  int d3_rows;            // exact_merge stage height: 32 (one wave of CTAs) or 64 rows
   // dense comparator (full attention)
   float* dpart;           // [U][G][dsplits][WI_PART]  row-range partials
   unsigned int* dticket;  // [U]

@@ -219,7 +219,9 @@ int wi_index_shape(const wi_index* ix, int* units, int* clusters, int* k_max, in
  * takes the steady rows).  The environment variables WI_D1_CTAS_PER_UNIT,
  * WI_ESTIMATE_CTAS_PER_UNIT and WI_D3_SPLITS (positive integers), and
  * WI_ESTIMATE_FIRST (0 or 1: the estimation CTAs before the top-k CTAs in
- * their shared launch; default: when they fit in one wave), read when the
+ * their shared launch; default: when they fit in one wave), WI_D3_STAGE_ROWS
+ * (32 or 64: rows per shared-memory stage of the exact-attention CTAs;
+ * default 32 when all of them are resident at once, else 64), read when the
  * index is made, override the defaults.  Results do not depend on the
  * layout beyond float rounding order.  Any output pointer may be NULL.
  */

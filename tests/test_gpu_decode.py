@@ -291,16 +291,19 @@ def test_single_kernel_launches_repeat_the_step(wi):
     ix.free()
 
 
+@pytest.mark.parametrize("rows", [32, 64])
 @pytest.mark.parametrize("splits", [1, 5, 12])
-def test_exact_split_counts(wi, monkeypatch, splits):
+def test_exact_split_counts(wi, monkeypatch, splits, rows):
     """The exact-attention rows cut into 1, 5 or 12 row-balanced splits per head (plus the steady
-    CTA) give the oracle's output; the layout query reports the count in use."""
+    CTA), streamed through 32- or 64-row stages, give the oracle's output; the layout query reports
+    the split count in use."""
     w = small(batch=2, n_q_heads=8, n_kv_heads=2, n_ctx=4096, seg_len=1024, clusters_per_seg=64, iters=2,
               budget_k=12, seed=5)
     k, v, q, K, V, Q = gen(w)
     p = params_of(w)
     idx = oracle.build_index(K, V, p)
     monkeypatch.setenv("WI_D3_SPLITS", str(splits))
+    monkeypatch.setenv("WI_D3_STAGE_ROWS", str(rows))
     ix = wi.WaveIndex.adopt(wi.config_from_workload(w), dev16(k), dev16(v), *index_arrays(idx))
     assert wi.wi_decode_layout(ix.handle)["exact_splits"] == splits
     for t in range(2):
