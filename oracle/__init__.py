@@ -29,6 +29,11 @@ Parity status per function (what pins it is in ``tests/test_oracle_pins.py``):
                               retrieved; one row gives its value row;
                               identical keys give the mean value row;
                               row-order invariance)
+  LruPagePolicy       pinned in tests/test_oracle_wave_buffer.py (hand-worked
+                              LRU trace; a second, stamp-and-argmin statement
+                              of the rounds over random traces; cache as
+                              large as the working set never evicts, no
+                              slots never admits)
 Approximation quality against full attention on synthetic data: parity
 unpinned (the summaries claim accuracy only on RULER / Needle-in-a-Haystack
 with trained models).
@@ -55,3 +60,4 @@ from .wave_index import (  # noqa: F401
     decode,
     full_attention,
 )
+from .wave_buffer import LruPagePolicy, pages_of_rows  # noqa: F401
