@@ -540,6 +540,82 @@ def variant_accuracy(wi, torch, w, k_dev, v_dev, qs, dev, stream):
     return res
 
 
+def h2d_copy_gbs(torch, dev, stream, gib=1.0):
+    """Host-to-device copy rate from page-locked memory (the copy engines over the CPU-GPU link),
+    the reference rate for rows read from host memory."""
+    n = int(gib * (1 << 30))
+    h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d = torch.empty(n, dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        d.copy_(h, non_blocking=True)
+        e0.record(stream)
+        for _ in range(3):
+            d.copy_(h, non_blocking=True)
+        e1.record(stream)
+    e1.synchronize()
+    rate = 3 * n / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del h, d
+    return rate
+
+
+def tier_record(wi, torch, w, k_dev, v_dev, dev, stream, steps=256, warmup=16):
+    """The host memory tier (wave buffer) on the main workload: K/V rows in page-locked host memory,
+    a device page cache with LRU rounds on the library's thread.  Each case builds a fresh index,
+    attaches the tier and launches steps one by one (no graphs: the rounds enqueue work between
+    steps); the untiered index is timed the same way.  Two query streams: a fresh query every step
+    (the bench's stream) and each query held for 8 steps (temporal locality, which the pages credit
+    real decoding with)."""
+    cfg = wi.config_from_workload(w)
+    pages = w.n_ctx // 16
+    qs = [torch.from_numpy(kvsynth.queries(w, step=s, seed=w.seed + 77).view(np.int16)).to(dev)
+          for s in range(steps + warmup)]
+    out = torch.empty((w.batch, w.layers, w.n_q_heads, 128), dtype=torch.float32, device=dev)
+
+    def run(ix, hold):
+        with torch.cuda.stream(stream):
+            for s in range(warmup):
+                ix.decode(qs[s // hold], out=out, stream=stream)
+            stream.synchronize()
+            before = ix.tier_stats() if ix is not None and getattr(ix, "_tier", False) else None
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for s in range(warmup, warmup + steps):
+                ix.decode(qs[s // hold], out=out, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+        return e0.elapsed_time(e1) / steps, before
+
+    cases = []
+    for frac, hold in [(None, 1), (0.0, 1), (0.25, 1), (0.25, 8), (1.0, 8)]:
+        ix = wi.WaveIndex.build(cfg, k_dev.clone(), v_dev.clone(), stream=stream)
+        stream.synchronize()
+        slots = 0 if frac is None else int(frac * pages)
+        if frac is not None:
+            ix.attach_tier(slots, 512, async_rounds=True, stream=stream)
+            ix._tier = True
+        ms, before = run(ix, hold)
+        rec = {"slots_fraction": frac, "query_held_steps": hold, "ms_per_step": ms, "steps_per_s": 1e3 / ms}
+        if frac is not None:
+            st = ix.tier_stats()
+            rc = st["rows_from_cache"] - before["rows_from_cache"]
+            rh = st["rows_from_host"] - before["rows_from_host"]
+            rec.update(slots_per_unit=slots, pages_per_unit=pages,
+                       row_hit_ratio=rc / max(rc + rh, 1),
+                       host_bytes_per_step=rh * 512 / steps,
+                       host_read_gbs=rh * 512 / steps / (ms * 1e-3) / 1e9,
+                       rounds=st["rounds"] - before["rounds"],
+                       admitted=st["admitted"] - before["admitted"], evicted=st["evicted"] - before["evicted"])
+        ix.check()
+        ix.free()
+        cases.append(rec)
+    return {"workload": w.name, "page_rows": 16, "admit_per_round": 512,
+            "device_kv_bytes_untiered": w.units * w.n_ctx * 512,
+            "h2d_copy_gbs": h2d_copy_gbs(torch, dev, stream),
+            "timing": f"{steps} steps launched one by one after {warmup}, CUDA events on the launching stream",
+            "cases": cases}
+
+
 def spawn_ranks(n):
     """--gpus N without a launcher: run this script under torch.distributed.run with N ranks."""
     import socket
@@ -567,6 +643,7 @@ def main():
                     help="comma-separated further workloads measured at full size (empty: none)")
     ap.add_argument("--config-steps", type=int, default=256, help="decode steps timed per further workload")
     ap.add_argument("--no-accuracy", action="store_true", help="skip the variant accuracy record")
+    ap.add_argument("--no-tier", action="store_true", help="skip the host memory tier record")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="profiling run: build one index of the workload, run this many decode steps, "
                          "print nothing else (a small case for ncu captures)")
@@ -700,6 +777,10 @@ def main():
     if rank == 0 and world == 1 and not args.no_accuracy:
         accuracy = variant_accuracy(wi, torch, w, k_dev, v_dev, qs[:4], dev, stream)
 
+    tier = None
+    if rank == 0 and world == 1 and not args.no_tier:
+        tier = tier_record(wi, torch, w, k_dev, v_dev, dev, stream)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, k, v)
@@ -757,6 +838,8 @@ def main():
             line["dense_comparator"] = dense
         if accuracy is not None:
             line["variant_accuracy"] = accuracy
+        if tier is not None:
+            line["wave_buffer"] = tier
         if configs:
             line["configs"] = configs
         print(json.dumps(line), flush=True)

@@ -68,6 +68,11 @@ _SIGS = {
     "wi_profile_begin": [_vp, ctypes.c_int],
     "wi_index_build_stats": [_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), _ip],
     "wi_profile_read": [_vp, ctypes.POINTER(ctypes.c_double), _ip, ctypes.POINTER(ctypes.c_ulonglong)],
+    "wi_tier_attach": [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp],
+    "wi_tier_round": [_vp, _vp],
+    "wi_tier_stats": [_vp, ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_ulonglong), _ip, _ip],
+    "wi_tier_tables": [_vp, _vp, _vp],
+    "wi_lru_round": [_vp, _vp, ctypes.c_int, ctypes.c_longlong, _vp, _vp, _ip, _vp, _vp, _ip],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(lib, _name)
@@ -77,8 +82,12 @@ lib.wi_free.argtypes = [_vp]
 lib.wi_free.restype = None
 lib.wi_last_error.argtypes = []
 lib.wi_last_error.restype = ctypes.c_char_p
+lib.wi_lru_new.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+lib.wi_lru_new.restype = _vp
+lib.wi_lru_free.argtypes = [_vp]
+lib.wi_lru_free.restype = None
 
-EXPORTED = sorted([*_SIGS, "wi_free", "wi_last_error"])
+EXPORTED = sorted([*_SIGS, "wi_free", "wi_last_error", "wi_lru_new", "wi_lru_free"])
 
 
 def _check(rc: int):
@@ -229,6 +238,56 @@ def wi_free(ix: int):
     lib.wi_free(ix)
 
 
+TIER_COUNTERS = ["rounds", "pages_read", "page_hits", "page_misses", "admitted", "evicted"]
+
+
+def wi_tier_attach(ix: int, slots_per_unit: int, admit_per_round: int, async_rounds: bool = True, stream=None):
+    _check(lib.wi_tier_attach(ix, slots_per_unit, admit_per_round, 1 if async_rounds else 0, _stream(stream)))
+
+
+def wi_tier_round(ix: int, stream=None):
+    _check(lib.wi_tier_round(ix, _stream(stream)))
+
+
+def wi_tier_stats(ix: int) -> dict:
+    c = (ctypes.c_longlong * 6)()
+    r = (ctypes.c_ulonglong * 2)()
+    slots, pages = ctypes.c_int(), ctypes.c_int()
+    _check(lib.wi_tier_stats(ix, c, r, ctypes.byref(slots), ctypes.byref(pages)))
+    d = dict(zip(TIER_COUNTERS, list(c)))
+    d.update(rows_from_cache=r[0], rows_from_host=r[1], slots=slots.value, pages=pages.value)
+    return d
+
+
+def wi_tier_tables(ix: int, slot_of=None, use=None):
+    _check(lib.wi_tier_tables(ix, _ptr(slot_of), _ptr(use)))
+
+
+class LruPolicy:
+    """The tier's page replacement policy alone, run on the host (wi_lru_*)."""
+
+    def __init__(self, pages: int, slots: int, admit_max: int):
+        self.h = lib.wi_lru_new(pages, slots, admit_max)
+        if not self.h:
+            raise ValueError("bad policy sizes")
+
+    def round(self, touched, t: int):
+        import numpy as np
+        tp = np.ascontiguousarray(np.asarray(list(touched), dtype=np.int32))
+        n = max(int(tp.size), 1)
+        ep, es, ap, as_ = (np.empty(n, np.int32) for _ in range(4))
+        ne, na = ctypes.c_int(), ctypes.c_int()
+        _check(lib.wi_lru_round(self.h, tp.ctypes.data if tp.size else None, int(tp.size), t, ep.ctypes.data,
+                                es.ctypes.data, ctypes.byref(ne), ap.ctypes.data, as_.ctypes.data, ctypes.byref(na)))
+        return ([(int(ep[i]), int(es[i])) for i in range(ne.value)],
+                [(int(ap[i]), int(as_[i])) for i in range(na.value)])
+
+    def __del__(self):
+        if getattr(self, "h", None):
+            lib.wi_lru_free(self.h)
+            self.h = None
+
+
 # ------------------------------------------------------------ convenience ----
 
 class WaveIndex:
@@ -291,6 +350,24 @@ class WaveIndex:
 
     def check(self):
         wi_check_device(self.handle)
+
+    def attach_tier(self, slots_per_unit: int, admit_per_round: int, async_rounds: bool = True, stream=None):
+        """Move the K/V rows to host memory behind a device page cache (after this, no call reads
+        this index's k / v tensors)."""
+        wi_tier_attach(self.handle, slots_per_unit, admit_per_round, async_rounds, stream)
+
+    def tier_round(self, stream=None):
+        wi_tier_round(self.handle, stream)
+
+    def tier_stats(self) -> dict:
+        return wi_tier_stats(self.handle)
+
+    def tier_tables(self):
+        s = wi_tier_stats(self.handle)
+        slot_of = torch.empty((self.units, s["pages"]), dtype=torch.int32)
+        use = torch.empty((self.units, s["pages"]), dtype=torch.int32)
+        wi_tier_tables(self.handle, slot_of, use)
+        return slot_of, use
 
     def free(self):
         if self.handle:

@@ -94,6 +94,8 @@ struct wi_index {
   std::vector<cudaEvent_t> prof_ev;  // WI_DECODE_EVENTS per slot
   int prof_slots = 0;
   long long prof_steps = 0;
+  // host memory tier (wave buffer), once attached
+  WiTierHost* tier = nullptr;
 };
 
 int wi_budget(const WiGeom& g, int C) {
@@ -192,6 +194,7 @@ int alloc(wi_index* ix, void** p, size_t bytes) {
 
 void destroy(wi_index* ix) {
   if (!ix) return;
+  if (ix->tier) wi_tier_destroy(ix->tier);
   if (ix->host_exec) cudaGraphExecDestroy(ix->host_exec);
   if (ix->host_graph) cudaGraphDestroy(ix->host_graph);
   if (ix->cap_stream) cudaStreamDestroy(ix->cap_stream);
@@ -603,6 +606,13 @@ int wi_decode_step(wi_index* ix, const void* q, const void* k_new, const void* v
   if (k_new && ix->appended >= ix->g.max_append)
     return fail(WI_EFULL, "append buffer full (%d tokens)", ix->g.max_append);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (ix->tier) {  // the tier's replacement rounds enqueue work of their own between steps
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    WI_CUDA(cudaStreamIsCapturing(st, &cs));
+    if (cs != cudaStreamCaptureStatusNone)
+      return fail(WI_EUNSUPPORTED, "an index with a host memory tier cannot be captured in a graph");
+    ix->b.tier.step = (int)ix->steps_run;
+  }
   ix->last_stream = st;
   const cudaEvent_t* ev = nullptr;
   if (ix->prof_slots > 0) {
@@ -611,6 +621,11 @@ int wi_decode_step(wi_index* ix, const void* q, const void* k_new, const void* v
   }
   cudaError_t e = wi_launch_decode(ix->g, ix->b, q, out, st, ev);
   if (e != cudaSuccess) return fail(WI_ECUDA, "decode launch: %s", cudaGetErrorString(e));
+  if (ix->tier) {
+    char msg[320];
+    const int rc = wi_tier_after_step(ix->tier, ix->steps_run, st, msg, sizeof(msg));
+    if (rc != WI_OK) return fail(rc, "%s", msg);
+  }
   ix->steps_run++;
   if (k_new) {
     const WiGeom& g = ix->g;
@@ -647,6 +662,7 @@ int wi_decode_kernel(wi_index* ix, int kernel, const void* q, float* out, void* 
 int wi_dense_decode(wi_index* ix, const void* q, float* out, void* stream) {
   g_err[0] = 0;
   if (!ix || !q || !out) return fail(WI_EINVAL, "index, q and out must be non-NULL");
+  if (ix->tier) return fail(WI_EUNSUPPORTED, "full attention reads the caller's K and V, which a host memory tier releases");
   if (reinterpret_cast<uintptr_t>(q) & 15) return fail(WI_EINVAL, "q must be 16-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   ix->last_stream = st;
@@ -708,7 +724,7 @@ int wi_decode_step_host(wi_index* ix, const void* q_host, const void* k_new_host
   const size_t qb = (size_t)g.U * g.G * 128 * 2, kb = (size_t)g.U * 128 * 2, ob = (size_t)g.U * g.G * 128 * 4;
   void* qd = nullptr;
   void* od = nullptr;
-  if (!k_new_host && ix->prof_slots == 0 && !ix->host_graph_off && (qd = mapped_host(q_host)) &&
+  if (!k_new_host && ix->prof_slots == 0 && !ix->host_graph_off && !ix->tier && (qd = mapped_host(q_host)) &&
       (od = mapped_host(out_host)) && ((reinterpret_cast<uintptr_t>(qd) | reinterpret_cast<uintptr_t>(od)) & 15) == 0) {
     if (ix->host_exec && (ix->host_q != qd || ix->host_o != od)) {  // other buffers: capture again
       drop_host_graph(ix);
@@ -888,6 +904,61 @@ int wi_check_device(wi_index* ix) {
     WI_CUDA(cudaMemset(ix->err, 0, 4));
     return fail(WI_EDEVICE, "device invariant violated (flags 0x%x)", herr);
   }
+  return WI_OK;
+}
+
+int wi_tier_attach(wi_index* ix, int slots_per_unit, int admit_per_round, int async, void* stream) {
+  g_err[0] = 0;
+  if (!ix) return fail(WI_EINVAL, "index is NULL");
+  if (ix->tier) return fail(WI_EINVAL, "the index already has a host memory tier");
+  const WiGeom& g = ix->g;
+  if (g.Gmax > 0) return fail(WI_EUNSUPPORTED, "a host memory tier needs an index that does not grow (max_append < seg_len)");
+  if (g.vs16) return fail(WI_EUNSUPPORTED, "a host memory tier needs fp32 value sums");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char msg[320];
+  WiTierDev dev{};
+  const int rc = wi_tier_create(g, ix->K, ix->V, slots_per_unit, admit_per_round, async, ix->device, st, &ix->tier,
+                                &dev, msg, sizeof(msg));
+  if (rc != WI_OK) return fail(rc, "%s", msg);
+  ix->b.tier = dev;
+  ix->last_stream = st;
+  return WI_OK;
+}
+
+int wi_tier_round(wi_index* ix, void* stream) {
+  g_err[0] = 0;
+  if (!ix || !ix->tier) return fail(WI_EINVAL, "index has no host memory tier");
+  if (ix->steps_run == 0) return WI_OK;
+  char msg[320];
+  const int rc = wi_tier_round_now(ix->tier, ix->steps_run - 1, static_cast<cudaStream_t>(stream), msg, sizeof(msg));
+  if (rc != WI_OK) return fail(rc, "%s", msg);
+  return WI_OK;
+}
+
+int wi_tier_stats(wi_index* ix, long long* counters, unsigned long long* rows, int* slots, int* pages) {
+  g_err[0] = 0;
+  if (!ix || !ix->tier) return fail(WI_EINVAL, "index has no host memory tier");
+  wi_tier_idle(ix->tier);
+  WI_CUDA(cudaStreamSynchronize(ix->last_stream));
+  if (counters) wi_tier_counters(ix->tier, counters);
+  if (rows) WI_CUDA(cudaMemcpy(rows, wi_tier_row_counters(ix->tier), 16, cudaMemcpyDeviceToHost));
+  int s = 0, p = 0;
+  wi_tier_geometry(ix->tier, &s, &p);
+  if (slots) *slots = s;
+  if (pages) *pages = p;
+  return WI_OK;
+}
+
+int wi_tier_tables(wi_index* ix, int32_t* slot_of, int32_t* use) {
+  g_err[0] = 0;
+  if (!ix || !ix->tier) return fail(WI_EINVAL, "index has no host memory tier");
+  wi_tier_idle(ix->tier);
+  WI_CUDA(cudaStreamSynchronize(ix->last_stream));
+  int s = 0, p = 0;
+  wi_tier_geometry(ix->tier, &s, &p);
+  const size_t bytes = (size_t)ix->g.U * p * 4;
+  if (slot_of) WI_CUDA(cudaMemcpy(slot_of, wi_tier_slot_table(ix->tier), bytes, cudaMemcpyDeviceToHost));
+  if (use) WI_CUDA(cudaMemcpy(use, wi_tier_use_table(ix->tier), bytes, cudaMemcpyDeviceToHost));
   return WI_OK;
 }
 

@@ -1127,6 +1127,7 @@ __global__ void __launch_bounds__(kSThreads, 1) k_select_estimate(TopkArgs a) {
 constexpr int kD3Warps = 8;
 constexpr int kD3Threads = 32 * (kD3Warps + 1);
 constexpr int kD3StageBytes = 96 * 1024;
+constexpr int kTierPf = 8;  // host memory tier: page slots of a run looked up ahead (more: row by row)
 
 template <int ROWS>
 struct D3Geo {
@@ -1140,7 +1141,7 @@ struct D3Geo {
     bf16 v[ROWS * WI_D];
   };
   static constexpr size_t SMEM = sizeof(Stage) * Stages + 2 * Stages * sizeof(uint64_t) + 4 * Stages * sizeof(int) +
-                                 sizeof(float) * kD3Warps * (WI_PART + WI_D) + 32;
+                                 sizeof(float) * kD3Warps * (WI_PART + WI_D) + 32 + 32 * kTierPf * sizeof(int);
 };
 
 struct ExactArgs {
@@ -1171,6 +1172,25 @@ struct ExactArgs {
   long long n;
   int G, C, kmax, P, NS, n_sink, W, max_append;
   float lam;
+  WiTierDev tier;  // host memory tier: clustered rows from cached pages or host memory (TIER instances)
+};
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+// The clustered rows of one unit seen through the host memory tier: page p (rows 16p .. 16p+15 of the
+// unit's row space) is read from cache slot slot_of[p] when it holds one, else from host memory.
+struct TierRows {
+  const int* slot_of;
+  const bf16* poolK;
+  const bf16* poolV;
+  const bf16* hostK;
+  const bf16* hostV;
+  int* use;
+  int step;
+  int (*pslot)[kTierPf];  // shared memory: [lane][page of its run] slots
+  unsigned long long n_cache = 0, n_host = 0;  // rows copied (lane 0's count of the warp's rows)
 };
 
 // Producer of exact_merge: the whole producer warp.  The CTA's rows form one
@@ -1228,6 +1248,59 @@ struct StagePacker {
     }
     if (ok) fpos = B;
   }
+
+  // The same stream through the host memory tier: this lane's run is rows [row0, row0 + len) of the
+  // unit's row space.  Its pages' slots are looked up first (one round trip for the warp); then for
+  // every stage the warp copies the stage's rows one row per instruction (16 bytes per lane: lanes
+  // 0-15 the key row, 16-31 the value row) with cp.async from the cached page or from host memory,
+  // and every lane arms the stage's barrier with an arrive on completion of its copies.
+  __device__ void push_tier(TierRows& tr, int row0, int len) {
+    const int lane = threadIdx.x & 31;
+    const int pg0 = row0 >> 4;
+    const int npg = len > 0 ? ((row0 + len - 1) >> 4) - pg0 + 1 : 0;
+#pragma unroll
+    for (int i = 0; i < kTierPf; ++i)
+      if (i < npg) tr.pslot[lane][i] = __ldcg(tr.slot_of + pg0 + i);
+    for (int i = 0; i < npg; ++i) tr.use[pg0 + i] = tr.step;
+    __syncwarp();
+    const int incl = warp_inclusive_scan(len);
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    const int my0 = fpos + incl - len, my1 = my0 + len;
+    const int A = fpos, B = fpos + total;
+    for (int t = A / kD3Rows; ok && t * kD3Rows < B; ++t) {
+      const int s = t % kD3Stages, r = t / kD3Stages;
+      const int lo = max(A, t * kD3Rows), hi = min(B, (t + 1) * kD3Rows);
+      if (lane == 0 && t > opened && r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, err)) ok = false;
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      opened = max(opened, t);
+      if (!ok) break;
+      unsigned own = __ballot_sync(0xffffffffu, len > 0 && my0 < hi && my1 > lo);
+      bf16* dbase = (lane < 16 ? st[s].k : st[s].v) + (lane & 15) * 8;
+      while (own) {
+        const int L = __ffs(own) - 1;
+        own &= own - 1;
+        const int L0 = __shfl_sync(0xffffffffu, my0, L), L1 = __shfl_sync(0xffffffffu, my1, L);
+        const int Lrow0 = __shfl_sync(0xffffffffu, row0, L);
+        for (int i = max(L0, lo); i < min(L1, hi); ++i) {  // uniform
+          const int sr = Lrow0 + (i - L0);
+          const int pgi = (sr >> 4) - (Lrow0 >> 4);
+          const int slot = pgi < kTierPf ? tr.pslot[L][pgi] : __ldcg(tr.slot_of + (sr >> 4));
+          const bf16* src = slot >= 0 ? (lane < 16 ? tr.poolK : tr.poolV) + ((size_t)slot * kWiPageRows + (sr & 15)) * WI_D
+                                      : (lane < 16 ? tr.hostK : tr.hostV) + (size_t)sr * WI_D;
+          cp_async16(dbase + (i - t * kD3Rows) * WI_D, src + (lane & 15) * 8);
+          if (slot >= 0) ++tr.n_cache; else ++tr.n_host;
+        }
+      }
+      asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(&full[s])) : "memory");
+      __syncwarp();
+      if (hi == (t + 1) * kD3Rows && lane == 0) {  // the stage is full: hand it over
+        nrows[s] = kD3Rows;
+        mbar_arrive(&full[s]);
+      }
+    }
+    if (ok) fpos = B;
+    __syncwarp();  // the slot scratch is rewritten by the next batch
+  }
   // Close the partial last stage and send the end markers (kD3Groups consecutive stages with no
   // rows: one for every consumer group); on failure, close what is open and wait for the copies in
   // flight, so that none lands after the CTA left.
@@ -1264,7 +1337,7 @@ struct StagePacker {
   }
 };
 
-template <typename VT, int ROWS>
+template <typename VT, int ROWS, bool TIER>
 __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
   using Geo = D3Geo<ROWS>;
   constexpr int kD3Stages = Geo::Stages, kD3WPS = Geo::WPS, kD3Groups = Geo::Groups;
@@ -1276,6 +1349,7 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
   float* red = reinterpret_cast<float*>(nrows + 4 * kD3Stages);  // [warps][WI_PART]
   float* vred = red + kD3Warps * WI_PART;                         // [warps][WI_D] value-sum terms
   int* flags = reinterpret_cast<int*>(vred + kD3Warps * WI_D);    // abort, last CTA, kk, non-empty
+  int(*pslot)[kTierPf] = reinterpret_cast<int(*)[kTierPf]>(flags + 8);  // [32][kTierPf] (tier only)
   const int split = blockIdx.x, h = blockIdx.y, u = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t uh = (size_t)u * a.G + h;
@@ -1295,13 +1369,33 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
     const bf16* Ku = a.K + (size_t)u * a.n * WI_D;
     const bf16* Vu = a.V + (size_t)u * a.n * WI_D;
     StagePacker<ROWS> pk{st, full, empty, nrows, a.err};
+    const long long ntier = (long long)a.n_sink + a.W;  // rows per unit of the tier's steady copy
+    TierRows tr{};
+    if constexpr (TIER) {
+      const size_t pu = (size_t)u * a.tier.pages, su = (size_t)u * a.tier.slots * kWiPageRows * WI_D;
+      tr.slot_of = a.tier.slot_of + pu;
+      tr.poolK = static_cast<const bf16*>(a.tier.poolK) + su;
+      tr.poolV = static_cast<const bf16*>(a.tier.poolV) + su;
+      tr.hostK = static_cast<const bf16*>(a.tier.hostK) + (size_t)u * a.n * WI_D;
+      tr.hostV = static_cast<const bf16*>(a.tier.hostV) + (size_t)u * a.n * WI_D;
+      tr.use = a.tier.use + pu;
+      tr.step = a.tier.step;
+      tr.pslot = pslot;
+    }
     const int amax = a.max_append > 0 ? a.max_append : 1;
     if (split == 0) {
       // ---- steady rows first: the sinks and (in an index that cannot grow) the build's local window
       // are fixed since the build (copied before the wait), the rest of the window after it
       const size_t w0 = (size_t)(a.n - a.W) * WI_D;
       const int wl = a.gmax == 0 ? a.W : 0;
-      pk.push(lane == 0 ? Ku : Ku + w0, lane == 0 ? Vu : Vu + w0, lane == 0 ? a.n_sink : (lane == 1 ? wl : 0));
+      if constexpr (TIER) {  // the tier's device copy of the sinks and the window, [n_sink | W] rows
+        const bf16* Ks = static_cast<const bf16*>(a.tier.steadyK) + (size_t)u * ntier * WI_D;
+        const bf16* Vs = static_cast<const bf16*>(a.tier.steadyV) + (size_t)u * ntier * WI_D;
+        const size_t ws = (size_t)a.n_sink * WI_D;
+        pk.push(lane == 0 ? Ks : Ks + ws, lane == 0 ? Vs : Vs + ws, lane == 0 ? a.n_sink : (lane == 1 ? wl : 0));
+      } else {
+        pk.push(lane == 0 ? Ku : Ku + w0, lane == 0 ? Vu : Vu + w0, lane == 0 ? a.n_sink : (lane == 1 ? wl : 0));
+      }
     }
     pdl_wait();
     const int ngrown = a.gmax > 0 ? min(*a.grown, a.gmax) : 0;
@@ -1349,15 +1443,26 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
       const int len = valid ? rr.y - i_in : 0;
       const int before = warp_inclusive_scan(len) - len;
       const int take = max(0, min(len, rows_left - before));
-      const size_t o = in_grown ? (((size_t)gseg * a.U + u) * a.seg_len + goff + i_in) * WI_D
-                                : (size_t)(rr.x + i_in) * WI_D;
-      pk.push((in_grown ? a.grownK : Ku) + o, (in_grown ? a.grownV : Vu) + o, take);  // whole warp
+      if constexpr (TIER) {  // no grown segments with the tier
+        pk.push_tier(tr, rr.x + i_in, take);  // whole warp
+      } else {
+        const size_t o = in_grown ? (((size_t)gseg * a.U + u) * a.seg_len + goff + i_in) * WI_D
+                                  : (size_t)(rr.x + i_in) * WI_D;
+        pk.push((in_grown ? a.grownK : Ku) + o, (in_grown ? a.grownV : Vu) + o, take);  // whole warp
+      }
       rows_left -= __shfl_sync(0xffffffffu, warp_inclusive_scan(take), 31);
       in = 0;
       pos += 32;
     }
     pk.finish(&flags[0]);
     if (lane == 0) atomicAdd(a.rows_total, (unsigned long long)pk.fpos);
+    if constexpr (TIER) {
+      asm volatile("cp.async.wait_all;" ::: "memory");  // none of the copies lands after the CTA left
+      if (lane == 0) {
+        atomicAdd(a.tier.rows_src, tr.n_cache);
+        atomicAdd(a.tier.rows_src + 1, tr.n_host);
+      }
+    }
   } else {
     // ---- consumers
     pdl_wait();
@@ -1700,18 +1805,22 @@ cudaError_t launch_scores(const WiGeom& g, const WiDecodeBufs& b, const bf16* q,
                     reinterpret_cast<uint32_t*>(b.scores), b.kmaxp, g.C, b.p1, b.err);
 }
 
-template <typename VT, int ROWS>
+template <typename VT, int ROWS, bool TIER>
 cudaError_t launch_exact_rows(const WiGeom& g, const WiDecodeBufs& b, const ExactArgs& a, cudaStream_t st) {
   static int smem_set[kWiSmemDevices] = {};
   constexpr size_t smem = D3Geo<ROWS>::SMEM;
-  cudaError_t e = wi_ensure_smem(k_exact_merge<VT, ROWS>, smem, smem_set);
+  cudaError_t e = wi_ensure_smem(k_exact_merge<VT, ROWS, TIER>, smem, smem_set);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_exact_merge<VT, ROWS>, dim3(b.nsplit + 1, g.G, g.U), dim3(kD3Threads), smem, st, a);
+  return launch_pdl(k_exact_merge<VT, ROWS, TIER>, dim3(b.nsplit + 1, g.G, g.U), dim3(kD3Threads), smem, st, a);
 }
 
 template <typename VT>
 cudaError_t launch_exact(const WiGeom& g, const WiDecodeBufs& b, const ExactArgs& a, cudaStream_t st) {
-  return b.d3_rows == 32 ? launch_exact_rows<VT, 32>(g, b, a, st) : launch_exact_rows<VT, 64>(g, b, a, st);
+  if constexpr (sizeof(VT) == 4) {  // the tier holds fp32 value-sum indexes only
+    if (b.tier.on)
+      return b.d3_rows == 32 ? launch_exact_rows<VT, 32, true>(g, b, a, st) : launch_exact_rows<VT, 64, true>(g, b, a, st);
+  }
+  return b.d3_rows == 32 ? launch_exact_rows<VT, 32, false>(g, b, a, st) : launch_exact_rows<VT, 64, false>(g, b, a, st);
 }
 
 template <int G>
@@ -1800,6 +1909,7 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   a.W = g.W;
   a.max_append = g.max_append;
   a.lam = lam;
+  a.tier = b.tier;
   if (mask & 4u) e = b.valsum16 ? launch_exact<bf16>(g, b, a, st) : launch_exact<float>(g, b, a, st);
   if (e != cudaSuccess) return e;
   return mark(ev, 3, st);

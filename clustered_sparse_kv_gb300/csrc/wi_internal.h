@@ -64,6 +64,40 @@ bool wi_assign_tc_supported(const WiGeom& g);
 cudaError_t wi_launch_assign_tc(const WiGeom& g, const void* K, const void* chat, int32_t* assign, int* err,
                                 cudaStream_t st);
 
+// ---- host memory tier (wi_tier.cu): the build's clustered K/V rows held in page-locked host memory,
+// pages of kWiPageRows rows cached in device memory (the wave buffer).
+constexpr int kWiPageRows = 16;
+struct WiTierDev {
+  int on;                 // the exact kernel reads clustered rows through the tier
+  int slots;              // cache slots (pages) per unit
+  int pages;              // pages per unit: ceil(n / kWiPageRows) over the unit's row space [0, n)
+  int step;               // decode step number written into `use` (set per launch)
+  const int* slot_of;     // [U][pages] device: cache slot holding each page, or -1
+  const void* poolK;      // [U][slots][kWiPageRows][128] bf16, device
+  const void* poolV;
+  const void* hostK;      // [U][n][128] bf16 page-locked host memory (its device address)
+  const void* hostV;
+  const void* steadyK;    // [U][n_sink + W][128] bf16 device: the build's sink and window rows
+  const void* steadyV;
+  int* use;               // [U][pages] device: last step whose exact kernel read each page
+  unsigned long long* rows_src;  // [2] device: exact rows read from the cache, from host memory
+};
+
+struct WiTierHost;  // the tier's host side: replacement policy, thread, buffers (wi_tier.cu)
+// Copies the index's permuted K/V rows (device, [U][n][128] each) to page-locked host memory and the
+// sinks and window to a device copy, then waits for st: K and V are not read afterwards.
+int wi_tier_create(const WiGeom& g, const void* K, const void* V, int slots, int admit, int async, int device,
+                   cudaStream_t st, WiTierHost** out, WiTierDev* dev, char* msg, size_t len);
+void wi_tier_destroy(WiTierHost* T);
+int wi_tier_after_step(WiTierHost* T, long long step, cudaStream_t st, char* msg, size_t len);
+int wi_tier_round_now(WiTierHost* T, long long step, cudaStream_t st, char* msg, size_t len);
+void wi_tier_idle(WiTierHost* T);
+void wi_tier_counters(WiTierHost* T, long long out[6]);
+int wi_tier_geometry(const WiTierHost* T, int* slots, int* pages);
+const int* wi_tier_slot_table(const WiTierHost* T);
+const int* wi_tier_use_table(const WiTierHost* T);
+const unsigned long long* wi_tier_row_counters(const WiTierHost* T);
+
 // ---- decode kernels (wi_decode.cu)
 struct WiDecodeBufs {
   CUtensorMap map_mu;     // mu as rows of 128 bf16, 128-row boxes, 128-byte swizzle (tensor-core scores)
@@ -101,6 +135,7 @@ struct WiDecodeBufs {
   int est_first;          // the select/estimate launch starts its estimation CTAs first
   int nsplit;             // exact_merge CTAs per head over the selected rows (plus one for steady rows)
   int d3_rows;            // exact_merge stage height: 32 (one wave of CTAs) or 64 rows
+  WiTierDev tier;         // host memory tier (tier.on == 0: none)
   // dense comparator (full attention)
   float* dpart;           // [U][G][dsplits][WI_PART]  row-range partials
   unsigned int* dticket;  // [U]

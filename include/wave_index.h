@@ -303,6 +303,70 @@ int wi_index_build_stats(wi_index* ix, double* build_ms, double* assign_ms, int*
  * violation recorded by any kernel since the last call (WI_EDEVICE). */
 int wi_check_device(wi_index* ix);
 
+/*
+ * Host memory tier: the wave buffer (summaries de/fr/zh section 2.B: a GPU
+ * block cache of the KV blocks retrieval keeps returning to, LRU replacement
+ * run by the CPU asynchronously, an execution buffer that feeds attention the
+ * tokens from the steady zone, the cache and CPU memory).
+ *
+ * wi_tier_attach copies the index's permuted K and V (the caller's k / v,
+ * device) to page-locked host memory owned by the library and the sink and
+ * window rows to a device copy, and waits for `stream`; from then on no call
+ * reads the caller's k / v, which the caller may free or reuse.  The host
+ * rows are split into pages of 16 consecutive rows of a unit; each unit gets
+ * `slots_per_unit` (0 .. pages per unit) page slots in device memory, empty at
+ * first.  The exact-attention kernel of every later decode step copies each
+ * retrieved row from its cached page or, if the page is not cached, straight
+ * from host memory over the CPU-GPU link, and stamps the page with the step.
+ * A replacement round takes the pages read since the previous round, in
+ * increasing page order per unit: a cached page becomes the most recently
+ * used; a page not cached is admitted (at most `admit_per_round` per unit and
+ * round) into the lowest free slot, else into the slot of the least recently
+ * used page unless that page was read in this same round, in which case the
+ * round admits nothing more.  A round unmaps its victims on the decode stream,
+ * fills their slots from host memory on a stream of its own and maps the new
+ * pages on the decode stream once the fill has landed: decode never waits for
+ * a round and never reads a slot being refilled.  With async != 0 a library
+ * thread runs a round whenever it is idle after a decode step (on the newest
+ * stamps); with async == 0 rounds run only in wi_tier_round.  Outputs do not
+ * depend on where rows were read from: they equal the same index's outputs
+ * without the tier bit for bit.
+ * Needs an index that does not grow (max_append < seg_len) and fp32 value
+ * sums (WI_EUNSUPPORTED otherwise).  Afterwards wi_dense_decode returns
+ * WI_EUNSUPPORTED, and wi_decode_step refuses a stream being captured into a
+ * graph.  Host memory: 2 * units * n_ctx * 256 bytes; device: 2 * units *
+ * slots_per_unit * 4096 bytes plus 8 bytes per page for the tables.
+ */
+int wi_tier_attach(wi_index* ix, int slots_per_unit, int admit_per_round, int async, void* stream);
+
+/* One replacement round now, on the calling thread, over the pages read by
+ * every decode step enqueued so far; waits for a running round first and for
+ * the round's own work before returning. */
+int wi_tier_round(wi_index* ix, void* stream);
+
+/* Counters of the tier since attach, after waiting for any running round and
+ * the index's last stream: counters[6] = rounds, pages read (as the rounds saw
+ * them), of which cached, of which not, pages admitted, pages evicted;
+ * rows[2] = rows the exact-attention kernels copied from cached pages, from
+ * host memory.  slots / pages: slots and pages per unit.  Outputs may be NULL. */
+int wi_tier_stats(wi_index* ix, long long* counters, unsigned long long* rows, int* slots, int* pages);
+
+/* Test hook: the tier's tables, host int32 [units][pages] each: the slot
+ * holding each page (-1: not cached) and the last step that read it (-1:
+ * none).  Waits like wi_tier_stats.  Either output may be NULL. */
+int wi_tier_tables(wi_index* ix, int32_t* slot_of, int32_t* use);
+
+/* The tier's replacement policy alone, on the host (no device involved), for
+ * checking: a cache of `slots` pages out of `pages` for one unit.  wi_lru_round
+ * runs one round for the pages in `touched` (any order, repeats ignored) at
+ * round number t and writes the evictions and admissions, in the order it made
+ * them, as (page, slot) pairs; each output array needs room for n entries (any
+ * may be NULL).  wi_lru_new returns NULL for bad sizes. */
+void* wi_lru_new(int pages, int slots, int admit_max);
+int wi_lru_round(void* policy, const int32_t* touched, int n, long long t, int32_t* ev_pages, int32_t* ev_slots,
+                 int* n_ev, int32_t* ad_pages, int32_t* ad_slots, int* n_ad);
+void wi_lru_free(void* policy);
+
 /* Error-path testing: with the environment variable WI_FAIL_ALLOC_AT=n (n >= 1),
  * the n-th device allocation made for any index fails as out-of-memory; the
  * call returns WI_ENOMEM having released what it had allocated. */
