@@ -562,10 +562,10 @@ def h2d_copy_gbs(torch, dev, stream, gib=1.0):
 def tier_record(wi, torch, w, k_dev, v_dev, dev, stream, steps=256, warmup=16):
     """The host memory tier (wave buffer) on the main workload: K/V rows in page-locked host memory,
     a device page cache with LRU rounds on the library's thread.  Each case builds a fresh index,
-    attaches the tier and launches steps one by one (no graphs: the rounds enqueue work between
-    steps); the untiered index is timed the same way.  Two query streams: a fresh query every step
-    (the bench's stream) and each query held for 8 steps (temporal locality, which the pages credit
-    real decoding with)."""
+    attaches the tier and runs steps as a decoding loop does: each step launched, then its output
+    waited for before the next (no graphs: the rounds enqueue work between steps); the untiered index
+    is timed the same way.  Two query streams: a fresh query every step (the bench's stream) and each
+    query held for 8 steps (temporal locality, which the pages credit real decoding with)."""
     cfg = wi.config_from_workload(w)
     pages = w.n_ctx // 16
     qs = [torch.from_numpy(kvsynth.queries(w, step=s, seed=w.seed + 77).view(np.int16)).to(dev)
@@ -576,12 +576,13 @@ def tier_record(wi, torch, w, k_dev, v_dev, dev, stream, steps=256, warmup=16):
         with torch.cuda.stream(stream):
             for s in range(warmup):
                 ix.decode(qs[s // hold], out=out, stream=stream)
-            stream.synchronize()
-            before = ix.tier_stats() if ix is not None and getattr(ix, "_tier", False) else None
+                stream.synchronize()
+            before = ix.tier_stats() if getattr(ix, "_tier", False) else None
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for s in range(warmup, warmup + steps):
                 ix.decode(qs[s // hold], out=out, stream=stream)
+                stream.synchronize()
             e1.record(stream)
             e1.synchronize()
         return e0.elapsed_time(e1) / steps, before
@@ -612,7 +613,8 @@ def tier_record(wi, torch, w, k_dev, v_dev, dev, stream, steps=256, warmup=16):
     return {"workload": w.name, "page_rows": 16, "admit_per_round": 512,
             "device_kv_bytes_untiered": w.units * w.n_ctx * 512,
             "h2d_copy_gbs": h2d_copy_gbs(torch, dev, stream),
-            "timing": f"{steps} steps launched one by one after {warmup}, CUDA events on the launching stream",
+            "timing": f"{steps} steps after {warmup}, each launched after the previous step's output was waited "
+                      f"for; CUDA events on the launching stream around the loop",
             "cases": cases}
 
 
