@@ -269,9 +269,11 @@ def job_value(world, steps, batch, layers, seconds):
     return world * steps * batch * layers / seconds
 
 
-def profile_run(wi, torch, w, dev, steps, dense=False, device_gen=False):
+def profile_run(wi, torch, w, dev, steps, dense=False, device_gen=False, tier=None):
     """One index of the workload and `steps` decode steps (each followed by a dense comparator step
-    if asked), nothing timed: the small case of the ncu captures."""
+    if asked; with `tier`, the index behind the host memory tier with that fraction of its pages
+    cacheable, a replacement round after every step), nothing timed: the small case of the ncu
+    captures."""
     if device_gen:
         g = kvsynth.DeviceGen(w, device=dev)
         kd, vd = g.kv_cache()
@@ -282,10 +284,14 @@ def profile_run(wi, torch, w, dev, steps, dense=False, device_gen=False):
         vd = torch.from_numpy(v.view(np.int16)).to(dev)
         qs = [torch.from_numpy(kvsynth.queries(w, step=s).view(np.int16)).to(dev) for s in range(steps)]
     ix = wi.WaveIndex.build(wi.config_from_workload(w), kd, vd)
+    if tier is not None:
+        ix.attach_tier(int(tier * (w.n_ctx // 16)), 512, async_rounds=False)
     for s in range(steps):
         ix.decode(qs[s])
         if dense:
             ix.dense_decode(qs[s])
+        if tier is not None:
+            ix.tier_round()
     torch.cuda.synchronize()
     ix.check()
     ix.free()
@@ -610,9 +616,13 @@ def tier_record(wi, torch, w, k_dev, v_dev, dev, stream, steps=256, warmup=16):
         ix.check()
         ix.free()
         cases.append(rec)
+    link = h2d_copy_gbs(torch, dev, stream)
+    for rec in cases:   # the miss path's roofline: rows read from host memory against the link's copy rate
+        if "host_read_gbs" in rec:
+            rec["link_frac"] = rec["host_read_gbs"] / link
     return {"workload": w.name, "page_rows": 16, "admit_per_round": 512,
             "device_kv_bytes_untiered": w.units * w.n_ctx * 512,
-            "h2d_copy_gbs": h2d_copy_gbs(torch, dev, stream),
+            "h2d_copy_gbs": link,
             "timing": f"{steps} steps after {warmup}, each launched after the previous step's output was waited "
                       f"for; CUDA events on the launching stream around the loop",
             "cases": cases}
@@ -653,6 +663,9 @@ def main():
                     help="with --profile-steps: also run the dense comparator after every decode step")
     ap.add_argument("--profile-device-gen", action="store_true",
                     help="with --profile-steps: generate the workload on the device")
+    ap.add_argument("--profile-tier", type=float, default=None,
+                    help="with --profile-steps: the index behind the host memory tier, this fraction of its "
+                         "pages cacheable")
     ap.add_argument("--profile-units", default="",
                     help="with --profile-steps: batch,layers,kv_heads of a smaller case of the workload "
                          "(query heads per kv head kept), for captures whose traffic scales by units")
@@ -698,7 +711,7 @@ def main():
             b, l, h = (int(x) for x in args.profile_units.split(","))
             w = w.with_(batch=b, layers=l, n_kv_heads=h, n_q_heads=h * w.group)
         profile_run(wi, torch, w, dev, args.profile_steps, dense=args.profile_dense,
-                    device_gen=args.profile_device_gen)
+                    device_gen=args.profile_device_gen, tier=args.profile_tier)
         return
     hbm, tf_burst, tf_sust, peak_kind = peaks()
     k, v = kvsynth.kv_cache(w, seed=seed)
