@@ -729,9 +729,6 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   uint16_t* kbin = reinterpret_cast<uint16_t*>(ks);  // [C] distance bins (0xFFFF: empty cluster) if !cached
   constexpr uint32_t kFarBin = 64 * 30;               // log_bin(2^30): the far keys' bins start here
   int kk = min(min(*a.kcur, kmax), a.nonempty[u]);
-  // the steady rows' count (appended tokens, segments grown out of the window), read now so that the
-  // split computation at the end does not wait for another round trip
-  const long long n_steady = (long long)a.n_sink + a.W + max(*a.app_count, 0) - (long long)*a.grown * a.seg_len;
   // the first keys' loads are in flight across the K0 reduction and the barrier below
   const int n4 = C / 4;
   uint4 f[4];
@@ -947,7 +944,8 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
     int4* sruns = a.sruns + uh * NSP * 32;
     if (tid < NSP) {
       int4 sp = make_int4(0, 0, 0, 0);
-      const long long S = n_steady, T = S + R;
+      const long long S = (long long)a.n_sink + a.W + max(*a.app_count, 0) - (long long)*a.grown * a.seg_len,
+                      T = S + R;
       const int rb = (int)max(0LL, (T * tid) / NSP - S);
       if (R > 0 && rb < R) {
         int lo = 0, hi = kk - 1;  // largest position whose first row is <= rb
@@ -1002,7 +1000,8 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
     const int NSP = a.NS + 1;
     int4 sp = make_int4(kk, 0, R, 0);
     if (tid < NSP) {
-      const long long S = n_steady, T = S + R;
+      const long long S = (long long)a.n_sink + a.W + max(*a.app_count, 0) - (long long)*a.grown * a.seg_len,
+                      T = S + R;
       const int rb = (int)max(0LL, (T * tid) / NSP - S);
       if (R > 0 && rb < R) {
         int lo = 0, hi = kk - 1;  // largest position whose first row is <= rb
