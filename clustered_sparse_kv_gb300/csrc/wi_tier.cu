@@ -34,6 +34,7 @@
 #include <atomic>
 #include <condition_variable>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <functional>
 #include <mutex>
@@ -319,8 +320,17 @@ int wi_tier_create(const WiGeom& g, const void* K, const void* V, int slots, int
   T->cap = std::max<size_t>(1, (size_t)g.U * (size_t)T->admit);
   const size_t U = g.U, rows = (size_t)g.U * g.n, ns = (size_t)g.n_sink + g.W;
   cudaError_t e = cudaSuccess;
+  // fault injection for the error path: WI_FAIL_TIER_ALLOC_AT=n makes the n-th allocation (device or
+  // page-locked host) of the tier report out-of-memory, nothing allocated
+  const char* fenv = getenv("WI_FAIL_TIER_ALLOC_AT");
+  const int fail_at = fenv ? atoi(fenv) : 0;
+  int n_alloc = 0;
+  auto refused = [&]() { return ++n_alloc == fail_at; };
   auto A = [&](void** p, size_t bytes) {
-    if (e == cudaSuccess) e = cudaMalloc(p, std::max<size_t>(bytes, 16));
+    if (e == cudaSuccess) e = refused() ? cudaErrorMemoryAllocation : cudaMalloc(p, std::max<size_t>(bytes, 16));
+  };
+  auto H = [&](void** p, size_t bytes, unsigned flags) {
+    if (e == cudaSuccess) e = refused() ? cudaErrorMemoryAllocation : cudaHostAlloc(p, std::max<size_t>(bytes, 16), flags);
   };
   A(reinterpret_cast<void**>(&T->slot_of), U * pages * 4);
   A(reinterpret_cast<void**>(&T->use), U * pages * 4);
@@ -331,11 +341,11 @@ int wi_tier_create(const WiGeom& g, const void* K, const void* V, int slots, int
   A(reinterpret_cast<void**>(&T->rows_src), 16);
   A(reinterpret_cast<void**>(&T->patch_d), 2 * T->cap * sizeof(int2));
   A(reinterpret_cast<void**>(&T->fill_d), T->cap * sizeof(int4));
-  if (e == cudaSuccess) e = cudaHostAlloc(&T->hostK, rows * WI_D * 2, cudaHostAllocMapped);
-  if (e == cudaSuccess) e = cudaHostAlloc(&T->hostV, rows * WI_D * 2, cudaHostAllocMapped);
-  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&T->use_h), U * pages * 4, cudaHostAllocDefault);
-  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&T->patch_h), 2 * T->cap * sizeof(int2), cudaHostAllocDefault);
-  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&T->fill_h), T->cap * sizeof(int4), cudaHostAllocDefault);
+  H(&T->hostK, rows * WI_D * 2, cudaHostAllocMapped);
+  H(&T->hostV, rows * WI_D * 2, cudaHostAllocMapped);
+  H(reinterpret_cast<void**>(&T->use_h), U * pages * 4, cudaHostAllocDefault);
+  H(reinterpret_cast<void**>(&T->patch_h), 2 * T->cap * sizeof(int2), cudaHostAllocDefault);
+  H(reinterpret_cast<void**>(&T->fill_h), T->cap * sizeof(int4), cudaHostAllocDefault);
   if (e == cudaSuccess) e = cudaHostGetDevicePointer(&T->hostK_d, T->hostK, 0);
   if (e == cudaSuccess) e = cudaHostGetDevicePointer(&T->hostV_d, T->hostV, 0);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&T->side, cudaStreamNonBlocking);
@@ -343,7 +353,8 @@ int wi_tier_create(const WiGeom& g, const void* K, const void* V, int slots, int
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     const int code = (e == cudaErrorMemoryAllocation) ? WI_ENOMEM : WI_ECUDA;
-    tier_fail(msg, len, code, "tier allocation", e);
+    if (n_alloc == fail_at) snprintf(msg, len, "tier allocation %d refused (WI_FAIL_TIER_ALLOC_AT)", fail_at);
+    else tier_fail(msg, len, code, "tier allocation", e);
     wi_tier_destroy(T);
     return code;
   }

@@ -369,7 +369,9 @@ void wi_lru_free(void* policy);
 
 /* Error-path testing: with the environment variable WI_FAIL_ALLOC_AT=n (n >= 1),
  * the n-th device allocation made for any index fails as out-of-memory; the
- * call returns WI_ENOMEM having released what it had allocated. */
+ * call returns WI_ENOMEM having released what it had allocated.  Likewise
+ * WI_FAIL_TIER_ALLOC_AT=n for the n-th allocation (device or page-locked
+ * host) of wi_tier_attach, which then leaves the index as it was. */
 
 /* Release the index and everything it owns (not k / v).  NULL is a no-op.
  * Synchronises the device first. */

@@ -193,3 +193,28 @@ def test_tier_refusals(wi):
         vb.attach_tier(8, 4)
     assert e.value.code == wi.WI_EUNSUPPORTED
     vb.free()
+
+
+def test_tier_allocation_failure_leaves_the_index_usable(wi, monkeypatch):
+    """Every allocation of the tier refused in turn: attach reports WI_ENOMEM, the index decodes as
+    before (untiered, from the caller's K/V), and a later attach succeeds."""
+    w = workload(45)
+    a, b, idx, K, V = pair(wi, w)
+    q = dev16(kvsynth.queries(w, step=0))
+    ref = a.decode(q).clone()
+    for n in range(1, 15):   # nine device allocations, five page-locked host ones
+        monkeypatch.setenv("WI_FAIL_TIER_ALLOC_AT", str(n))
+        with pytest.raises(wi.WiError) as e:
+            b.attach_tier(32, 16)
+        assert e.value.code == wi.WI_ENOMEM, n
+        assert "WI_FAIL_TIER_ALLOC_AT" in str(e.value)
+        assert torch.equal(b.decode(q), ref), n
+    monkeypatch.setenv("WI_FAIL_TIER_ALLOC_AT", "15")   # past the last allocation: nothing refused
+    b.attach_tier(32, 16, async_rounds=False)
+    monkeypatch.delenv("WI_FAIL_TIER_ALLOC_AT")
+    b.k.fill_(NAN16)
+    b.v.fill_(NAN16)
+    assert torch.equal(b.decode(q), ref)
+    b.check()
+    a.free()
+    b.free()
