@@ -571,7 +571,8 @@ def tier_record(wi, torch, w, k_dev, v_dev, dev, stream, steps=256, warmup=16):
     attaches the tier and runs steps as a decoding loop does: each step launched, then its output
     waited for before the next (no graphs: the rounds enqueue work between steps); the untiered index
     is timed the same way.  Two query streams: a fresh query every step (the bench's stream) and each
-    query held for 8 steps (temporal locality, which the pages credit real decoding with)."""
+    query held for 8 steps (temporal locality, which the pages credit real decoding with); last, one query
+    for the whole run, whose pages all end up cached (the hit path alone)."""
     cfg = wi.config_from_workload(w)
     pages = w.n_ctx // 16
     qs = [torch.from_numpy(kvsynth.queries(w, step=s, seed=w.seed + 77).view(np.int16)).to(dev)
@@ -594,7 +595,7 @@ def tier_record(wi, torch, w, k_dev, v_dev, dev, stream, steps=256, warmup=16):
         return e0.elapsed_time(e1) / steps, before
 
     cases = []
-    for frac, hold in [(None, 1), (0.0, 1), (0.25, 1), (0.25, 8), (1.0, 8)]:
+    for frac, hold in [(None, 1), (0.0, 1), (0.25, 1), (0.25, 8), (1.0, 8), (1.0, steps + warmup)]:
         ix = wi.WaveIndex.build(cfg, k_dev.clone(), v_dev.clone(), stream=stream)
         stream.synchronize()
         slots = 0 if frac is None else int(frac * pages)
