@@ -579,11 +579,13 @@ def tier_record(wi, torch, w, k_dev, v_dev, dev, stream, steps=256, warmup=16):
           for s in range(steps + warmup)]
     out = torch.empty((w.batch, w.layers, w.n_q_heads, 128), dtype=torch.float32, device=dev)
 
-    def run(ix, hold):
+    def run(ix, hold, rounds_async):
         with torch.cuda.stream(stream):
             for s in range(warmup):
                 ix.decode(qs[s // hold], out=out, stream=stream)
                 stream.synchronize()
+                if getattr(ix, "_tier", False) and not rounds_async:
+                    ix.tier_round(stream=stream)   # rounds after every warm-up step, none while timed
             before = ix.tier_stats() if getattr(ix, "_tier", False) else None
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -595,15 +597,25 @@ def tier_record(wi, torch, w, k_dev, v_dev, dev, stream, steps=256, warmup=16):
         return e0.elapsed_time(e1) / steps, before
 
     cases = []
-    for frac, hold in [(None, 1), (0.0, 1), (0.25, 1), (0.25, 8), (1.0, 8), (1.0, steps + warmup)]:
+    every = steps + warmup
+    for frac, hold, rounds_async in [(None, 1, True), (0.0, 1, True), (0.25, 1, True), (0.25, 8, True),
+                                     (1.0, 8, True), (1.0, every, True), (None, every, True), (1.0, every, False)]:
         ix = wi.WaveIndex.build(cfg, k_dev.clone(), v_dev.clone(), stream=stream)
         stream.synchronize()
         slots = 0 if frac is None else int(frac * pages)
         if frac is not None:
-            ix.attach_tier(slots, 512, async_rounds=True, stream=stream)
+            ix.attach_tier(slots, 512, async_rounds=rounds_async, stream=stream)
             ix._tier = True
-        ms, before = run(ix, hold)
-        rec = {"slots_fraction": frac, "query_held_steps": hold, "ms_per_step": ms, "steps_per_s": 1e3 / ms}
+        ms, before = run(ix, hold, rounds_async)
+        rec = {"slots_fraction": frac, "query_held_steps": hold, "rounds_while_timed": rounds_async and frac is not None,
+               "ms_per_step": ms, "steps_per_s": 1e3 / ms}
+        if not rounds_async or frac is None:   # the exact kernel alone: a graph of 64 launches of it
+            timer = Timer(torch, stream)
+            kid = wi.DECODE_KERNELS.index("exact_merge")
+            g = timer.graph(lambda s_: wi.wi_decode_kernel(ix.handle, kid, qs[-1], out, stream), 64)
+            timer.replay([g])
+            rec["exact_alone_us"] = 1e3 * timer.replay([g] * 3) / (3 * 64)
+            del g
         if frac is not None:
             st = ix.tier_stats()
             rc = st["rows_from_cache"] - before["rows_from_cache"]

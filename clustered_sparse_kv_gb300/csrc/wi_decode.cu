@@ -1190,7 +1190,8 @@ struct TierRows {
   int* use;
   int step;
   int (*pslot)[kTierPf];  // shared memory: [lane][page of its run] slots
-  unsigned long long n_cache = 0, n_host = 0;  // rows copied (lane 0's count of the warp's rows)
+  unsigned long long n_cache = 0, n_host = 0;  // rows copied: this lane's from cached pages; the warp's
+                                               // from host memory (every lane counts them all)
 };
 
 // Producer of exact_merge: the whole producer warp.  The CTA's rows form one
@@ -1250,10 +1251,12 @@ struct StagePacker {
   }
 
   // The same stream through the host memory tier: this lane's run is rows [row0, row0 + len) of the
-  // unit's row space.  Its pages' slots are looked up first (one round trip for the warp); then for
-  // every stage the warp copies the stage's rows one row per instruction (16 bytes per lane: lanes
-  // 0-15 the key row, 16-31 the value row) with cp.async from the cached page or from host memory,
-  // and every lane arms the stage's barrier with an arrive on completion of its copies.
+  // unit's row space.  Its pages' slots are looked up first (one round trip for the warp).  For every
+  // stage, each lane bulk-copies the pieces of its part that sit in cached pages (a piece ends at a
+  // page boundary), after lane 0 announced their bytes; then the warp copies the rows of the pages
+  // not cached, one row per instruction (16 bytes per lane: lanes 0-15 the key row, 16-31 the value
+  // row) with cp.async from host memory, and every lane arms the stage's barrier with an arrive on
+  // completion of its copies.
   __device__ void push_tier(TierRows& tr, int row0, int len) {
     const int lane = threadIdx.x & 31;
     const int pg0 = row0 >> 4;
@@ -1274,7 +1277,38 @@ struct StagePacker {
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       opened = max(opened, t);
       if (!ok) break;
-      unsigned own = __ballot_sync(0xffffffffu, len > 0 && my0 < hi && my1 > lo);
+      // this lane's part of the stage, page piece by page piece: the cached pieces by bulk copy
+      const int q0 = max(my0, lo), q1 = min(my1, hi);
+      auto piece_slot = [&](int sr) {
+        const int pgi = (sr >> 4) - pg0;
+        return pgi < kTierPf ? tr.pslot[lane][pgi] : __ldcg(tr.slot_of + (sr >> 4));
+      };
+      int cbytes = 0, hrows = 0;
+      for (int i = q0; i < q1;) {
+        const int sr = row0 + (i - my0), e = min(q1, i + kWiPageRows - (sr & 15));
+        if (piece_slot(sr) >= 0) cbytes += (e - i) * WI_D * 4; else hrows += e - i;
+        i = e;
+      }
+      const int cb = __reduce_add_sync(0xffffffffu, cbytes);
+      if (lane == 0 && cb > 0)
+        asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&full[s])),
+                     "r"((uint32_t)cb)
+                     : "memory");
+      __syncwarp();
+      for (int i = q0; i < q1;) {
+        const int sr = row0 + (i - my0), e = min(q1, i + kWiPageRows - (sr & 15));
+        const int slot = piece_slot(sr);
+        if (slot >= 0) {
+          const size_t o = ((size_t)slot * kWiPageRows + (sr & 15)) * WI_D;
+          const uint32_t bytes = (uint32_t)(e - i) * WI_D * 2;
+          bulk_g2s(&st[s].k[(i - t * kD3Rows) * WI_D], tr.poolK + o, bytes, &full[s]);
+          bulk_g2s(&st[s].v[(i - t * kD3Rows) * WI_D], tr.poolV + o, bytes, &full[s]);
+          tr.n_cache += e - i;  // this lane's cached rows
+        }
+        i = e;
+      }
+      // the rows of pages not cached: the lanes that own some, one row per warp instruction
+      unsigned own = __ballot_sync(0xffffffffu, hrows > 0);
       bf16* dbase = (lane < 16 ? st[s].k : st[s].v) + (lane & 15) * 8;
       while (own) {
         const int L = __ffs(own) - 1;
@@ -1285,10 +1319,10 @@ struct StagePacker {
           const int sr = Lrow0 + (i - L0);
           const int pgi = (sr >> 4) - (Lrow0 >> 4);
           const int slot = pgi < kTierPf ? tr.pslot[L][pgi] : __ldcg(tr.slot_of + (sr >> 4));
-          const bf16* src = slot >= 0 ? (lane < 16 ? tr.poolK : tr.poolV) + ((size_t)slot * kWiPageRows + (sr & 15)) * WI_D
-                                      : (lane < 16 ? tr.hostK : tr.hostV) + (size_t)sr * WI_D;
+          if (slot >= 0) continue;  // bulk-copied above (uniform)
+          const bf16* src = (lane < 16 ? tr.hostK : tr.hostV) + (size_t)sr * WI_D;
           cp_async16(dbase + (i - t * kD3Rows) * WI_D, src + (lane & 15) * 8);
-          if (slot >= 0) ++tr.n_cache; else ++tr.n_host;
+          ++tr.n_host;
         }
       }
       asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(&full[s])) : "memory");
@@ -1458,8 +1492,9 @@ __global__ void __launch_bounds__(kD3Threads, 2) k_exact_merge(ExactArgs a) {
     if (lane == 0) atomicAdd(a.rows_total, (unsigned long long)pk.fpos);
     if constexpr (TIER) {
       asm volatile("cp.async.wait_all;" ::: "memory");  // none of the copies lands after the CTA left
+      const unsigned nc = __reduce_add_sync(0xffffffffu, (unsigned)tr.n_cache);
       if (lane == 0) {
-        atomicAdd(a.tier.rows_src, tr.n_cache);
+        atomicAdd(a.tier.rows_src, (unsigned long long)nc);
         atomicAdd(a.tier.rows_src + 1, tr.n_host);
       }
     }
