@@ -218,3 +218,32 @@ def test_tier_allocation_failure_leaves_the_index_usable(wi, monkeypatch):
     b.check()
     a.free()
     b.free()
+
+
+@pytest.mark.parametrize("group_topk", [0, 1])
+def test_tier_host_buffers_and_group_retrieval(wi, group_topk):
+    """The host-buffer entry point (query and output in page-locked host memory) and group-shared
+    retrieval through the tier: the same bits as the untiered index."""
+    w = workload(46)
+    k, v, q, K, V, Q = gen(w)
+    idx = oracle.build_index(K, V, params_of(w))
+    cfg = wi.config_from_workload(w)
+    cfg.group_topk = group_topk
+    a = wi.WaveIndex.adopt(cfg, dev16(k), dev16(v), *index_arrays(idx))
+    b = wi.WaveIndex.adopt(cfg, dev16(k), dev16(v), *index_arrays(idx))
+    b.attach_tier(w.n_ctx // PAGE // 4, 64, async_rounds=True)
+    b.k.fill_(NAN16)
+    b.v.fill_(NAN16)
+    oh_a = torch.empty((w.batch, w.layers, w.n_q_heads, 128), dtype=torch.float32).pin_memory()
+    oh_b = torch.empty_like(oh_a).pin_memory()
+    for t in range(6):
+        qh = torch.from_numpy(kvsynth.queries(w, step=t // 2).view(np.int16)).pin_memory()
+        wi.wi_decode_step_host(a.handle, qh, oh_a)
+        wi.wi_decode_step_host(b.handle, qh, oh_b)
+        assert torch.equal(oh_a, oh_b), t
+    st = b.tier_stats()
+    assert st["rows_from_cache"] + st["rows_from_host"] > 0
+    a.check()
+    b.check()
+    a.free()
+    b.free()
