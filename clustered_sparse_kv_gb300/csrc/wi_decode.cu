@@ -548,7 +548,8 @@ struct TopkArgs {
 struct alignas(16) SelSmem {
   int hist[2][kTopkBins];
   int s_wsum[32];
-  int s_bin, s_above, s_ncand, s_pad;
+  int s_bin, s_above, s_ncand, s_app;  // s_app, s_grown: the steady-row counters, fetched early
+  int s_grown, s_pad[3];
   uint64_t s_bar, s_pad2;  // completion of the keys' bulk copy (cached keys)
   int s_spos[68];  // first position of each split
   int s_wt[32];
@@ -741,6 +742,10 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
   };
   // cached keys: one bulk copy of the head's C keys into shared memory (the copy engine fetches them
   // as one request instead of every thread's vector loads); above kSelKeysMax, vector loads
+  if (tid == 0) {  // the steady-row counters the split computation needs at the end, in flight meanwhile
+    cp_async4(&sm.s_app, a.app_count);
+    cp_async4(&sm.s_grown, a.grown);
+  }
   if (cached) {
     if (tid == 0) {
       mbar_init(&sm.s_bar, 1);
@@ -944,7 +949,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
     int4* sruns = a.sruns + uh * NSP * 32;
     if (tid < NSP) {
       int4 sp = make_int4(0, 0, 0, 0);
-      const long long S = (long long)a.n_sink + a.W + max(*a.app_count, 0) - (long long)*a.grown * a.seg_len,
+      const long long S = (long long)a.n_sink + a.W + max(sm.s_app, 0) - (long long)sm.s_grown * a.seg_len,
                       T = S + R;
       const int rb = (int)max(0LL, (T * tid) / NSP - S);
       if (R > 0 && rb < R) {
@@ -1000,7 +1005,7 @@ __device__ __forceinline__ void select_role(unsigned char* raw, const TopkArgs& 
     const int NSP = a.NS + 1;
     int4 sp = make_int4(kk, 0, R, 0);
     if (tid < NSP) {
-      const long long S = (long long)a.n_sink + a.W + max(*a.app_count, 0) - (long long)*a.grown * a.seg_len,
+      const long long S = (long long)a.n_sink + a.W + max(sm.s_app, 0) - (long long)sm.s_grown * a.seg_len,
                       T = S + R;
       const int rb = (int)max(0LL, (T * tid) / NSP - S);
       if (R > 0 && rb < R) {
