@@ -142,6 +142,13 @@ def test_tier_async_rounds_and_appends(wi):
     assert st["rounds"] >= 1 and st["admitted"] > 0
     assert st["page_hits"] + st["page_misses"] == st["pages_read"]
     assert st["evicted"] <= st["admitted"]
+    # a round on request while the thread runs them too: it waits for the thread's round, then runs
+    b.tier_round()
+    assert b.tier_stats()["rounds"] == st["rounds"] + 1
+    ob = b.decode(dev16(kvsynth.queries(w, step=T)))
+    oa = a.decode(dev16(kvsynth.queries(w, step=T)))
+    torch.cuda.synchronize()
+    assert torch.equal(oa, ob)
     slot_of, use = (x.numpy() for x in b.tier_tables())
     for u in range(w.units):
         used = slot_of[u][slot_of[u] >= 0]
