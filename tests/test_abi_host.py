@@ -104,6 +104,14 @@ def test_calls_on_null_index(wi):
     assert wi.lib.wi_last_selection(None, 16, None, None) == -1
     assert wi.lib.wi_index_shape(None, None, None, None, None, None) == -1
     assert wi.lib.wi_check_device(None) == -1
+    assert wi.lib.wi_tier_attach(None, 8, 8, 0, None) == -1
+    assert wi.lib.wi_tier_round(None, None) == -1
+    assert wi.lib.wi_tier_stats(None, None, None, None, None) == -1
+    assert wi.lib.wi_tier_tables(None, None, None) == -1
+    assert "no host memory tier" in wi.lib.wi_last_error().decode() or "NULL" in wi.lib.wi_last_error().decode()
+    assert wi.lib.wi_lru_new(0, 4, 4) is None     # bad sizes: no policy
+    assert wi.lib.wi_lru_round(None, None, 0, 0, None, None, None, None, None, None) == -1
+    wi.lib.wi_lru_free(None)  # no-op
     wi.lib.wi_free(None)  # no-op
     cfg = good_cfg(wi)
     assert wi.lib.wi_kmeans_step(ctypes.byref(cfg), None, 16, 16, 16, None) == -1
