@@ -38,6 +38,7 @@
 #include <cstring>
 #include <functional>
 #include <mutex>
+#include <new>
 #include <queue>
 #include <thread>
 #include <utility>
@@ -285,7 +286,14 @@ void worker(WiTierHost* T) {
     char msg[256] = {0};
     cudaError_t e = cudaEventSynchronize(T->ev_snap);
     if (e != cudaSuccess) rc = tier_fail(msg, sizeof(msg), WI_ECUDA, "tier snapshot wait", e);
-    if (rc == WI_OK) rc = run_round(T, t, st, msg, sizeof(msg));
+    if (rc == WI_OK) {
+      try {
+        rc = run_round(T, t, st, msg, sizeof(msg));
+      } catch (...) {  // host memory for the round's lists ran out: the thread stops its rounds
+        snprintf(msg, sizeof(msg), "tier round: host allocation failed");
+        rc = WI_ENOMEM;
+      }
+    }
     lk.lock();
     if (rc != WI_OK && T->werr.load() == 0) {
       snprintf(T->wmsg, sizeof(T->wmsg), "%s", msg);
@@ -310,7 +318,11 @@ int wi_tier_create(const WiGeom& g, const void* K, const void* V, int slots, int
     snprintf(msg, len, "admit_per_round must be >= 0");
     return WI_EINVAL;
   }
-  WiTierHost* T = new WiTierHost();
+  WiTierHost* T = new (std::nothrow) WiTierHost();
+  if (!T) {
+    snprintf(msg, len, "tier: host allocation failed");
+    return WI_ENOMEM;
+  }
   T->g = g;
   T->slots = slots;
   T->pages = pages;
@@ -380,9 +392,15 @@ int wi_tier_create(const WiGeom& g, const void* K, const void* V, int slots, int
     wi_tier_destroy(T);
     return WI_ECUDA;
   }
-  T->pol.reserve(U);
-  for (size_t u = 0; u < U; ++u) T->pol.emplace_back(pages, slots, T->admit);
-  if (T->async) T->th = std::thread(worker, T);
+  try {
+    T->pol.reserve(U);
+    for (size_t u = 0; u < U; ++u) T->pol.emplace_back(pages, slots, T->admit);
+    if (T->async) T->th = std::thread(worker, T);
+  } catch (...) {  // host memory for the policy, or the replacement thread, could not be had
+    snprintf(msg, len, "tier: the replacement policy or its thread could not be set up");
+    wi_tier_destroy(T);
+    return WI_ENOMEM;
+  }
   dev->on = 1;
   dev->slots = slots;
   dev->pages = pages;
@@ -456,7 +474,14 @@ int wi_tier_round_now(WiTierHost* T, long long step, cudaStream_t st, char* msg,
     const cudaError_t e = cudaEventSynchronize(T->ev_snap);
     if (e != cudaSuccess) rc = tier_fail(msg, len, WI_ECUDA, "tier snapshot wait", e);
   }
-  if (rc == WI_OK) rc = run_round(T, step, st, msg, len);
+  if (rc == WI_OK) {
+    try {
+      rc = run_round(T, step, st, msg, len);
+    } catch (...) {
+      snprintf(msg, len, "tier round: host allocation failed");
+      rc = WI_ENOMEM;
+    }
+  }
   lk.lock();
   T->busy = false;
   T->cv.notify_all();
@@ -484,6 +509,9 @@ const int* wi_tier_use_table(const WiTierHost* T) { return T->use; }
 const unsigned long long* wi_tier_row_counters(const WiTierHost* T) { return T->rows_src; }
 
 // ---- the replacement policy alone, for checking on the host (no device involved)
+static int lru_round_impl(LruPages* L, const int32_t* touched, int n, long long t, int32_t* ev_pages,
+                          int32_t* ev_slots, int* n_ev, int32_t* ad_pages, int32_t* ad_slots, int* n_ad);
+
 extern "C" {
 
 void* wi_lru_new(int pages, int slots, int admit_max) {
@@ -499,6 +527,17 @@ int wi_lru_round(void* h, const int32_t* touched, int n, long long t, int32_t* e
                  int* n_ev, int32_t* ad_pages, int32_t* ad_slots, int* n_ad) {
   if (!h || n < 0 || (n > 0 && !touched) || !n_ev || !n_ad) return WI_EINVAL;
   LruPages* L = static_cast<LruPages*>(h);
+  try {
+    return lru_round_impl(L, touched, n, t, ev_pages, ev_slots, n_ev, ad_pages, ad_slots, n_ad);
+  } catch (...) {
+    return WI_ENOMEM;
+  }
+}
+
+}  // extern "C"
+
+static int lru_round_impl(LruPages* L, const int32_t* touched, int n, long long t, int32_t* ev_pages,
+                          int32_t* ev_slots, int* n_ev, int32_t* ad_pages, int32_t* ad_slots, int* n_ad) {
   std::vector<int> tp(touched, touched + n);
   std::sort(tp.begin(), tp.end());
   tp.erase(std::unique(tp.begin(), tp.end()), tp.end());
@@ -519,6 +558,4 @@ int wi_lru_round(void* h, const int32_t* touched, int n, long long t, int32_t* e
   return WI_OK;
 }
 
-void wi_lru_free(void* h) { delete static_cast<LruPages*>(h); }
-
-}  // extern "C"
+extern "C" void wi_lru_free(void* h) { delete static_cast<LruPages*>(h); }
