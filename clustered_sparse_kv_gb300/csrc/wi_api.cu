@@ -455,8 +455,8 @@ extern "C" {
 
 const char* wi_last_error(void) { return g_err; }
 
-int wi_build_index(const wi_config* cfg, void* k, void* v, const void* init_centroids, void* stream,
-                   wi_index** out) {
+static int build_index_impl(const wi_config* cfg, void* k, void* v, const void* init_centroids, void* stream,
+                            wi_index** out) {
   g_err[0] = 0;
   wi_index* ix = nullptr;
   int rc = new_index(cfg, k, v, out, &ix);
@@ -513,7 +513,7 @@ done:
   return rc;
 }
 
-int wi_index_import(const wi_config* cfg, void* k, void* v, const int32_t* counts, const int32_t* perm,
+static int index_import_impl(const wi_config* cfg, void* k, void* v, const int32_t* counts, const int32_t* perm,
                     const uint16_t* mu, const float* valsum, void* stream, wi_index** out) {
   g_err[0] = 0;
   wi_index* ix = nullptr;
@@ -833,7 +833,7 @@ int wi_init_centroids(const wi_config* cfg, const void* k, void* centroids, void
   return WI_OK;
 }
 
-int wi_profile_begin(wi_index* ix, int max_steps) {
+static int profile_begin_impl(wi_index* ix, int max_steps) {
   g_err[0] = 0;
   if (!ix || max_steps < 0) return fail(WI_EINVAL, "index is NULL or max_steps < 0");
   for (cudaEvent_t e : ix->prof_ev) cudaEventDestroy(e);
@@ -960,6 +960,36 @@ int wi_tier_tables(wi_index* ix, int32_t* slot_of, int32_t* use) {
   if (slot_of) WI_CUDA(cudaMemcpy(slot_of, wi_tier_slot_table(ix->tier), bytes, cudaMemcpyDeviceToHost));
   if (use) WI_CUDA(cudaMemcpy(use, wi_tier_use_table(ix->tier), bytes, cudaMemcpyDeviceToHost));
   return WI_OK;
+}
+
+// The entry points that allocate host memory (std::vector, the index object's lists): an allocation
+// failure is reported as WI_ENOMEM, never thrown across the C ABI.
+int wi_build_index(const wi_config* cfg, void* k, void* v, const void* init_centroids, void* stream,
+                   wi_index** out) {
+  try {
+    return build_index_impl(cfg, k, v, init_centroids, stream, out);
+  } catch (...) {
+    if (out) *out = nullptr;
+    return fail(WI_ENOMEM, "host allocation failed");
+  }
+}
+
+int wi_index_import(const wi_config* cfg, void* k, void* v, const int32_t* counts, const int32_t* perm,
+                    const uint16_t* mu, const float* valsum, void* stream, wi_index** out) {
+  try {
+    return index_import_impl(cfg, k, v, counts, perm, mu, valsum, stream, out);
+  } catch (...) {
+    if (out) *out = nullptr;
+    return fail(WI_ENOMEM, "host allocation failed");
+  }
+}
+
+int wi_profile_begin(wi_index* ix, int max_steps) {
+  try {
+    return profile_begin_impl(ix, max_steps);
+  } catch (...) {
+    return fail(WI_ENOMEM, "host allocation failed");
+  }
 }
 
 void wi_free(wi_index* ix) {
