@@ -72,10 +72,20 @@ def run_case(wi, w, idx=None, steps=1, append=False, kv=None, strict_ids=False):
     return worst
 
 
-@pytest.mark.parametrize("g", [1, 4, 7])
+@pytest.mark.parametrize("g", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_decode_parity_group_sizes(wi, g):
+    """Every group size the kernels are instantiated for (1-8 query heads per kv head: different
+    head packings in the scores MMA and the estimation's lane layout)."""
     w = small(n_ctx=4096, seg_len=1024, clusters_per_seg=64, iters=3, n_q_heads=g, n_kv_heads=1, budget_k=6)
     assert run_case(wi, w) < 1e-4
+
+
+@pytest.mark.parametrize("g", [3, 5, 8])
+def test_decode_parity_group_sizes_multi_unit(wi, g):
+    """The odd group sizes with several units and an appending step."""
+    w = small(batch=2, n_q_heads=2 * g, n_kv_heads=2, n_ctx=4096, seg_len=1024, clusters_per_seg=64, iters=2,
+              budget_k=7, seed=30 + g)
+    assert run_case(wi, w, steps=2, append=True) < 1e-4
 
 
 def test_decode_parity_multi_unit(wi):
@@ -394,7 +404,7 @@ def test_valsum_bf16_variant_built_index(wi):
     ix.free()
 
 
-@pytest.mark.parametrize("g", [4, 7])
+@pytest.mark.parametrize("g", [2, 4, 7, 8])
 def test_group_topk_variant(wi, g):
     """Group-shared retrieval: every query head of a kv head takes the top-k of the heads' summed
     scores (the same ids for all of them), with its own logits, estimate and retrieved-term
