@@ -33,7 +33,7 @@ def check(w, got, Q, K, V, KA=None, VA=None):
     return err.max()
 
 
-@pytest.mark.parametrize("g,kv", [(1, 1), (4, 2), (7, 1), (8, 1)])
+@pytest.mark.parametrize("g,kv", [(1, 1), (2, 2), (3, 1), (4, 2), (5, 1), (6, 2), (7, 1), (8, 1)])
 def test_dense_parity_group_sizes(wi, g, kv):
     w = small(n_ctx=4096, seg_len=1024, clusters_per_seg=64, iters=2, n_q_heads=g * kv, n_kv_heads=kv,
               budget_k=6, seed=3 + g)
