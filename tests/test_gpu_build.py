@@ -169,6 +169,15 @@ def test_seeded_build_parity_ragged_steady(wi):
     seeded_build_case(wi, w)
 
 
+@pytest.mark.parametrize("seg,cs", [(128, 16), (256, 32), (1024, 128)])
+def test_seeded_build_parity_small_geometries(wi, seg, cs):
+    """The smallest segment and cluster counts the configuration admits (128-token segments, 16
+    clusters: 8 tokens per cluster, SIMT assignment) and two tensor-core ones, many segments each."""
+    w = small(batch=1, layers=2, n_q_heads=4, n_kv_heads=2, n_ctx=16 * seg, seg_len=seg, clusters_per_seg=cs,
+              iters=2, budget_k=4, seed=84 + cs)
+    seeded_build_case(wi, w)
+
+
 def test_default_build_invariants_and_quality(wi):
     """Full default build (10 rounds from the default seeds) on the tiny workload:
     invariants of the index, and a clustering objective within 1% of the oracle's."""

@@ -80,6 +80,15 @@ def test_decode_parity_group_sizes(wi, g):
     assert run_case(wi, w) < 1e-4
 
 
+@pytest.mark.parametrize("seg,cs", [(128, 16), (256, 32)])
+def test_decode_parity_small_geometries(wi, seg, cs):
+    """128- and 256-token segments with 16 and 32 clusters (the smallest the configuration admits):
+    many segments, few tokens per cluster, a budget of a fifth of the clusters."""
+    w = small(batch=2, n_q_heads=8, n_kv_heads=2, n_ctx=32 * seg, seg_len=seg, clusters_per_seg=cs, iters=2,
+              budget_k=(32 * cs) // 5, seed=40 + cs)
+    assert run_case(wi, w, steps=2, append=True) < 1e-4
+
+
 @pytest.mark.parametrize("g", [3, 5, 8])
 def test_decode_parity_group_sizes_multi_unit(wi, g):
     """The odd group sizes with several units and an appending step."""
