@@ -19,6 +19,8 @@ READING below:
     so the three zones partition the context;
   * centroid initialisation: the first token of each stride-(S/C_s) block of
     the segment, normalised and rounded to bf16;
+  * a zero vector normalises to zero (a key of norm 0 adds nothing to a
+    centroid sum; a zero seed or a zero sum gives the zero centroid);
   * spherical k-means on unit-normalised keys; centroids are rounded to bf16
     before every assignment; ties go to the lowest centroid id; empty clusters
     keep their centroid; the index keeps the T-th assignment;
@@ -89,7 +91,11 @@ def budget_k(n_clusters: int, p: IndexParams) -> int:
 # ------------------------------------------------------ spherical k-means ----
 
 def _unit_rows(x: np.ndarray) -> np.ndarray:
-    return x / np.linalg.norm(x, axis=1, keepdims=True)
+    """Rows scaled to unit length.  READING (pages silent): a zero row has no direction and stays
+    zero, so a key of norm 0 adds nothing to a spherical sum, and a zero seed or a zero sum gives
+    the zero centroid (which scores 0 against every key)."""
+    nrm = np.linalg.norm(x, axis=1, keepdims=True)
+    return np.divide(x, nrm, out=np.zeros_like(x), where=nrm > 0)
 
 
 def init_centroids(k_seg: np.ndarray, p: IndexParams) -> np.ndarray:

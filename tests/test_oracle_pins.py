@@ -301,6 +301,32 @@ def test_update_empty_cluster_keeps_previous_centroid():
         np.testing.assert_array_equal(c[j], oracle.bf16_round(u / np.linalg.norm(u)))
 
 
+def test_zero_keys_have_no_direction():
+    """A key of norm 0 adds nothing to its cluster's spherical sum: members {3 e0, 0} give e0
+    exactly, as {3 e0} alone; a cluster whose members are all zero, or whose unit vectors cancel
+    ({2 e1, -5 e1}), gets the zero centroid; a zero seed gives the zero centroid, which scores 0
+    against every key (so a key with all scores <= 0 ties at 0 and goes to the lowest such id)."""
+    e = np.eye(D)
+    k = np.stack([3 * e[0], np.zeros(D), np.zeros(D), 2 * e[1], -5 * e[1]])
+    a = np.array([0, 0, 1, 2, 2])
+    c_prev = oracle.bf16_round(np.ones((3, D)) / np.sqrt(D))
+    c = oracle.update(k, a, c_prev)
+    np.testing.assert_array_equal(c[0], e[0])
+    np.testing.assert_array_equal(c[1], np.zeros(D))
+    np.testing.assert_array_equal(c[2], np.zeros(D))
+    assert np.all(np.isfinite(c))
+    # segment 0, 2 e1, -e0-e1, 3 e2 with 2 clusters seeded at positions 0 and 2 (stride 2): the first seed
+    # is the zero key, so c0 = 0; c1 = bf16(-(e0 + e1)/sqrt 2) = -181/256 on axes 0 and 1.  Scores
+    # (K_i . c0, K_i . c1): 0 -> (0, 0), tie, 0; 2 e1 -> (0, -1.41), 0; -e0-e1 -> (0, 1.41), 1;
+    # 3 e2 -> (0, 0), tie, 0.
+    K = np.stack([np.zeros(D), 2 * e[1], -e[0] - e[1], 3 * e[2]])
+    p = IndexParams(seg_len=4, clusters_per_seg=2, iters=1, n_sink=0, local_window=0)
+    c0 = oracle.init_centroids(K, p)
+    np.testing.assert_array_equal(c0[0], np.zeros(D))
+    np.testing.assert_array_equal(c0[1], -(181 / 256) * (e[0] + e[1]))
+    assert list(oracle.assign(K, c0)) == [0, 0, 1, 0]
+
+
 def test_kmeans_second_round_centroid_hand_value():
     """Inside spherical_kmeans the second round's centroids come from the first round's
     assignment by the same spherical update.  Segment of 4 keys 3 e0, 0.5 e1, 2 e2, 4 e3 and
