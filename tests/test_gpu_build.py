@@ -134,9 +134,17 @@ def check_index(w, K, V, k_perm, v_perm, exp, ref, c_last):
         assert num <= 1e-5 * np.linalg.norm(ref[u]["valsum"][ne])
 
 
-def seeded_build_case(wi, w):
-    """Oracle clusters with T rounds; both sides then run the final round from the oracle's last centroids."""
+def seeded_build_case(wi, w, zero_rows=None):
+    """Oracle clusters with T rounds; both sides then run the final round from the oracle's last centroids.
+    zero_rows: (unit, position) pairs whose key is set to zero on both sides first."""
     k, v, q, K, V, Q = gen(w)
+    if zero_rows:
+        shape = k.shape
+        k = k.copy().reshape(w.units, w.n_ctx, 128)
+        for u, pos in zero_rows:
+            k[u, pos] = 0
+        k = k.reshape(shape)
+        K = oracle.bf16_from_bits(k).reshape(w.units, w.n_ctx, 128)
     p = params_of(w)
     full = oracle.build_index(K, V, p)
     c_last = seg_centroids(full, w.iters - 1)
@@ -178,6 +186,17 @@ def test_seeded_build_parity_small_geometries(wi, seg, cs, nseg):
     w = small(batch=1, layers=2, n_q_heads=4, n_kv_heads=2, n_ctx=nseg * seg, seg_len=seg, clusters_per_seg=cs,
               iters=2, budget_k=4, seed=84 + cs)
     seeded_build_case(wi, w)
+
+
+def test_seeded_build_parity_zero_keys(wi):
+    """Keys of norm 0 (padding-like rows): seed positions, clustered positions and a sink.  They add
+    nothing to a centroid's sum, a zero seed gives the zero centroid, every score against it is 0."""
+    w = small(batch=1, n_q_heads=4, n_kv_heads=2, n_ctx=4096, seg_len=1024, clusters_per_seg=64, iters=3,
+              budget_k=4, seed=88)
+    rng = np.random.default_rng(88)
+    rows = [(u, p) for u in range(w.units) for p in (0, 16, 1024 + 32, 2048 + 5 * 16)]       # sink and seeds
+    rows += [(u, int(p)) for u in range(w.units) for p in rng.choice(np.arange(8, 4000), 60, replace=False)]
+    seeded_build_case(wi, w, zero_rows=rows)
 
 
 def test_default_build_invariants_and_quality(wi):
@@ -223,7 +242,35 @@ def test_default_seeds_match_oracle_init(wi, shape):
     """k_init_centroids (the centroids of the first round when none are given) element by
     element against oracle.init_centroids, within one bf16 step (fp32 vs float64 norm)."""
     w = small(batch=2, layers=2, n_q_heads=4, n_kv_heads=2, iters=1, budget_k=4, seed=83, **shape)
+    default_seeds_case(wi, w)
+
+
+def test_default_seeds_zero_keys(wi):
+    """Keys of norm 0 at seed positions give zero centroids, exactly; a zero key ties every centroid
+    at score 0 and goes to the segment's first; the one-round build still follows the oracle."""
+    w = small(batch=1, n_q_heads=4, n_kv_heads=2, n_ctx=4096, seg_len=1024, clusters_per_seg=64, iters=1,
+              budget_k=4, seed=86)
+    stride = w.seg_len // w.clusters_per_seg
+    rng = np.random.default_rng(86)
+    rows = [(u, s * w.seg_len + j * stride) for u in range(w.units) for s in range(w.n_segments)
+            for j in (0, 3, 17, w.clusters_per_seg - 1)]
+    rows += [(u, int(p)) for u in range(w.units) for p in rng.choice(w.n_ctx, 80, replace=False)]
+    c = default_seeds_case(wi, w, zero_rows=rows)
+    for u, pos in rows:
+        s, j = divmod(pos, w.seg_len)
+        if j % stride == 0:
+            assert not c[u, s, j // stride].any(), (u, pos)
+
+
+def default_seeds_case(wi, w, zero_rows=()):
     k, v, q, K, V, Q = gen(w)
+    if zero_rows:
+        shape = k.shape
+        k = k.copy().reshape(w.units, w.n_ctx, 128)
+        for u, pos in zero_rows:
+            k[u, pos] = 0
+        k = k.reshape(shape)
+        K = oracle.bf16_from_bits(k).reshape(w.units, w.n_ctx, 128)
     p = params_of(w)
     cfg = wi.config_from_workload(w)
     c = torch.empty((w.units, w.n_segments, w.clusters_per_seg, 128), dtype=torch.int16, device=DEV)
@@ -247,6 +294,7 @@ def test_default_seeds_match_oracle_init(wi, shape):
         dis = compare_assignment(a_gpu, a_ref, K[u], lambda s: ref[u, s], w.seg_len, w.clusters_per_seg)
         assert dis <= 1e-3 * (w.n_ctx - w.n_sink - w.local_window)
     ix.free()
+    return got
 
 
 @pytest.mark.parametrize("cs,base,seg", [(512, 128, 1024), (256, 64, 1024), (64, 16, 1024), (48, 16, 768)])

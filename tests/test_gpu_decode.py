@@ -80,6 +80,21 @@ def test_decode_parity_group_sizes(wi, g):
     assert run_case(wi, w) < 1e-4
 
 
+def test_decode_parity_zero_keys(wi):
+    """Keys of norm 0 throughout the context (steady and clustered), with the oracle's index."""
+    w = small(batch=1, n_q_heads=8, n_kv_heads=2, n_ctx=4096, seg_len=1024, clusters_per_seg=64, iters=2,
+              budget_k=6, seed=89)
+    k, v, q, K, V, Q = gen(w)
+    rng = np.random.default_rng(89)
+    shape = k.shape
+    k = k.copy().reshape(w.units, w.n_ctx, 128)
+    for u in range(w.units):
+        k[u, rng.choice(w.n_ctx, 300, replace=False)] = 0
+        k[u, :2] = 0                       # two sinks
+        k[u, w.n_ctx - 5:] = 0             # the window's last rows
+    assert run_case(wi, w, kv=(k.reshape(shape), v)) < 1e-4
+
+
 @pytest.mark.parametrize("seg,cs", [(128, 16), (256, 32)])
 def test_decode_parity_small_geometries(wi, seg, cs):
     """128- and 256-token segments with 16 and 32 clusters (the smallest the configuration admits):
