@@ -172,8 +172,15 @@ def cpu_baseline(w, k, v, budget_s=15.0):
         step += 1
     dt = time.perf_counter() - t0
     steps_equiv = heads / (w.units * w.group)
+    # the build, for context: one segment-unit (one segment of one kv head, every round), timed once
+    t0 = time.perf_counter()
+    oracle.build_unit_index(K[0][:w.seg_len], V[0][:w.seg_len], p10)
+    tb = time.perf_counter() - t0
     return {"value": steps_equiv / dt * w.batch * w.layers, "unit": UNIT, "cores": blas_threads(),
             "kind": "oracle",
+            "build": {"segment_units_per_s": 1.0 / tb, "seconds": tb,
+                      "sample": f"one segment-unit ({w.seg_len} tokens, {w.clusters_per_seg} clusters, "
+                                f"{w.iters} rounds)"},
             "sample": f"{step} full decode steps ({heads} query heads) of {w.name} in {dt:.1f} s; the oracle index "
                       f"is a one-round k-means index built before timing"}
 
@@ -303,12 +310,14 @@ class Timer:
 
     def __init__(self, torch, stream):
         self.torch, self.stream = torch, stream
+        self.calls = {}  # id(graph) -> calls of fn captured in it
 
     def graph(self, fn, n):
         g = self.torch.cuda.CUDAGraph()
         with self.torch.cuda.graph(g, stream=self.stream):
             for s in range(n):
                 fn(s)
+        self.calls[id(g)] = n
         return g
 
     def replay(self, graphs):
@@ -322,6 +331,19 @@ class Timer:
             e1.record(self.stream)
         self.stream.synchronize()
         return e0.elapsed_time(e1)
+
+    def replay_each(self, graphs, out):
+        """Replay `graphs` in order with an event after each; appends (milliseconds, graph) per graph
+        to `out` (a list, so that a thread can fill it)."""
+        torch = self.torch
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
+        with torch.cuda.stream(self.stream):
+            ev[0].record(self.stream)
+            for i, g in enumerate(graphs):
+                g.replay()
+                ev[i + 1].record(self.stream)
+        self.stream.synchronize()
+        out.extend((ev[i].elapsed_time(ev[i + 1]), g) for i, g in enumerate(graphs))
 
     def steps_plan(self, fn, steps, chunk):
         """Graphs covering exactly `steps` calls of fn (chunks of `chunk`), each replayed once untimed."""
@@ -765,7 +787,8 @@ def main():
     # sampler runs inside that window
     import threading
     soak = max(1, int(math.ceil(1.6 / max(d["ms"] / 1e3, 1e-6))))
-    th = threading.Thread(target=timer.replay, args=(d["graphs"] * soak,))
+    soak_ms = []
+    th = threading.Thread(target=timer.replay_each, args=(d["graphs"] * soak, soak_ms))
     th.start()
     time.sleep(0.05)
     with ClockSampler(local) as clocks:
@@ -773,6 +796,11 @@ def main():
     th.join()
     ms_per_step = ms / K
     value = job_value(world, K, w.batch, w.layers, ms / 1e3)
+    # spread of the step time: each graph replay of the clock-sampling window gives its mean step time
+    per_step_us = sorted(1e3 * t / L for t, g in soak_ms if timer.calls[id(g)] == L)
+    step_dist = {"p10": float(np.percentile(per_step_us, 10)), "median": float(np.median(per_step_us)),
+                 "p90": float(np.percentile(per_step_us, 90)), "samples": len(per_step_us), "unit": "us",
+                 "over": f"mean step time of each {L}-step graph replay in the clock-sampling window"}
     step_bytes = d["step_bytes"]
 
     # e2e: host buffers through the C ABI, copies inside the timed region
@@ -846,6 +874,7 @@ def main():
             "dtype": "bf16", "accumulate": "fp32", "data": "synthetic",
             "config": line_cfg,
             "roofline": roofline_of(d, w, hbm, peak_kind),
+            "step_us_dist": step_dist,
             "step_hbm_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
             "step_frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / hbm,
             "step_bytes": step_bytes,
