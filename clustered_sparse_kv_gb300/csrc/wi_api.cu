@@ -274,6 +274,11 @@ int alloc_index(wi_index* ix, cudaStream_t st) {
   // estimation CTAs that fit in one wave go first, so their stream overlaps the top-k CTAs
   const int ef = env_int("WI_ESTIMATE_FIRST", -1);
   b.est_first = ef >= 0 ? (ef != 0) : ((size_t)U * pe < (size_t)sms);
+  // when the top-k and estimation CTAs all fit in one wave, the top-k chain is the step's critical
+  // path and its loads queue behind the estimation stream: two stages in flight per estimation CTA
+  // (instead of three) still stream the value sums within the top-k's time
+  const int esd = env_int("WI_ESTIMATE_DEPTH", 0);
+  b.es_depth = esd == 2 || esd == 3 ? esd : ((size_t)U * (G + pe) <= (size_t)sms ? 2 : 3);
   // exact attention: (splits + 1 steady CTA) per head.  Few heads: fill two CTAs per SM in one wave
   // (the step is a latency chain); many heads: about two waves of split CTAs, so that the heads'
   // unequal row counts balance across the SMs

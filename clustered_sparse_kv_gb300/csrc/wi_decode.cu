@@ -306,7 +306,7 @@ constexpr size_t es_smem() {
 template <int G, typename VT, int GK>
 __device__ void estimate_role(unsigned char* raw, const VT* __restrict__ valsum, const int* __restrict__ cnt,
                               const uint32_t* __restrict__ scores, float* __restrict__ part, int C, int u, int p,
-                              int P, float lam, int* err) {
+                              int P, float lam, int depth, int* err) {
   using HG = HeadGeo<G>;
   EsStage<VT>* st = reinterpret_cast<EsStage<VT>*>(raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(raw + sizeof(EsStage<VT>) * kEsStages);
@@ -351,13 +351,20 @@ __device__ void estimate_role(unsigned char* raw, const VT* __restrict__ valsum,
         const int j0 = c0 + it * kSTile, nj = min(kSTile, c1 - j0);
         for (int h = 0; h < G; ++h) bulk_g2s(st[s].sc[h], scores + ((size_t)u * GK + h) * C + j0, nj * 4, &full[s]);
       };
-      const int pre = min(ntile, kEsStages);
+      // at most `depth` tiles in flight (the ring has kEsStages slots): tile it is issued once tile
+      // it - depth has been consumed
+      depth = depth == 2 ? 2 : kEsStages;
+      const int pre = min(ntile, depth);
       for (int it = 0; it < pre; ++it) issue_index(it);
       pdl_wait();
       for (int it = 0; it < pre; ++it) issue_scores(it);
       int issued = pre;
       for (int it = pre; it < ntile; ++it) {
         const int s = it % kEsStages, r = it / kEsStages;
+        if (depth < kEsStages) {
+          const int od = it - depth;  // phase (od / kEsStages) of its slot completes when it is consumed
+          if (!mbar_wait(&empty[od % kEsStages], (od / kEsStages) & 1, err)) { *s_abort = 1; break; }
+        }
         if (!mbar_wait(&empty[s], (r - 1) & 1, err)) { *s_abort = 1; break; }
         issue_index(it);
         issue_scores(it);
@@ -542,6 +549,7 @@ struct TopkArgs {
   int* err;
   int U, G, C, kmax, NS, PE, n_sink, W, P1, seg_len;
   int est_first;  // the estimation CTAs take the first block indices (they start before the top-k CTAs)
+  int es_depth;   // estimation stages in flight per CTA (2 or kEsStages)
   float lam;
 };
 
@@ -1111,7 +1119,7 @@ __global__ void __launch_bounds__(kSThreads, 1) k_select_estimate(TopkArgs a) {
   } else {
     const int e = a.est_first ? bi : bi - nsel;
     estimate_role<G, VT, G + (GRP ? 1 : 0)>(se_raw, static_cast<const VT*>(a.valsum), a.cnt, a.scores, a.part1,
-                                            a.C, e / a.PE, e % a.PE, a.PE, a.lam, a.err);
+                                            a.C, e / a.PE, e % a.PE, a.PE, a.lam, a.es_depth, a.err);
   }
 }
 
@@ -1910,6 +1918,7 @@ cudaError_t launch_g(const WiGeom& g, const WiDecodeBufs& b, const void* qv, flo
   t.lam = lam;
   t.n_sink = g.n_sink;
   t.est_first = b.est_first;
+  t.es_depth = b.es_depth;
   if (mask & 2u) e = launch_select<G>(g, b, t, st);
   if (e != cudaSuccess || (e = mark(ev, 2, st)) != cudaSuccess) return e;
   ExactArgs a;

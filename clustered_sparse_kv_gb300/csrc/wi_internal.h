@@ -133,6 +133,7 @@ struct WiDecodeBufs {
   int p1;                 // k_scores CTAs per unit
   int p_es;               // estimation CTAs per unit (= estimation partials per head)
   int est_first;          // the select/estimate launch starts its estimation CTAs first
+  int es_depth;           // estimation stages in flight per CTA (2 or 3)
   int nsplit;             // exact_merge CTAs per head over the selected rows (plus one for steady rows)
   int d3_rows;            // exact_merge stage height: 32 (one wave of CTAs) or 64 rows
   WiTierDev tier;         // host memory tier (tier.on == 0: none)

@@ -221,8 +221,10 @@ int wi_index_shape(const wi_index* ix, int* units, int* clusters, int* k_max, in
  * WI_ESTIMATE_FIRST (0 or 1: the estimation CTAs before the top-k CTAs in
  * their shared launch; default: when they fit in one wave), WI_D3_STAGE_ROWS
  * (32 or 64: rows per shared-memory stage of the exact-attention CTAs;
- * default 32 when all of them are resident at once, else 64), read when the
- * index is made, override the defaults.  Results do not depend on the
+ * default 32 when all of them are resident at once, else 64) and
+ * WI_ESTIMATE_DEPTH (2 or 3: value-sum tiles in flight per estimation CTA;
+ * default 2 when the top-k and estimation CTAs fit in one wave, else 3),
+ * read when the index is made, override the defaults.  Results do not depend on the
  * layout beyond float rounding order.  Any output pointer may be NULL.
  */
 int wi_decode_layout(const wi_index* ix, int* score_ctas, int* estimate_ctas, int* exact_splits);
