@@ -375,6 +375,32 @@ def test_select_estimate_block_orders(wi, monkeypatch, est_first, pe):
     ix.free()
 
 
+@pytest.mark.parametrize("pe", [1, 2])
+def test_estimation_depth_does_not_change_results(wi, monkeypatch, pe):
+    """Two or three value-sum tiles in flight per estimation CTA (four and two tiles per CTA here):
+    the same bits out, and the oracle's output."""
+    w = small(batch=1, n_q_heads=8, n_kv_heads=2, n_ctx=8192, seg_len=1024, clusters_per_seg=64, iters=2,
+              budget_k=12, seed=7)
+    k, v, q, K, V, Q = gen(w)
+    p = params_of(w)
+    idx = oracle.build_index(K, V, p)
+    monkeypatch.setenv("WI_ESTIMATE_CTAS_PER_UNIT", str(pe))
+    outs = []
+    for depth in (2, 3):
+        monkeypatch.setenv("WI_ESTIMATE_DEPTH", str(depth))
+        ix = wi.WaveIndex.adopt(wi.config_from_workload(w), dev16(k), dev16(v), *index_arrays(idx))
+        outs.append([ix.decode(dev16(kvsynth.queries(w, step=t))).clone() for t in range(2)])
+        torch.cuda.synchronize()
+        ix.check()
+        ix.free()
+    for t in range(2):
+        assert torch.equal(outs[0][t], outs[1][t]), t
+        Qt = oracle.bf16_from_bits(kvsynth.queries(w, step=t)).reshape(w.units, w.group, 128)
+        ref = oracle.decode(Qt, K, V, idx, p, w.group)
+        err = rel_l2(outs[0][t].cpu().numpy().reshape(w.units, w.group, 128).astype(np.float64), ref)
+        assert err.max() <= OUT_REL_L2, (t, err.max())
+
+
 def _bf16_valsum_index(idx):
     """The bf16 value-sum variant's definition: the stored fp32 value sums rounded to bf16."""
     return [{**d, "valsum": oracle.bf16_round(oracle.fp32_round(d["valsum"]))} for d in idx]
