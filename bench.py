@@ -194,26 +194,25 @@ def run_reference(args, w, rank, world):
     K, V, idx, p0 = oracle_setup(w, k, v)
     p = oracle.IndexParams(seg_len=w.seg_len, clusters_per_seg=w.clusters_per_seg, iters=w.iters, n_sink=w.n_sink,
                            local_window=w.local_window, budget_frac=w.budget_frac, budget_k=w.budget_k)
-    # one step = one query head of one unit (1/32 of a decode step), bounded to ~2 min in total
+    # one step of this arm = one unit's decode (its G query heads in one oracle call, 1/U of a decode
+    # step), as in the CPU baseline of the main arm; bounded to ~2 min in total
     t_one = time.perf_counter()
-    q = kvsynth.queries(w, step=0)
-    Q = oracle.bf16_from_bits(q).reshape(w.units, w.group, 128)
-    oracle.decode_unit(Q[0][:1], K[0], V[0], idx[0], p)
+    Q = oracle.bf16_from_bits(kvsynth.queries(w, step=0)).reshape(w.units, w.group, 128)
+    oracle.decode_unit(Q[0], K[0], V[0], idx[0], p)
     t_one = time.perf_counter() - t_one
     steps = min(args.steps, max(1, int(120.0 / max(t_one, 1e-4))))
     for s in range(args.warmup):
-        oracle.decode_unit(Q[s % w.units][:1], K[s % w.units], V[s % w.units], idx[s % w.units], p)
+        oracle.decode_unit(Q[s % w.units], K[s % w.units], V[s % w.units], idx[s % w.units], p)
     t0 = time.perf_counter()
     for s in range(steps):
-        u, h = (s // w.group) % w.units, s % w.group
-        if h == 0 and u == 0:
-            Q = oracle.bf16_from_bits(kvsynth.queries(w, step=s)).reshape(w.units, w.group, 128)
-        oracle.decode_unit(Q[u][h:h + 1], K[u], V[u], idx[u], p)
+        u = s % w.units
+        if u == 0:
+            Q = oracle.bf16_from_bits(kvsynth.queries(w, step=s // w.units)).reshape(w.units, w.group, 128)
+        oracle.decode_unit(Q[u], K[u], V[u], idx[u], p)
     dt = time.perf_counter() - t0
-    per_step = w.units * w.group
-    value = steps / per_step / dt * w.batch * w.layers
-    sample = (f"{steps} query-head decodes (1/{per_step} of a step each) of {w.name}; one-round k-means oracle "
-              f"index built before timing")
+    value = steps / w.units / dt * w.batch * w.layers
+    sample = (f"{steps} unit decodes ({w.group} query heads each, 1/{w.units} of a step) of {w.name}; "
+              f"one-round k-means oracle index built before timing")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": steps, "warmup": args.warmup, "ms_per_step": 1000.0 / value, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
