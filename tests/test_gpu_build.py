@@ -178,11 +178,12 @@ def test_seeded_build_parity_ragged_steady(wi):
 
 
 @pytest.mark.parametrize("seg,cs,nseg", [(128, 16, 16), (256, 32, 16), (1024, 128, 16), (768, 384, 4),
-                                         (3968, 496, 2)])
+                                         (3968, 496, 2), (16384, 512, 2)])
 def test_seeded_build_parity_small_geometries(wi, seg, cs, nseg):
     """The smallest segment and cluster counts the configuration admits (128-token segments, 16
-    clusters: 8 tokens per cluster), a tensor-core one, and large cluster counts outside the
-    tensor-core set (384, 496: the SIMT assignment), several segments each."""
+    clusters: 8 tokens per cluster), a tensor-core one, large cluster counts outside the
+    tensor-core set (384, 496: the SIMT assignment), and the longest segment admitted (16384 tokens),
+    several segments each."""
     w = small(batch=1, layers=2, n_q_heads=4, n_kv_heads=2, n_ctx=nseg * seg, seg_len=seg, clusters_per_seg=cs,
               iters=2, budget_k=4, seed=84 + cs)
     seeded_build_case(wi, w)

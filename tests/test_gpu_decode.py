@@ -206,6 +206,17 @@ def test_topk_large_cluster_count(wi, n_ctx, budget):
     assert run_case(wi, w, strict_ids=False) < 1e-4
 
 
+def test_topk_cluster_count_at_the_key_cache_limit(wi):
+    """C = 32768, the most clusters whose keys the top-k keeps in shared memory (k = 590, above the
+    list capacity), and the same count with every score tied (the radix path over the cached keys)."""
+    w = small(n_ctx=65536, seg_len=1024, clusters_per_seg=512, iters=1, n_q_heads=4, budget_k=0,
+              budget_frac=0.018, seed=37)
+    assert w.clusters == 32768
+    assert run_case(wi, w, strict_ids=False) < 1e-4
+    w = w.with_(budget_k=100, seed=38)
+    assert run_case(wi, w, idx=tied_index(w, lambda j: 0), strict_ids=True) < 1e-4
+
+
 def test_topk_large_cluster_count_ties(wi):
     """Every score tied at C = 65536 (more ties than ranking threads: the radix path over keys read
     from global memory) and two score levels at C = 40960; the selection must equal the oracle's."""
@@ -218,6 +229,13 @@ def test_topk_large_cluster_count_ties(wi):
 def test_decode_large_budget(wi):
     # k above the top-k's list capacity (512): the selection goes through per-chunk bit masks
     w = small(n_ctx=16384, seg_len=1024, clusters_per_seg=128, iters=2, n_q_heads=4, budget_k=700, seed=33)
+    assert run_case(wi, w, strict_ids=False) < 1e-4
+
+
+def test_decode_largest_budget(wi):
+    # k = 4096, the largest budget the configuration admits, over C = 8192 clusters
+    w = small(n_ctx=65536, seg_len=1024, clusters_per_seg=128, iters=1, n_q_heads=4, budget_k=4096, seed=39)
+    assert w.clusters == 8192
     assert run_case(wi, w, strict_ids=False) < 1e-4
 
 
