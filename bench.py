@@ -180,7 +180,9 @@ def cpu_baseline(w, k, v, budget_s=15.0):
             "kind": "oracle",
             "build": {"segment_units_per_s": 1.0 / tb, "seconds": tb,
                       "sample": f"one segment-unit ({w.seg_len} tokens, {w.clusters_per_seg} clusters, "
-                                f"{w.iters} rounds)"},
+                                f"{w.iters} rounds)",
+                      "extrapolated_build_s": {n: kvsynth.get_workload(n).units * kvsynth.get_workload(n).n_segments
+                                               * tb for n in [w.name] + EXTRA_CONFIGS}},
             "sample": f"{step} full decode steps ({heads} query heads) of {w.name} in {dt:.1f} s; the oracle index "
                       f"is a one-round k-means index built before timing"}
 
