@@ -219,8 +219,10 @@ __global__ void __launch_bounds__(32 * kSortWarps) k_segment_sort(const int32_t*
 // One warp per cluster: c_j = bf16(u_j / |u_j|), u_j = sum over members (in
 // position order) of K_i * (1/|K_i|), the norm taken in fp32 from the row
 // itself.  Eight member rows in flight per warp.  Empty clusters keep c_j.
+// The kernel waits on its dependent slot-then-row loads, so resident warps
+// set its speed: 40 registers let six blocks (48 warps) share an SM.
 constexpr int kUpdRows = 8;
-__global__ void __launch_bounds__(256) k_centroid_update(const bf16* __restrict__ K, const int* __restrict__ seg_counts,
+__global__ void __launch_bounds__(256, 6) k_centroid_update(const bf16* __restrict__ K, const int* __restrict__ seg_counts,
                                                          const int* __restrict__ seg_offsets,
                                                          const int* __restrict__ slots, bf16* __restrict__ chat,
                                                          int total, int S, int Cs, int nseg, long long n) {
@@ -239,12 +241,15 @@ __global__ void __launch_bounds__(256) k_centroid_update(const bf16* __restrict_
 #pragma unroll
     for (int i = 0; i < kUpdRows; ++i)
       w[i] = t0 + i < m ? ldg_u2(Kb + (long long)sl[t0 + i] * WI_D) : make_uint2(0u, 0u);
-    // the eight rows' squared norms in one warp transpose-reduction (lanes 4i..4i+3 end with row i's)
-    float x[kUpdRows][4], ss[kUpdRows];
+    // the eight rows' squared norms in one warp transpose-reduction (lanes 4i..4i+3 end with row i's);
+    // the rows stay packed across it and are unpacked again for the sums (a few integer operations),
+    // so the unpacked values never hold 32 registers and more warps fit on an SM
+    float ss[kUpdRows];
 #pragma unroll
     for (int i = 0; i < kUpdRows; ++i) {
-      unpack_bf16x4(w[i], x[i]);
-      ss[i] = x[i][0] * x[i][0] + x[i][1] * x[i][1] + x[i][2] * x[i][2] + x[i][3] * x[i][3];
+      float x[4];
+      unpack_bf16x4(w[i], x);
+      ss[i] = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
     }
     const float sq = transpose_reduce<kUpdRows>(ss);
     const float ivl = sq > 0.f ? 1.0f / sqrtf(sq) : 0.f;
@@ -252,8 +257,11 @@ __global__ void __launch_bounds__(256) k_centroid_update(const bf16* __restrict_
     for (int i = 0; i < kUpdRows; ++i) {
       const float iv = __shfl_sync(0xffffffffu, ivl, 4 * i);
       if (t0 + i < m) {  // warp-uniform
+        uint32_t lo = w[i].x, hi = w[i].y;
+        asm volatile("" : "+r"(lo), "+r"(hi));  // a fresh unpack: the first one is not kept alive
+        const float x[4] = {bf16_lo(lo), bf16_hi(lo), bf16_lo(hi), bf16_hi(hi)};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] = fmaf(x[i][e], iv, acc[e]);
+        for (int e = 0; e < 4; ++e) acc[e] = fmaf(x[e], iv, acc[e]);
       }
     }
   }
