@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(256) k_assign_simt(const bf16* __restrict__ K,
 }
 
 // Counting sort of one segment's clustered tokens by (cluster, position),
-// stable and in O(S): each of the 16 warps takes a contiguous chunk of the
+// stable and in O(S): each of the W warps takes a contiguous chunk of the
 // segment's positions; pass 1 counts per (warp, cluster) (match_any groups the
 // lanes of one cluster, whose leader adds the group's size); a scan turns the
 // counts into each warp's first slot per cluster (clusters in order, warps in
@@ -137,8 +137,9 @@ __global__ void __launch_bounds__(256) k_assign_simt(const bf16* __restrict__ K,
 // order and gives each lane its slot = that start + its rank among the lanes
 // of its cluster.  Outputs per segment-unit: counts [Cs], offsets [Cs+1]
 // (local slots), slots [S] (position relative to the segment start, in slot
-// order).
-constexpr int kSortWarps = 16;
+// order).  W = 32 when the segment-units fit in one wave (shorter chunks: the
+// sort's few CTAs are latency-bound), else 16 (more CTAs resident per SM).
+template <int kSortWarps>
 __global__ void __launch_bounds__(32 * kSortWarps) k_segment_sort(const int32_t* __restrict__ assign,
                                                                   int* __restrict__ seg_counts,
                                                                   int* __restrict__ seg_offsets,
@@ -398,12 +399,24 @@ cudaError_t wi_launch_assign(const WiGeom& g, const void* K, const void* chat, i
 
 cudaError_t wi_launch_segment_sort(const WiGeom& g, const int32_t* assign, int* seg_counts, int* seg_offsets,
                                    int* slots, int* err, cudaStream_t st) {
-  const size_t smem = sizeof(int) * ((size_t)(kSortWarps + 2) * g.Cs + 1 + 32 + (size_t)g.S);
-  static int smem_set[kWiSmemDevices] = {};
-  cudaError_t e = wi_ensure_smem(k_segment_sort, smem, smem_set);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  k_segment_sort<<<g.U * g.nseg, 32 * kSortWarps, smem, st>>>(assign, seg_counts, seg_offsets, slots, g.S, g.Cs,
-                                                              g.nseg, g.n, err);
+  const bool one_wave = (long long)g.U * g.nseg <= sms;
+  const int warps = one_wave ? 32 : 16;
+  const size_t smem = sizeof(int) * ((size_t)(warps + 2) * g.Cs + 1 + 32 + (size_t)g.S);
+  if (one_wave) {
+    static int smem_set[kWiSmemDevices] = {};
+    if ((e = wi_ensure_smem(k_segment_sort<32>, smem, smem_set)) != cudaSuccess) return e;
+    k_segment_sort<32><<<g.U * g.nseg, 32 * 32, smem, st>>>(assign, seg_counts, seg_offsets, slots, g.S, g.Cs,
+                                                            g.nseg, g.n, err);
+  } else {
+    static int smem_set[kWiSmemDevices] = {};
+    if ((e = wi_ensure_smem(k_segment_sort<16>, smem, smem_set)) != cudaSuccess) return e;
+    k_segment_sort<16><<<g.U * g.nseg, 32 * 16, smem, st>>>(assign, seg_counts, seg_offsets, slots, g.S, g.Cs,
+                                                            g.nseg, g.n, err);
+  }
   return cudaGetLastError();
 }
 
