@@ -11,6 +11,7 @@ import sys
 import pytest
 
 import oracle
+import oracle.bf16 as bf16_mod
 import oracle.wave_buffer as wb
 import oracle.wave_index as wi_mod
 import test_oracle_pins as pins
@@ -112,6 +113,36 @@ CASES = {
         wi_mod, "budget_k", "return int(math.ceil(p.budget_frac * n_clusters))",
         "return int(math.floor(p.budget_frac * n_clusters))",
         [pins.test_budget_matches_configured_counts]),
+    "bf16 rounding truncates": (
+        bf16_mod, "bf16_round", "np.rint(np.ldexp(m, 8))", "np.trunc(np.ldexp(m, 8))",
+        [pins.test_bf16_round_matches_torch_cast, pins.test_bf16_round_hand_values]),
+    "bf16 rounding keeps one bit too many": (
+        bf16_mod, "bf16_round", "return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)",
+        "return np.ldexp(np.rint(np.ldexp(m, 9)), e - 9)",
+        [pins.test_bf16_round_matches_torch_cast, pins.test_bf16_round_hand_values]),
+    "sinks not in the steady zone": (
+        wi_mod, "steady_positions", "lo = np.arange(min(p.n_sink, n))", "lo = np.arange(0)",
+        [pins.test_steady_zone_partition, lambda: pins.test_all_clusters_selected_is_full_attention(4)]),
+    "growth one segment early": (
+        wi_mod, "grown_segments", "return n_appended // p.seg_len",
+        "return (n_appended + p.local_window) // p.seg_len",
+        [pins.test_budget_counts_grown_clusters, pins.test_all_clusters_after_growth_is_full_attention,
+         pins.test_grown_segment_equals_build_of_that_segment_alone,
+         lambda: pins.test_window_keeps_between_w_and_w_plus_s_rows(300, 0)]),
+    "growth one append late": (
+        wi_mod, "grown_segments", "return n_appended // p.seg_len", "return max(n_appended - 1, 0) // p.seg_len",
+        [lambda: pins.test_window_keeps_between_w_and_w_plus_s_rows(8, 512),
+         lambda: pins.test_window_keeps_between_w_and_w_plus_s_rows(300, 512)]),
+    "grown segment taken from the window's end": (
+        wi_mod, "grow_unit_index", "pos = w0 + g * S + np.arange(S)", "pos = K_all.shape[0] - S + np.arange(S)",
+        [pins.test_grown_segment_equals_build_of_that_segment_alone, pins.test_all_clusters_after_growth_is_full_attention]),
+    "group retrieval by the first head's scores": (
+        wi_mod, "decode_unit", "select_topk(mu @ q_heads.sum(axis=0), nonempty, k)",
+        "select_topk(mu @ q_heads[0], nonempty, k)",
+        [pins.test_group_topk_variant_pins]),
+    "dense comparator without the appended rows": (
+        wi_mod, "full_attention", "if k_app is not None and k_app.shape[1] > 0:", "if False:",
+        [pins.test_full_attention_equals_wave_index_with_every_cluster_retrieved, pins.test_full_attention_closed_forms]),
     "merge rescales with the wrong sign": (
         wi_mod, "lse_merge", "Z = sum(z * math.exp(m - M) for m, z, _ in parts if m > -np.inf)",
         "Z = sum(z * math.exp(M - m) for m, z, _ in parts if m > -np.inf)",

@@ -594,3 +594,21 @@ def test_budget_counts_grown_clusters():
     _, info = oracle.decode_unit(Q, K, V, gi, p, KA, VA, details=True)
     C = gi["counts"].shape[0]
     assert len(info[0]["selected"]) == math.ceil(0.05 * C) == math.ceil(0.05 * (128 + 32))
+
+
+@pytest.mark.parametrize("W,appended", [(8, 0), (8, 247), (8, 248), (8, 600), (300, 0), (300, 211), (300, 512)])
+def test_window_keeps_between_w_and_w_plus_s_rows(W, appended):
+    """READING (decode-time growth): the local window never holds fewer than W rows nor W + S: an
+    append that would leave W + S rows turns the oldest S into a segment.  Checked on the zones the
+    decode uses: with one cluster retrieved, a head's exact rows are the sinks, the window and that
+    cluster's rows, and every clustered row belongs to the build or to a grown segment."""
+    S = 256
+    w, p, K, V, Q, KA, VA, K_all, V_all, idx = grown_case(n=2048, S=S, Cs=16, W=W, appended=appended, budget_k=1)
+    gi = oracle.grow_unit_index(idx, K_all, V_all, w.n_ctx, p)
+    _, info = oracle.decode_unit(Q, K, V, gi, p, KA, VA, details=True)
+    for h in range(Q.shape[0]):
+        (j,) = info[h]["selected"]
+        window = info[h]["exact_rows"] - p.n_sink - int(gi["counts"][j])
+        assert W <= window < W + S, (W, appended, window)
+    # the rows not in the steady zone are exactly the clustered ones
+    assert int(gi["counts"].sum()) == w.n_ctx + appended - p.n_sink - (W + appended % S)
