@@ -101,6 +101,10 @@ CASES = {
         wi_mod, "build_unit_index", "mu[ne] = bf16_round(ksum[ne] / counts[ne, None])",
         "mu[ne] = bf16_round(_unit_rows(ksum[ne]))",
         [lambda: pins.test_singleton_clusters_make_estimation_exact(3), pins.test_two_token_cluster_estimate_closed_form]),
+    "members listed in reverse position order": (
+        wi_mod, "build_unit_index", 'perm = idx[np.argsort(assignment[idx], kind="stable")]',
+        "perm = idx[np.lexsort((-idx, assignment[idx]))]",
+        [pins.test_index_conservation, pins.test_segments_are_clustered_independently]),
     "value sums of the keys": (
         wi_mod, "build_unit_index", "np.add.at(vsum, assignment[idx], V[idx])",
         "np.add.at(vsum, assignment[idx], K[idx])",
