@@ -445,6 +445,36 @@ def test_valsum_bf16_variant_imported_index(wi, g):
     ix.free()
 
 
+@pytest.mark.parametrize("g", [4, 7])
+def test_group_topk_with_bf16_value_sums(wi, g):
+    """Both variants at once: group-shared retrieval over an index whose value sums are read as
+    bf16, with appended tokens; parity with the oracle's group variant on the bf16-rounded sums."""
+    w = small(n_ctx=8192, seg_len=1024, clusters_per_seg=64, iters=2, n_q_heads=2 * g, n_kv_heads=2, budget_k=8,
+              seed=23)
+    k, v, q, K, V, Q = gen(w)
+    p = params_of(w)
+    idx = oracle.build_index(K, V, p)
+    T = 2
+    cfg = wi.config_from_workload(w, max_append=T)
+    cfg.valsum_bf16 = 1
+    cfg.group_topk = 1
+    ix = wi.WaveIndex.adopt(cfg, dev16(k), dev16(v), *index_arrays(idx))
+    ka, va = kvsynth.kv_cache(w, p0=w.n_ctx, p1=w.n_ctx + T)
+    KA = oracle.bf16_from_bits(ka).reshape(w.units, T, 128)
+    VA = oracle.bf16_from_bits(va).reshape(w.units, T, 128)
+    for t in range(T):
+        qb = kvsynth.queries(w, step=t)
+        out = ix.decode(dev16(qb), dev16(ka[:, :, :, t]), dev16(va[:, :, :, t]))
+        out = out.cpu().numpy().reshape(w.units, w.group, 128).astype(np.float64)
+        ix.check()
+        Qt = oracle.bf16_from_bits(qb).reshape(w.units, w.group, 128)
+        ref = oracle.decode(Qt, K, V, _bf16_valsum_index(idx), p, w.group, k_app=KA[:, :t], v_app=VA[:, :t],
+                            group_topk=True)
+        err = rel_l2(out, ref)
+        assert err.max() <= OUT_REL_L2, (t, err.max())
+    ix.free()
+
+
 def test_valsum_bf16_variant_built_index(wi):
     """The library's own build with the variant: the decode matches the oracle on the exported
     index with its value sums rounded to bf16."""
