@@ -475,6 +475,27 @@ def test_group_topk_with_bf16_value_sums(wi, g):
     ix.free()
 
 
+def test_valsum_bf16_with_64_row_stages(wi, monkeypatch):
+    """The bf16 value-sum instance of the exact kernel with 64-row stages (the layout of launches
+    in several waves), forced on a small index: parity with the oracle."""
+    w = small(n_ctx=8192, seg_len=1024, clusters_per_seg=64, iters=2, n_q_heads=8, n_kv_heads=2, budget_k=8,
+              seed=25)
+    k, v, q, K, V, Q = gen(w)
+    p = params_of(w)
+    idx = oracle.build_index(K, V, p)
+    monkeypatch.setenv("WI_D3_STAGE_ROWS", "64")
+    cfg = wi.config_from_workload(w)
+    cfg.valsum_bf16 = 1
+    ix = wi.WaveIndex.adopt(cfg, dev16(k), dev16(v), *index_arrays(idx))
+    qb = kvsynth.queries(w, step=0)
+    out = ix.decode(dev16(qb)).cpu().numpy().reshape(w.units, w.group, 128).astype(np.float64)
+    ix.check()
+    Qt = oracle.bf16_from_bits(qb).reshape(w.units, w.group, 128)
+    ref = oracle.decode(Qt, K, V, _bf16_valsum_index(idx), p, w.group)
+    assert rel_l2(out, ref).max() <= OUT_REL_L2
+    ix.free()
+
+
 def test_valsum_bf16_variant_built_index(wi):
     """The library's own build with the variant: the decode matches the oracle on the exported
     index with its value sums rounded to bf16."""

@@ -227,6 +227,31 @@ def test_tier_allocation_failure_leaves_the_index_usable(wi, monkeypatch):
     b.free()
 
 
+def test_tier_with_64_row_stages(wi, monkeypatch):
+    """The tier instance of the exact kernel with 64-row stages (the layout of launches in several
+    waves), forced: the same bits as the untiered index with the same stages, every step."""
+    monkeypatch.setenv("WI_D3_STAGE_ROWS", "64")
+    w = workload(47)
+    a, b, idx, K, V = pair(wi, w)
+    pages = w.n_ctx // PAGE
+    b.attach_tier(pages // 4, 64, async_rounds=False)
+    b.k.fill_(NAN16)
+    b.v.fill_(NAN16)
+    for t in range(6):
+        qd = dev16(kvsynth.queries(w, step=t // 2))
+        oa = a.decode(qd).clone()
+        ob = b.decode(qd).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob), t
+        b.tier_round()
+    st = b.tier_stats()
+    assert st["rows_from_cache"] > 0 and st["rows_from_host"] > 0
+    a.check()
+    b.check()
+    a.free()
+    b.free()
+
+
 @pytest.mark.parametrize("group_topk", [0, 1])
 def test_tier_host_buffers_and_group_retrieval(wi, group_topk):
     """The host-buffer entry point (query and output in page-locked host memory) and group-shared
