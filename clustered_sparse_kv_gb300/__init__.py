@@ -65,6 +65,7 @@ _SIGS = {
     "wi_kmeans_step_noalloc": [_cfgp, _vp, _vp, _vp, _vp, _vp],
     "wi_init_centroids": [_cfgp, _vp, _vp, _vp],
     "wi_check_device": [_vp],
+    "wi_selftest_wait_timeout": [_ip, _ip],
     "wi_profile_begin": [_vp, ctypes.c_int],
     "wi_index_build_stats": [_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), _ip],
     "wi_profile_read": [_vp, ctypes.POINTER(ctypes.c_double), _ip, ctypes.POINTER(ctypes.c_ulonglong)],
@@ -208,6 +209,13 @@ def wi_kmeans_step_noalloc(cfg: wi_config, k, centroids, assign, new_centroids, 
 
 def wi_check_device(ix: int):
     _check(lib.wi_check_device(ix))
+
+
+def wi_selftest_wait_timeout() -> dict:
+    """Run the kernels' bounded wait on a barrier nothing completes (test hook; about one second)."""
+    err, ret = ctypes.c_int(), ctypes.c_int()
+    _check(lib.wi_selftest_wait_timeout(ctypes.byref(err), ctypes.byref(ret)))
+    return {"device_error": err.value, "wait_returned": ret.value}
 
 
 WI_NUM_DECODE_KERNELS = 3

@@ -17,7 +17,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libwaveindex.so")
 
 SOURCES = ["wi_api.cu", "wi_build.cu", "wi_decode.cu", "wi_dense.cu", "wi_assign_tc.cu", "wi_noalloc.cu",
-           "wi_grow.cu", "wi_tier.cu"]
+           "wi_grow.cu", "wi_tier.cu", "wi_selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -305,6 +305,18 @@ int wi_index_build_stats(wi_index* ix, double* build_ms, double* assign_ms, int*
  * violation recorded by any kernel since the last call (WI_EDEVICE). */
 int wi_check_device(wi_index* ix);
 
+/* Test hook: the failure path of the kernels' bounded waits, run on purpose.
+ * Launches, on the current device, one kernel whose thread waits on a
+ * shared-memory mbarrier that nothing ever completes, through the same
+ * bounded wait the library's kernels use (it gives up after about 2^31 SM
+ * cycles, ~1 s, records the timeout bit 16 in the kernel's error word and
+ * returns), and synchronises the device.  On WI_OK, *device_error is the
+ * kernel's error word (16 when the wait gave up) and *wait_returned 1 when the
+ * wait returned without completion (2 if it had completed).  No fault, trap
+ * or endless loop; the context stays usable.  Host outputs; errors:
+ * WI_EINVAL (null pointer), WI_ENOMEM, WI_ECUDA. */
+int wi_selftest_wait_timeout(int* device_error, int* wait_returned);
+
 /*
  * Host memory tier: the wave buffer (summaries de/fr/zh section 2.B: a GPU
  * block cache of the KV blocks retrieval keeps returning to, LRU replacement

@@ -113,6 +113,7 @@ def test_calls_on_null_index(wi):
     assert wi.lib.wi_lru_round(None, None, 0, 0, None, None, None, None, None, None) == -1
     wi.lib.wi_lru_free(None)  # no-op
     wi.lib.wi_free(None)  # no-op
+    assert wi.lib.wi_selftest_wait_timeout(None, None) == -1   # checked before any device work
     cfg = good_cfg(wi)
     assert wi.lib.wi_kmeans_step(ctypes.byref(cfg), None, 16, 16, 16, None) == -1
     assert wi.lib.wi_kmeans_step(ctypes.byref(good_cfg(wi, head_dim=96)), 16, 16, 16, 16, None) == -1
