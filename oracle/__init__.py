@@ -24,7 +24,8 @@ Parity status per function (what pins it is in ``tests/test_oracle_pins.py``):
   grow_unit_index     pinned (a grown segment equals build_unit_index of
                               that segment alone; all clusters after growth
                               = textbook softmax; singleton grown clusters
-                              make the estimate exact)
+                              make the estimate exact; the window keeps W to
+                              W + S - 1 rows)
   full_attention      pinned (equals decode_unit with every cluster
                               retrieved; one row gives its value row;
                               identical keys give the mean value row;
@@ -37,6 +38,8 @@ Parity status per function (what pins it is in ``tests/test_oracle_pins.py``):
 Approximation quality against full attention on synthetic data: parity
 unpinned (the summaries claim accuracy only on RULER / Needle-in-a-Haystack
 with trained models).
+tests/test_oracle_mutations.py plants plausible slips in this package's source
+and requires each to turn one of those pins red.
 """
 from .bf16 import bf16_round, bf16_from_bits, bf16_to_bits, fp32_round  # noqa: F401
 from .wave_index import (  # noqa: F401
